@@ -1,0 +1,447 @@
+"""Benchmark of the spark2_5 decode attention block on GB300.
+
+One step = one decode of every layer of the workload for every sequence of its
+batch: RMSNorm + q_k_v_proj/g_proj, split + rope + cache write, split-K GQA
+attention, gate + o_proj + residual, per layer, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line.  ``value`` is decode tokens/s of the whole job (steps/s
+times the batch, summed over ranks) with every input resident in HBM; the
+weights and caches of several copies of the workload are rotated so the bytes
+a step reads are never in L2 from the step before.  ``e2e`` is the same metric
+through the public call with the step's input ``h`` copied from pinned host
+memory and the output read back every step.  ``roofline`` is for the kernel
+with the largest share of the step.  ``cpu_baseline`` (and ``--impl
+reference``) time the float64 CPU oracle on a bounded sample of the workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from decode_attention_block_gb300 import build_lib, synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "full+sliding_bf16_b1_pos700"
+METRIC = "decode attn-block steps/s & tokens/s; achieved HBM GB/s vs ~8 TB/s peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; the path shards by sequence, so
+# ranks run independent replicas and only the timing is reduced)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# bytes and peaks
+# ---------------------------------------------------------------------------
+
+def step_bytes(wl: synth.Workload) -> dict:
+    """Algorithmic HBM bytes of one step: every weight byte once, every KV row
+    a token attends to once (K and V).  h and out are not counted."""
+    w = wl.weight_bytes_per_layer()
+    q_dim, kv_dim, H, es = wl.n_q * wl.head_dim, wl.n_kv * wl.head_dim, wl.hidden, wl.elem_bytes
+    per = {"qkv_gate": 0, "split_rope": 0, "attention": 0, "gate_oproj": 0}
+    for li in range(len(wl.layers)):
+        per["qkv_gate"] += ((q_dim + 2 * kv_dim + wl.n_q) * H + H) * es
+        per["gate_oproj"] += H * q_dim * es
+        per["attention"] += sum(wl.rows_read(li, b) for b in range(wl.batch)) * wl.kv_row_bytes()
+    total = len(wl.layers) * w + per["attention"]
+    assert total == per["qkv_gate"] + per["gate_oproj"] + per["attention"]
+    return {"total": total, "per_kernel": per}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx = float(parts[1])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class Copy:
+    """One full set of a workload's inputs resident on the device."""
+
+    def __init__(self, wl, B, device, ring_geom):
+        self.layers = []
+        for li, spec in enumerate(wl.layers):
+            w = synth.make_weights(wl, li, device)
+            k, v = synth.make_cache(wl, li, device)
+            self.layers.append((spec, B.LayerWeights(**w), B.KvLayer(k, v, spec.ring_capacity)))
+        self.h = synth.make_h(wl, device)
+        self.buf = [torch.empty_like(self.h), torch.empty_like(self.h)]
+
+
+def run_step(B, geom, wl, cp, ws, stream):
+    cur = cp.h
+    for i, (spec, w, kv) in enumerate(cp.layers):
+        out = cp.buf[i % 2]
+        B.spark_attn_decode(geom, cur, w, kv, B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING,
+                            wl.positions, out, ws, stream)
+        cur = out
+    return cur
+
+
+def run_step_staged(B, geom, wl, cp, ws, bufs, stream, ev):
+    """The same work as run_step, launched stage by stage with CUDA events
+    around each kernel on the launching stream."""
+    cur = cp.h
+    for i, (spec, w, kv) in enumerate(cp.layers):
+        out = cp.buf[i % 2]
+        cls = B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING
+        ev.mark("qkv_gate", stream, lambda: B.spark_dbg_qkv_gate(geom, cur, w, bufs["qkvg"], stream))
+        ev.mark("split_rope", stream, lambda: B.spark_dbg_split_rope(geom, bufs["qkvg"], kv, cls, wl.positions,
+                                                                      bufs["q_rot"], stream))
+        ev.mark("attention", stream, lambda: B.spark_dbg_attention(geom, bufs["q_rot"], kv, cls, wl.positions,
+                                                                    bufs["a"], ws, 0, stream))
+        ev.mark("gate_oproj", stream, lambda: B.spark_dbg_gate_oproj(geom, bufs["a"], bufs["qkvg"], cur, w, out,
+                                                                      stream))
+        cur = out
+
+
+class KernelEvents:
+    def __init__(self):
+        self.pairs = {}
+
+    def mark(self, name, stream, launch):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        launch()
+        e.record(stream)
+        self.pairs.setdefault(name, []).append((s, e))
+
+    def avg_ms(self):
+        return {k: sum(s.elapsed_time(e) for s, e in v) / len(v) for k, v in self.pairs.items()}
+
+
+def bench_ours(args, wl, rank, local, world):
+    from decode_attention_block_gb300 import binding as B
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    build_lib.build()
+    B.load()
+    geom = B.spark_geom_default()
+    stream = torch.cuda.current_stream(device)
+    sb = step_bytes(wl)
+    l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
+    copies = args.copies or max(1, math.ceil(4 * l2 / sb["total"]))
+    cps = [Copy(wl, B, device, geom) for _ in range(copies)]
+    ws = B.make_workspace(geom, wl.batch, device)
+    H, q_dim = wl.hidden, wl.n_q * wl.head_dim
+    bufs = {"qkvg": torch.empty((wl.batch, q_dim + 2 * wl.n_kv * wl.head_dim + wl.n_q), device=device),
+            "q_rot": torch.empty((wl.batch, q_dim), device=device),
+            "a": torch.empty((wl.batch, q_dim), device=device)}
+    torch.cuda.synchronize()
+
+    # warm-up
+    for i in range(args.warmup):
+        run_step(B, geom, wl, cps[i % copies], ws, stream)
+    torch.cuda.synchronize()
+
+    steps = args.steps
+    if steps <= 0:   # auto: about two seconds of timed work
+        t0 = time.perf_counter()
+        for i in range(20):
+            run_step(B, geom, wl, cps[i % copies], ws, stream)
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 20
+        steps = int(min(20000, max(50, 2.0 / max(per, 1e-6))))
+
+    # timed region: exactly `steps` steps
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(steps):
+            run_step(B, geom, wl, cps[i % copies], ws, stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = sampler.summary()
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world, device)
+    ms_per_step = ms_total / steps
+    kernels_per_step = 4 * len(wl.layers)
+
+    # per-kernel durations: the same steps launched stage by stage with events
+    ev = KernelEvents()
+    ksteps = min(steps, max(20, 2000 // max(1, len(wl.layers))))
+    for i in range(ksteps):
+        run_step_staged(B, geom, wl, cps[i % copies], ws, bufs, stream, ev)
+    torch.cuda.synchronize()
+    kavg = ev.avg_ms()   # ms per launch
+    launches_per_step = {k: len(wl.layers) for k in kavg}
+    share = {k: kavg[k] * launches_per_step[k] for k in kavg}
+    tot = sum(share.values())
+    top = max(share, key=share.get)
+    per_launch_bytes = sb["per_kernel"][top] / len(wl.layers)
+    peaks = measured_peaks()
+    achieved = per_launch_bytes / (kavg[top] * 1e-3) / 1e9
+
+    # end to end through the public call: h from pinned host, out read back
+    h_host = [synth.make_h(wl, "cpu").pin_memory() for _ in range(2)]
+    out_host = torch.empty((wl.batch, H), dtype=torch.float32).pin_memory()
+    e2e_steps = max(10, min(steps, 2000))
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        cp = cps[i % copies]
+        cp.h.copy_(h_host[i % 2], non_blocking=True)
+        res = run_step(B, geom, wl, cp, ws, stream)
+        out_host.copy_(res, non_blocking=True)
+        torch.cuda.current_stream(device).synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world, device)
+    err = B.spark_attn_error_word(ws)
+    if err != 0:
+        raise RuntimeError(f"device error word {err:#x}")
+
+    tokens = wl.batch * world
+    value = tokens * steps / (ms_total * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) activations and caches, N(0,1/fan_in) weights; no checkpoint)",
+        "config": {"workload": wl.name, "description": wl.description, "batch": wl.batch,
+                   "positions": wl.positions if wl.batch <= 8 else
+                   {"min": min(wl.positions), "max": max(wl.positions), "sum": sum(wl.positions)},
+                   "layers": ["full" if s.is_full else "sliding" for s in wl.layers][:8]
+                   + (["..."] if len(wl.layers) > 8 else []),
+                   "n_layers": len(wl.layers),
+                   "parallelism": f"replicas x{world} (independent sequences, no collective)",
+                   "l2": f"{copies} rotating copies of weights+caches ({copies * sb['total'] / 1e6:.0f} MB) "
+                         f"vs {l2 / 1e6:.0f} MB L2"},
+        "steps_per_s": round(1e3 / ms_per_step * world, 3),
+        "hbm_bytes_per_step": sb["total"],
+        "hbm_gbs": round(sb["total"] / (ms_per_step * 1e-3) / 1e9, 1),
+        "hbm_frac": round(sb["total"] / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "hbm_peak_gbs": peaks["hbm_gbs"],
+        "hbm_peak_source": peaks["source"],
+        "roofline": {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "bytes_per_launch": per_launch_bytes,
+                     "avg_launch_us": round(kavg[top] * 1e3, 3)},
+        "kernels": {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": launches_per_step[k],
+                        "share": round(share[k] / tot, 4),
+                        "bytes_per_launch": sb["per_kernel"][k] // len(wl.layers),
+                        "gbs": round(sb["per_kernel"][k] / len(wl.layers) / (kavg[k] * 1e-3) / 1e9, 1)}
+                    for k in kavg},
+        "e2e": {"value": round(tokens * e2e_steps / e2e_s, 3), "unit": "tokens/s",
+                "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * H * 4},
+        "gpu_launches": kernels_per_step * steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the oracle (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def time_oracle(wl: synth.Workload, budget_s: float) -> dict:
+    """Time the float64 CPU oracle on (layer, sequence) units of one step, in
+    order, until `budget_s` is spent; report the rate scaled to a whole step."""
+    import oracle
+
+    geom = oracle.OracleGeometry(hidden=wl.hidden, n_q=wl.n_q, n_kv=wl.n_kv, head_dim=wl.head_dim,
+                                 window=wl.window)
+    h = synth.to_numpy(synth.make_h(wl, "cpu")).astype(np.float64)
+    units_total = len(wl.layers) * wl.batch
+    units = 0
+    elapsed = 0.0
+    max_seqs = max(1, min(wl.batch, 2))
+    for li, spec in enumerate(wl.layers):
+        w = {k: synth.to_numpy(v) for k, v in synth.make_weights(wl, li, "cpu").items()}
+        seqs = list(range(max_seqs))
+        k, v = synth.make_cache(wl, li, "cpu", sequences=seqs)
+        kn, vn = synth.to_numpy(k), synth.to_numpy(v)
+        for b in seqs:
+            t0 = time.perf_counter()
+            oracle.decode_step(geom, h, w, kn, vn, spec.is_full, wl.positions, spec.ring_capacity, sequences=[b])
+            elapsed += time.perf_counter() - t0
+            units += 1
+            if elapsed >= budget_s:
+                break
+        if elapsed >= budget_s:
+            break
+    steps_per_s = (units / units_total) / elapsed
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(steps_per_s * wl.batch, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{units} of {units_total} (layer, sequence) decode units of one step "
+                      f"({elapsed:.1f} s, numpy float64, BLAS threads up to {cores} cores)"}
+
+
+def bench_reference(args, wl, rank, world):
+    """The reference arm: the float64 CPU oracle as it stands, on the host
+    cores, each step a bounded sample of the workload; rank 0 only."""
+    if rank != 0:
+        return None
+    k_steps = args.steps if args.steps > 0 else 3
+    per_step = max(1.0, min(15.0, 120.0 / (k_steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_oracle(wl, 0.0)               # one (layer, sequence) unit each
+    runs = [time_oracle(wl, per_step) for _ in range(k_steps)]
+    value = float(np.median([r["value"] for r in runs]))
+    base = dict(runs[-1])
+    base["value"] = round(value, 6)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "tokens/s",
+            "n_gpus": world, "steps": k_steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "description": wl.description, "batch": wl.batch},
+            "cpu_baseline": base,
+            "e2e": {"value": round(value, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about two seconds' worth)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.workloads()))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--copies", type=int, default=0, help="rotating input copies (0: enough to beat L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, local, world = dist_env()
+    wl = synth.workloads()[args.workload]
+
+    if args.impl == "reference":
+        line = bench_reference(args, wl, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    dist_init(world, "nccl")
+    line = bench_ours(args, wl, rank, local, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = time_oracle(wl, float(os.environ.get("SPARK_ORACLE_BUDGET_S", "15")))
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,282 @@
+"""ctypes binding of ``libspark_attn.so`` (the C ABI in ``include/spark_attn.h``).
+
+Argument marshalling only: every step of the block runs in the library's CUDA
+kernels.  Tensors are PyTorch CUDA tensors (PyTorch provides device memory and
+streams); the functions carry the C entry points' names and check only what
+the C side cannot see (tensor devices, dtypes, contiguity and shapes).  The
+library must have been built (``decode_attention_block_gb300.build_lib.build``);
+importing the binding without it raises instead of falling back to anything.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from .build_lib import LIB_PATH
+
+SPARK_OK = 0
+SPARK_F32 = 0
+SPARK_BF16 = 1
+SPARK_SLIDING = 0
+SPARK_FULL = 1
+SPARK_MAX_BATCH = 1024
+
+_DTYPE_CODE = {torch.float32: SPARK_F32, torch.bfloat16: SPARK_BF16}
+
+
+class SparkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {spark_attn_status_string(status)} (status {status})")
+
+
+class SparkGeom(ctypes.Structure):
+    _fields_ = [
+        ("hidden", ctypes.c_int32),
+        ("n_q", ctypes.c_int32),
+        ("n_kv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("full_rotary_dim", ctypes.c_int32),
+        ("window", ctypes.c_int32),
+        ("full_theta", ctypes.c_float),
+        ("sliding_theta", ctypes.c_float),
+        ("eps", ctypes.c_float),
+        ("scale", ctypes.c_float),
+    ]
+
+
+class SparkLayerWeights(ctypes.Structure):
+    _fields_ = [
+        ("norm_w", ctypes.c_void_p),
+        ("qkv_w", ctypes.c_void_p),
+        ("g_w", ctypes.c_void_p),
+        ("o_w", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+class SparkKvLayer(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("capacity", ctypes.c_int64),
+        ("ring_capacity", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+# every symbol include/spark_attn.h declares, with its ctypes signature
+_P = ctypes.c_void_p
+_SIGNATURES = {
+    "spark_geom_default": (None, [ctypes.POINTER(SparkGeom)]),
+    "spark_attn_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(SparkGeom), ctypes.c_int32]),
+    "spark_attn_workspace_init": (ctypes.c_int, [_P, ctypes.c_size_t, _P]),
+    "spark_attn_error_word": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32), _P]),
+    "spark_attn_decode": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkLayerWeights),
+                                         ctypes.POINTER(SparkKvLayer), ctypes.c_int32,
+                                         ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P,
+                                         ctypes.c_size_t, _P]),
+    "spark_dbg_qkv_gate": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkLayerWeights),
+                                          ctypes.c_int32, _P, _P]),
+    "spark_dbg_split_rope": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
+                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                            _P, _P]),
+    "spark_dbg_attention": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
+                                           ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                           _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
+    "spark_dbg_gate_oproj": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, _P, _P,
+                                            ctypes.POINTER(SparkLayerWeights), ctypes.c_int32, _P, _P]),
+    "spark_attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "spark_attn_abi_version": (ctypes.c_int32, []),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library once and bind every declared entry point."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "decode_attention_block_gb300.build_lib.build() (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def declared_symbols() -> list[str]:
+    return list(_SIGNATURES)
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _check(status: int, where: str) -> None:
+    if status != SPARK_OK:
+        raise SparkError(status, where)
+
+
+def _positions(positions) -> ctypes.Array:
+    vals = [int(p) for p in positions]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+@dataclass
+class LayerWeights:
+    """One layer's weights as CUDA tensors (all float32 or all bfloat16):
+    ``norm_w [hidden]``, ``qkv_w [n_q*d + 2*n_kv*d, hidden]``,
+    ``g_w [n_q, hidden]``, ``o_w [hidden, n_q*d]``."""
+
+    norm_w: torch.Tensor
+    qkv_w: torch.Tensor
+    g_w: torch.Tensor
+    o_w: torch.Tensor
+
+    def to_c(self) -> SparkLayerWeights:
+        dt = self.qkv_w.dtype
+        if dt not in _DTYPE_CODE:
+            raise TypeError(f"weights must be float32 or bfloat16, got {dt}")
+        return SparkLayerWeights(_dev_ptr(self.norm_w, "norm_w", dt), _dev_ptr(self.qkv_w, "qkv_w", dt),
+                                 _dev_ptr(self.g_w, "g_w", dt), _dev_ptr(self.o_w, "o_w", dt),
+                                 _DTYPE_CODE[dt])
+
+
+@dataclass
+class KvLayer:
+    """One layer's cache as CUDA tensors ``k``, ``v`` of shape
+    ``[batch, capacity, n_kv, head_dim]`` (float32 or bfloat16) and the ring
+    capacity (0 = linear addressing)."""
+
+    k: torch.Tensor
+    v: torch.Tensor
+    ring_capacity: int = 0
+
+    def to_c(self) -> SparkKvLayer:
+        dt = self.k.dtype
+        if dt not in _DTYPE_CODE:
+            raise TypeError(f"cache must be float32 or bfloat16, got {dt}")
+        if self.k.dim() != 4 or self.k.shape != self.v.shape:
+            raise ValueError("k and v must both be [batch, capacity, n_kv, head_dim]")
+        return SparkKvLayer(_dev_ptr(self.k, "k", dt), _dev_ptr(self.v, "v", dt),
+                            int(self.k.shape[1]), int(self.ring_capacity), _DTYPE_CODE[dt])
+
+
+# ---------------------------------------------------------------------------
+# the entry points
+# ---------------------------------------------------------------------------
+
+def spark_geom_default() -> SparkGeom:
+    g = SparkGeom()
+    load().spark_geom_default(ctypes.byref(g))
+    return g
+
+
+def spark_attn_workspace_bytes(geom: SparkGeom, batch: int) -> int:
+    return int(load().spark_attn_workspace_bytes(ctypes.byref(geom), int(batch)))
+
+
+def spark_attn_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check(load().spark_attn_workspace_init(_dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                            _stream(stream)), "spark_attn_workspace_init")
+
+
+def spark_attn_error_word(ws: torch.Tensor, stream=None) -> int:
+    word = ctypes.c_uint32(0)
+    _check(load().spark_attn_error_word(_dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                        ctypes.byref(word), _stream(stream)), "spark_attn_error_word")
+    return int(word.value)
+
+
+def make_workspace(geom: SparkGeom, batch: int, device=None, stream=None) -> torch.Tensor:
+    """Allocate (through PyTorch) and initialise a workspace for ``batch``."""
+    nbytes = spark_attn_workspace_bytes(geom, batch)
+    if nbytes == 0:
+        raise ValueError("invalid geometry or batch for a workspace")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    spark_attn_workspace_init(ws, stream)
+    return ws
+
+
+def spark_attn_decode(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, kv: KvLayer,
+                      layer_class: int, positions, out: torch.Tensor, ws: torch.Tensor,
+                      stream=None) -> None:
+    batch = len(positions)
+    wc, kc, pos = weights.to_c(), kv.to_c(), _positions(positions)
+    _check(load().spark_attn_decode(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32),
+                                    ctypes.byref(wc), ctypes.byref(kc), int(layer_class), pos,
+                                    batch, _dev_ptr(out, "out", torch.float32),
+                                    _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                    _stream(stream)), "spark_attn_decode")
+
+
+def spark_dbg_qkv_gate(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, qkvg: torch.Tensor,
+                       stream=None) -> None:
+    wc = weights.to_c()
+    _check(load().spark_dbg_qkv_gate(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32), ctypes.byref(wc),
+                                     int(h.shape[0]), _dev_ptr(qkvg, "qkvg", torch.float32),
+                                     _stream(stream)), "spark_dbg_qkv_gate")
+
+
+def spark_dbg_split_rope(geom: SparkGeom, qkvg: torch.Tensor, kv: KvLayer, layer_class: int, positions,
+                         q_rot: torch.Tensor, stream=None) -> None:
+    kc, pos = kv.to_c(), _positions(positions)
+    _check(load().spark_dbg_split_rope(ctypes.byref(geom), _dev_ptr(qkvg, "qkvg", torch.float32),
+                                       ctypes.byref(kc), int(layer_class), pos, len(positions),
+                                       _dev_ptr(q_rot, "q_rot", torch.float32), _stream(stream)),
+           "spark_dbg_split_rope")
+
+
+def spark_dbg_attention(geom: SparkGeom, q_rot: torch.Tensor, kv: KvLayer, layer_class: int, positions,
+                        a: torch.Tensor, ws: torch.Tensor, n_ctas: int = 0, stream=None) -> None:
+    kc, pos = kv.to_c(), _positions(positions)
+    _check(load().spark_dbg_attention(ctypes.byref(geom), _dev_ptr(q_rot, "q_rot", torch.float32),
+                                      ctypes.byref(kc), int(layer_class), pos, len(positions),
+                                      _dev_ptr(a, "a", torch.float32), int(n_ctas),
+                                      _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                      _stream(stream)), "spark_dbg_attention")
+
+
+def spark_dbg_gate_oproj(geom: SparkGeom, a: torch.Tensor, qkvg: torch.Tensor, h: torch.Tensor,
+                         weights: LayerWeights, out: torch.Tensor, stream=None) -> None:
+    wc = weights.to_c()
+    _check(load().spark_dbg_gate_oproj(ctypes.byref(geom), _dev_ptr(a, "a", torch.float32),
+                                       _dev_ptr(qkvg, "qkvg", torch.float32), _dev_ptr(h, "h", torch.float32),
+                                       ctypes.byref(wc), int(h.shape[0]), _dev_ptr(out, "out", torch.float32),
+                                       _stream(stream)), "spark_dbg_gate_oproj")
+
+
+def spark_attn_status_string(status: int) -> str:
+    return load().spark_attn_status_string(int(status)).decode()
+
+
+def spark_attn_abi_version() -> int:
+    return int(load().spark_attn_abi_version())

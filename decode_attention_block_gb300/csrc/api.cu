@@ -1,0 +1,270 @@
+// api.cu -- the library's C ABI (declared in include/spark_attn.h): argument
+// validation, the per-class parameter selection and the launch sequence of
+// one decode step.
+//
+// Host logic follows turbospark-runtime 0.3.0:
+//  * src/families/spark/attn.rs, rope_params_for: full layers take
+//    (full_rotary_dim, full_theta), sliding layers (head_dim, sliding_theta);
+//  * src/families/spark/attn.rs, encode_attention_block: seq_len =
+//    position + 1; full layers read [0, seq_len) with identity addressing;
+//    sliding layers read [seq_len - window, seq_len) through the ring once
+//    seq_len exceeds its capacity;
+//  * RealForwardError::{Unsupported, Gpu} become the status codes.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "launch.h"
+
+namespace spark {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+}  // namespace spark
+
+using namespace spark;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_geom(const spark_geom* g) {
+  if (!g) return SPARK_ERR_INVALID_ARG;
+  if (g->head_dim != kHeadDim) return SPARK_ERR_UNSUPPORTED;
+  if (g->n_kv < 1 || g->n_kv > 8 || g->n_q != kGroup * g->n_kv) return SPARK_ERR_UNSUPPORTED;
+  if (g->hidden < 8 || g->hidden > 8192 || g->hidden % 8 != 0) return SPARK_ERR_UNSUPPORTED;
+  if (g->full_rotary_dim < 2 || g->full_rotary_dim > kHeadDim || g->full_rotary_dim % 2 != 0)
+    return SPARK_ERR_UNSUPPORTED;
+  if (g->window < 1) return SPARK_ERR_INVALID_ARG;
+  if (!(g->full_theta > 0.f) || !(g->sliding_theta > 0.f) || !isfinite(g->full_theta) ||
+      !isfinite(g->sliding_theta))
+    return SPARK_ERR_INVALID_ARG;
+  if (!(g->eps >= 0.f) || !isfinite(g->eps) || !isfinite(g->scale)) return SPARK_ERR_INVALID_ARG;
+  return SPARK_OK;
+}
+
+int check_dtype(int32_t dt) { return (dt == SPARK_F32 || dt == SPARK_BF16) ? SPARK_OK : SPARK_ERR_INVALID_ARG; }
+
+int check_weights(const spark_layer_weights* w, bool need_qkv, bool need_o) {
+  if (!w) return SPARK_ERR_INVALID_ARG;
+  if (check_dtype(w->dtype) != SPARK_OK) return SPARK_ERR_INVALID_ARG;
+  if (need_qkv && (!w->norm_w || !w->qkv_w || !w->g_w)) return SPARK_ERR_INVALID_ARG;
+  if (need_qkv && (!aligned16(w->norm_w) || !aligned16(w->qkv_w) || !aligned16(w->g_w)))
+    return SPARK_ERR_INVALID_ARG;
+  if (need_o && (!w->o_w || !aligned16(w->o_w))) return SPARK_ERR_INVALID_ARG;
+  return SPARK_OK;
+}
+
+int check_batch(int32_t batch) {
+  return (batch >= 1 && batch <= SPARK_MAX_BATCH) ? SPARK_OK : SPARK_ERR_INVALID_ARG;
+}
+
+// The KV layer against the class and the positions: every row a call writes
+// or reads must lie inside the buffer.
+int check_kv(const spark_geom* g, const spark_kv_layer* kv, int32_t cls, const int32_t* positions,
+             int32_t batch) {
+  if (!kv || !positions) return SPARK_ERR_INVALID_ARG;
+  if (cls != SPARK_FULL && cls != SPARK_SLIDING) return SPARK_ERR_INVALID_ARG;
+  if (!kv->k || !kv->v || !aligned16(kv->k) || !aligned16(kv->v)) return SPARK_ERR_INVALID_ARG;
+  if (check_dtype(kv->dtype) != SPARK_OK) return SPARK_ERR_INVALID_ARG;
+  if (kv->capacity < 1 || kv->ring_capacity < 0) return SPARK_ERR_INVALID_ARG;
+  if (kv->ring_capacity > 0) {
+    if (cls == SPARK_FULL) return SPARK_ERR_BAD_RING;  // a full layer reads its whole history
+    if (kv->ring_capacity > kv->capacity) return SPARK_ERR_INVALID_ARG;
+    if (kv->ring_capacity < g->window) return SPARK_ERR_BAD_RING;  // would evict live rows
+  }
+  // TMA coordinates of cache rows are 32-bit
+  if ((int64_t)batch * kv->capacity >= ((int64_t)1 << 31)) return SPARK_ERR_UNSUPPORTED;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t p = positions[b];
+    if (p < 0 || p >= INT32_MAX - 1) return SPARK_ERR_POSITION;
+    if (kv->ring_capacity == 0 && (int64_t)p >= kv->capacity) return SPARK_ERR_POSITION;
+  }
+  return SPARK_OK;
+}
+
+int check_ws(const spark_geom* g, int32_t batch, void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPARK_ERR_WORKSPACE;
+  if (bytes < ws_layout(g->n_q, g->n_kv, batch).total) return SPARK_ERR_WORKSPACE;
+  return SPARK_OK;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPARK_OK : SPARK_ERR_CUDA; }
+
+template <typename T>
+inline T* ws_at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<unsigned char*>(ws) + off);
+}
+
+void rope_for(const spark_geom* g, int32_t cls, int* rotary_dim, double* theta) {
+  // attn.rs, rope_params_for
+  if (cls == SPARK_FULL) {
+    *rotary_dim = g->full_rotary_dim;
+    *theta = (double)g->full_theta;
+  } else {
+    *rotary_dim = g->head_dim;
+    *theta = (double)g->sliding_theta;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+void spark_geom_default(spark_geom* g) {
+  if (!g) return;
+  g->hidden = 2560;
+  g->n_q = 16;
+  g->n_kv = 4;
+  g->head_dim = 256;
+  g->full_rotary_dim = 64;
+  g->window = 512;
+  g->full_theta = 5.0e6f;
+  g->sliding_theta = 1.0e4f;
+  g->eps = 1.0e-6f;
+  g->scale = 0.0625f;  // 256^-0.5
+}
+
+size_t spark_attn_workspace_bytes(const spark_geom* g, int32_t batch) {
+  if (check_geom(g) != SPARK_OK || check_batch(batch) != SPARK_OK) return 0;
+  return ws_layout(g->n_q, g->n_kv, batch).total;
+}
+
+int spark_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes == 0) return SPARK_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream));
+}
+
+int spark_attn_error_word(void* workspace, size_t workspace_bytes, uint32_t* word, void* stream) {
+  if (!workspace || workspace_bytes < 256 || !word) return SPARK_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  *word = host;
+  return cuda_status(e);
+}
+
+int spark_dbg_qkv_gate(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                       int32_t batch, float* qkvg, void* stream) {
+  int s;
+  if ((s = check_geom(g)) != SPARK_OK) return s;
+  if ((s = check_weights(w, true, false)) != SPARK_OK) return s;
+  if ((s = check_batch(batch)) != SPARK_OK) return s;
+  if (!h || !qkvg || !aligned16(h) || !aligned16(qkvg)) return SPARK_ERR_INVALID_ARG;
+  return cuda_status(launch_qkv_gate(w->dtype, h, w->norm_w, w->qkv_w, w->g_w, qkvg, g->hidden,
+                                     g->n_q, g->n_kv, batch, g->eps, (cudaStream_t)stream));
+}
+
+int spark_dbg_split_rope(const spark_geom* g, const float* qkvg, const spark_kv_layer* kv,
+                         int32_t layer_class, const int32_t* positions, int32_t batch,
+                         float* q_rot, void* stream) {
+  int s;
+  if ((s = check_geom(g)) != SPARK_OK) return s;
+  if ((s = check_batch(batch)) != SPARK_OK) return s;
+  if ((s = check_kv(g, kv, layer_class, positions, batch)) != SPARK_OK) return s;
+  if (!qkvg || !q_rot || !aligned16(qkvg) || !aligned16(q_rot)) return SPARK_ERR_INVALID_ARG;
+  // no workspace here: the kernel's own bounds check has no error word to set
+  int rotary_dim;
+  double theta;
+  rope_for(g, layer_class, &rotary_dim, &theta);
+  return cuda_status(launch_split_rope(kv->dtype, qkvg, q_rot, kv->k, kv->v, g->n_q, g->n_kv,
+                                       kv->capacity, kv->ring_capacity, rotary_dim, theta,
+                                       positions, batch, nullptr, (cudaStream_t)stream));
+}
+
+int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_layer* kv,
+                        int32_t layer_class, const int32_t* positions, int32_t batch, float* a,
+                        int32_t n_ctas, void* workspace, size_t workspace_bytes, void* stream) {
+  int s;
+  if ((s = check_geom(g)) != SPARK_OK) return s;
+  if ((s = check_batch(batch)) != SPARK_OK) return s;
+  if ((s = check_kv(g, kv, layer_class, positions, batch)) != SPARK_OK) return s;
+  if ((s = check_ws(g, batch, workspace, workspace_bytes)) != SPARK_OK) return s;
+  if (!q_rot || !a || !aligned16(q_rot) || !aligned16(a)) return SPARK_ERR_INVALID_ARG;
+  if (n_ctas < 0 || n_ctas > kMaxAttnCtas) return SPARK_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(g->n_q, g->n_kv, batch);
+  return cuda_status(launch_attention(
+      kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity, kv->ring_capacity,
+      layer_class == SPARK_FULL, g->window, g->scale, positions, batch, a,
+      ws_at<float>(workspace, L.part), ws_at<uint32_t>(workspace, L.counters),
+      ws_at<uint32_t>(workspace, L.err), n_ctas, (cudaStream_t)stream));
+}
+
+int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* qkvg, const float* h,
+                         const spark_layer_weights* w, int32_t batch, float* out, void* stream) {
+  int s;
+  if ((s = check_geom(g)) != SPARK_OK) return s;
+  if ((s = check_weights(w, false, true)) != SPARK_OK) return s;
+  if ((s = check_batch(batch)) != SPARK_OK) return s;
+  if (!a || !qkvg || !h || !out || !aligned16(a) || !aligned16(qkvg) || !aligned16(h) ||
+      !aligned16(out))
+    return SPARK_ERR_INVALID_ARG;
+  return cuda_status(launch_gate_oproj(w->dtype, a, qkvg, h, w->o_w, out, g->hidden, g->n_q,
+                                       g->n_kv, batch, (cudaStream_t)stream));
+}
+
+int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                      const spark_kv_layer* kv, int32_t layer_class, const int32_t* positions,
+                      int32_t batch, float* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  int s;
+  if ((s = check_geom(g)) != SPARK_OK) return s;
+  if ((s = check_weights(w, true, true)) != SPARK_OK) return s;
+  if ((s = check_batch(batch)) != SPARK_OK) return s;
+  if ((s = check_kv(g, kv, layer_class, positions, batch)) != SPARK_OK) return s;
+  if ((s = check_ws(g, batch, workspace, workspace_bytes)) != SPARK_OK) return s;
+  if (!h || !out || !aligned16(h) || !aligned16(out)) return SPARK_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(g->n_q, g->n_kv, batch);
+  cudaStream_t st = (cudaStream_t)stream;
+  float* qkvg = ws_at<float>(workspace, L.qkvg);
+  float* q_rot = ws_at<float>(workspace, L.q_rot);
+  float* a = ws_at<float>(workspace, L.a);
+  uint32_t* err = ws_at<uint32_t>(workspace, L.err);
+  int rotary_dim;
+  double theta;
+  rope_for(g, layer_class, &rotary_dim, &theta);
+  cudaError_t e = launch_qkv_gate(w->dtype, h, w->norm_w, w->qkv_w, w->g_w, qkvg, g->hidden,
+                                  g->n_q, g->n_kv, batch, g->eps, st);
+  if (e == cudaSuccess)
+    e = launch_split_rope(kv->dtype, qkvg, q_rot, kv->k, kv->v, g->n_q, g->n_kv, kv->capacity,
+                          kv->ring_capacity, rotary_dim, theta, positions, batch, err, st);
+  if (e == cudaSuccess)
+    e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity,
+                         kv->ring_capacity, layer_class == SPARK_FULL, g->window, g->scale,
+                         positions, batch, a, ws_at<float>(workspace, L.part),
+                         ws_at<uint32_t>(workspace, L.counters), err, 0, st);
+  if (e == cudaSuccess)
+    e = launch_gate_oproj(w->dtype, a, qkvg, h, w->o_w, out, g->hidden, g->n_q, g->n_kv, batch, st);
+  return cuda_status(e);
+}
+
+const char* spark_attn_status_string(int status) {
+  switch (status) {
+    case SPARK_OK: return "ok";
+    case SPARK_ERR_INVALID_ARG: return "invalid argument";
+    case SPARK_ERR_POSITION: return "position outside the layer's cache";
+    case SPARK_ERR_BAD_RING: return "ring capacity would evict rows inside the window";
+    case SPARK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPARK_ERR_UNSUPPORTED: return "geometry not supported by the kernels";
+    case SPARK_ERR_CUDA: return "CUDA runtime error";
+    case SPARK_ERR_DEVICE: return "a kernel reported a failure in the workspace error word";
+    default: return "unknown status";
+  }
+}
+
+int32_t spark_attn_abi_version(void) { return SPARK_ATTN_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,219 @@
+// common.cuh -- device helpers shared by the block's kernels: inline PTX for
+// mbarriers, TMA tensor loads, packed fp32x2 FMA and bounded waits; the
+// per-sequence window arithmetic shared by host and device; the workspace
+// layout.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spark_attn.h"
+
+namespace spark {
+
+constexpr int kHeadDim = 256;        // the only head_dim the kernels are built for
+constexpr int kGroup = 4;            // query heads per KV head
+constexpr int kMaxAttnCtas = 1024;   // partial-result slots reserved for CTAs
+constexpr int kPartFloats = 2 * kGroup + kGroup * kHeadDim;  // m[4], l[4], o[4][256]
+
+// device error word bits
+constexpr uint32_t kErrWaitTimeout = 1u;
+constexpr uint32_t kErrIndex = 2u;
+
+// ---------------------------------------------------------------------------
+// window / ring arithmetic (attn.rs, encode_attention_block: the window set-up;
+// the ring only addresses rows once seq_len exceeds its capacity)
+// ---------------------------------------------------------------------------
+struct Window {
+  int64_t kv_start;   // first logical position read
+  int64_t rows;       // number of positions read = seq_len - kv_start
+  int64_t first_slot; // cache row of position kv_start
+  int64_t len_a;      // rows from first_slot upwards before the ring wraps to row 0
+};
+
+__host__ __device__ inline Window window_of(int64_t position, bool full, int64_t window,
+                                            int64_t ring_capacity) {
+  Window w;
+  const int64_t seq_len = position + 1;
+  if (full) {
+    w.kv_start = 0;
+  } else {
+    w.kv_start = seq_len > window ? seq_len - window : 0;
+  }
+  w.rows = seq_len - w.kv_start;
+  const bool ring_active = !full && ring_capacity > 0 && seq_len > ring_capacity;
+  if (ring_active) {
+    w.first_slot = w.kv_start % ring_capacity;
+    const int64_t to_end = ring_capacity - w.first_slot;
+    w.len_a = w.rows < to_end ? w.rows : to_end;
+  } else {
+    w.first_slot = w.kv_start;
+    w.len_a = w.rows;
+  }
+  return w;
+}
+
+// cache row that receives the token at `position` (kv_write.rs, kv_write_target)
+__host__ __device__ inline int64_t write_slot_of(int64_t position, int64_t ring_capacity) {
+  return ring_capacity > 0 ? position % ring_capacity : position;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout (host computes, kernels receive the pieces as pointers)
+// ---------------------------------------------------------------------------
+struct WsLayout {
+  size_t err = 0;       // uint32 error word
+  size_t counters = 0;  // uint32 [batch * n_kv] merge tickets
+  size_t qkvg = 0;      // f32 [batch][qkvg_ld]
+  size_t q_rot = 0;     // f32 [batch][q_dim]
+  size_t a = 0;         // f32 [batch][q_dim]
+  size_t part = 0;      // f32 [kMaxAttnCtas + batch * n_kv][kPartFloats]
+  size_t total = 0;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int qkvg_ld(int n_q, int n_kv) { return n_q * kHeadDim + 2 * n_kv * kHeadDim + n_q; }
+
+inline WsLayout ws_layout(int n_q, int n_kv, int batch) {
+  WsLayout L;
+  size_t off = 256;
+  L.err = 0;
+  L.counters = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)batch * n_kv, 256);
+  L.qkvg = off;
+  off = align_up(off + sizeof(float) * (size_t)batch * qkvg_ld(n_q, n_kv), 256);
+  L.q_rot = off;
+  off = align_up(off + sizeof(float) * (size_t)batch * n_q * kHeadDim, 256);
+  L.a = off;
+  off = align_up(off + sizeof(float) * (size_t)batch * n_q * kHeadDim, 256);
+  L.part = off;
+  off = align_up(off + sizeof(float) * (size_t)(kMaxAttnCtas + (size_t)batch * n_kv) * kPartFloats, 256);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.release.cta.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, at most `limit_ns`.  Returns
+// false (and leaves the wait) if the time runs out or if another thread of the
+// block raised `*abort`.  Every wait in these kernels goes through here, so no
+// thread can spin forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// 3-D tiled TMA load global -> shared, completing on `bar` (byte count).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// d = a * b + c on two fp32 lanes at once (Blackwell packed FFMA2)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// bf16 pair packed in one 32-bit word -> two fp32 (exact widening)
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// 16-byte load of data read exactly once: not allocated in L1
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace spark

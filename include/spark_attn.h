@@ -1,0 +1,210 @@
+/*
+ * spark_attn.h -- C ABI of the spark2_5 single-token decode attention block
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The block (turbospark-runtime 0.3.0, src/families/spark/mod.rs, module doc
+ * "One decoder layer, transcribed", and src/families/spark/attn.rs,
+ * encode_attention_block) computes, for every sequence b of a batch:
+ *
+ *   x      = h / sqrt(mean(h^2) + eps) * input_layernorm     (plain w)
+ *   qkv    = q_k_v_proj @ x           rows: q (n_q*d) | k (n_kv*d) | v (n_kv*d)
+ *   g      = g_proj @ x               one logit per query head
+ *   q, k   = NeoX rope at the token's position, per layer class:
+ *              full    -> leading full_rotary_dim dims at full_theta
+ *              sliding -> all head_dim dims at sliding_theta
+ *   k, v   -> written into the cache row of the token's position
+ *   a      = GQA attention (query head h reads KV head h / (n_q/n_kv)),
+ *            scale `scale`, over the whole history (full layer) or the last
+ *            `window` positions through the ring (sliding layer)
+ *   a      = a * sigmoid(g) broadcast over head_dim       (before o_proj)
+ *   out    = h + o_proj @ a                                (raw residual)
+ *
+ * Conventions shared by every entry point:
+ *   - Device pointers are CUDA device addresses owned by the caller; the
+ *     library never allocates or frees memory and never synchronises a stream
+ *     unless the entry point says so.  All device pointers must be 16-byte
+ *     aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued on it in order; a non-zero return means nothing was enqueued,
+ *     except SPARK_ERR_CUDA from a failed launch.
+ *   - Matrices are row-major: a [rows x cols] weight has out[r] = sum_c W[r,c] in[c].
+ *   - Host arrays (`positions`) are read during the call only.
+ *   - Return value: SPARK_OK (0) or a negative spark_status.
+ */
+#ifndef SPARK_ATTN_H
+#define SPARK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPARK_ATTN_ABI_VERSION 1
+/* largest batch one call accepts */
+#define SPARK_MAX_BATCH 1024
+
+/* Status codes.  INVALID_ARG / POSITION / BAD_RING / WORKSPACE / UNSUPPORTED
+ * are detected on the host before anything is enqueued (the counterpart of
+ * the pages' RealForwardError::Unsupported); CUDA is a launch error reported
+ * by the runtime (RealForwardError::Gpu); DEVICE is a failure a kernel
+ * recorded in the workspace error word. */
+typedef enum spark_status {
+  SPARK_OK = 0,
+  SPARK_ERR_INVALID_ARG = -1,  /* null pointer, batch out of range, bad enum, misaligned pointer */
+  SPARK_ERR_POSITION = -2,     /* position < 0, or its cache row lies outside the layer's capacity */
+  SPARK_ERR_BAD_RING = -3,     /* ring capacity that would evict a row still inside the window */
+  SPARK_ERR_WORKSPACE = -4,    /* workspace null, too small or misaligned */
+  SPARK_ERR_UNSUPPORTED = -5,  /* geometry the kernels are not built for */
+  SPARK_ERR_CUDA = -6,         /* a CUDA runtime call failed */
+  SPARK_ERR_DEVICE = -7        /* a kernel set the workspace error word */
+} spark_status;
+
+typedef enum spark_dtype { SPARK_F32 = 0, SPARK_BF16 = 1 } spark_dtype;
+
+/* Layer class: an entry of 1 in the model's full_attention_layer_mask marks a
+ * full layer (src/families/spark/attn.rs, encode_attention_block, the rope
+ * and window set-up). */
+typedef enum spark_layer_class { SPARK_SLIDING = 0, SPARK_FULL = 1 } spark_layer_class;
+
+/* Block geometry.  spark_geom_default() fills spark2_5's values: hidden 2560,
+ * 16 query heads over 4 KV heads at head_dim 256, full layers rotate 64 dims
+ * at theta 5e6, sliding layers all 256 at theta 1e4, window 512, eps 1e-6,
+ * scale 256^-0.5 (mod.rs module doc; attn.rs module doc item 2).
+ * Supported: head_dim == 256, n_q == 4 * n_kv with 1 <= n_kv <= 8,
+ * hidden a multiple of 8 in [8, 8192], full_rotary_dim even in [2, 256],
+ * window >= 1, thetas > 0, eps >= 0, finite scale. */
+typedef struct spark_geom {
+  int32_t hidden;
+  int32_t n_q;
+  int32_t n_kv;
+  int32_t head_dim;
+  int32_t full_rotary_dim;
+  int32_t window;
+  float full_theta;
+  float sliding_theta;
+  float eps;
+  float scale;
+} spark_geom;
+
+/* One layer's weights (device, caller-owned), all of element type `dtype`:
+ *   norm_w [hidden]                       input_layernorm.weight
+ *   qkv_w  [n_q*d + 2*n_kv*d][hidden]     q_k_v_proj.weight (rows q | k | v)
+ *   g_w    [n_q][hidden]                  g_proj.weight
+ *   o_w    [hidden][n_q*d]                o_proj.weight                     */
+typedef struct spark_layer_weights {
+  const void* norm_w;
+  const void* qkv_w;
+  const void* g_w;
+  const void* o_w;
+  int32_t dtype; /* spark_dtype */
+} spark_layer_weights;
+
+/* One layer's KV cache (device, caller-owned): K and V are two buffers of
+ * [batch][capacity][n_kv][head_dim] elements of `dtype`.
+ * ring_capacity == 0: linear addressing, position p lives in row p
+ *   (needs p < capacity).
+ * ring_capacity  > 0: a ring of that many rows (sliding layers only;
+ *   ring_capacity <= capacity and ring_capacity >= window): position p lives
+ *   in row p mod ring_capacity, and attention addresses rows through the ring
+ *   once seq_len = p + 1 exceeds it (attn.rs, encode_attention_block, the
+ *   window set-up; kv_write.rs, kv_write_target). */
+typedef struct spark_kv_layer {
+  void* k;
+  void* v;
+  int64_t capacity;
+  int32_t ring_capacity;
+  int32_t dtype; /* spark_dtype */
+} spark_kv_layer;
+
+/* Fill `g` with spark2_5's geometry. */
+void spark_geom_default(spark_geom* g);
+
+/* Bytes of device workspace spark_attn_decode / spark_dbg_attention need for
+ * `batch` sequences (0 for invalid arguments).  The workspace holds the fused
+ * projection outputs, the rotated queries, the attention output, the split-K
+ * partial results, the merge tickets and a device error word. */
+size_t spark_attn_workspace_bytes(const spark_geom* g, int32_t batch);
+
+/* Zero a workspace (enqueued on `stream`).  Required once after allocation:
+ * the split-K merge tickets must start at zero; every call leaves them at
+ * zero again. */
+int spark_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Read and clear the workspace's device error word.  SYNCHRONISES `stream`.
+ * Bits: 1 = a pipeline wait ran out of time, 2 = an index outside its buffer
+ * was skipped. */
+int spark_attn_error_word(void* workspace, size_t workspace_bytes, uint32_t* word, void* stream);
+
+/* One decode step of the attention block for `batch` independent sequences
+ * (attn.rs, encode_attention_block, plus the input RMSNorm and the raw
+ * residual add of mod.rs's layer loop).
+ *   h          [batch][hidden] fp32 device: residual stream in.
+ *   w          the layer's weights.
+ *   kv         the layer's cache; row slot(positions[b]) of K and V of each
+ *              sequence b is overwritten with the token's rope'd k and its v,
+ *              rounded to the cache's element type; nothing else is written.
+ *   layer_class SPARK_FULL / SPARK_SLIDING.
+ *   positions  [batch] HOST int32: the token's position in each sequence;
+ *              the token attends to positions [kv_start, positions[b]].
+ *   out        [batch][hidden] fp32 device: h + o_proj(...).  May equal h.
+ *   workspace  >= spark_attn_workspace_bytes(g, batch) bytes, 256-byte
+ *              aligned, initialised once by spark_attn_workspace_init.  Calls
+ *              sharing a workspace must be ordered on one stream.
+ * Errors: INVALID_ARG, POSITION, BAD_RING, WORKSPACE, UNSUPPORTED before any
+ * work is enqueued; CUDA if a launch fails. */
+int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                      const spark_kv_layer* kv, int32_t layer_class,
+                      const int32_t* positions, int32_t batch, float* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- the block's stages, one kernel each (same conventions) ------------- */
+
+/* Input RMSNorm + q_k_v_proj + g_proj (attn.rs: the fused projection and
+ * the gate's projection, which read the same normed x).
+ *   qkvg [batch][n_q*d + 2*n_kv*d + n_q] fp32 device: q | k | v | g-logits. */
+int spark_dbg_qkv_gate(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                       int32_t batch, float* qkvg, void* stream);
+
+/* Split + per-class NeoX rope + cache write (attn.rs: encode_split_qkv and
+ * encode_rope_neox_subdim on q and on k in its slot).
+ *   qkvg  as produced by spark_dbg_qkv_gate (read only).
+ *   q_rot [batch][n_q*d] fp32 device: rotated queries.
+ *   kv    row slot(p) of K receives rope(k), of V receives v. */
+int spark_dbg_split_rope(const spark_geom* g, const float* qkvg, const spark_kv_layer* kv,
+                         int32_t layer_class, const int32_t* positions, int32_t batch,
+                         float* q_rot, void* stream);
+
+/* GQA decode attention over each sequence's window (attn.rs,
+ * encode_attention_block -> kv_write.rs, encode_attention_any), split over
+ * the GPU with a log-sum-exp merge.
+ *   q_rot [batch][n_q*d] fp32 device.
+ *   a     [batch][n_q*d] fp32 device: un-gated attention output.
+ *   n_ctas number of thread blocks sharing the work (0 = one per SM); the
+ *          result does not depend on it beyond floating-point reassociation.
+ *   workspace as for spark_attn_decode. */
+int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_layer* kv,
+                        int32_t layer_class, const int32_t* positions, int32_t batch,
+                        float* a, int32_t n_ctas, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Head gate + o_proj + raw residual (attn.rs: encode_sigmoid_head_gate_mul
+ * and the o_proj GEMV; mod.rs: encode_residual_add).
+ *   a    [batch][n_q*d] fp32 device, un-gated attention output.
+ *   qkvg gate logits are read from column n_q*d + 2*n_kv*d of each row.
+ *   h    [batch][hidden] fp32 device; out [batch][hidden], may equal h. */
+int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* qkvg,
+                         const float* h, const spark_layer_weights* w, int32_t batch,
+                         float* out, void* stream);
+
+/* Human-readable text of a status code (static storage). */
+const char* spark_attn_status_string(int status);
+
+/* SPARK_ATTN_ABI_VERSION of the loaded library. */
+int32_t spark_attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPARK_ATTN_H */

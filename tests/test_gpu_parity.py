@@ -1,0 +1,378 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every stage is checked on its own with inputs drawn by the seeded generators
+(so a stage's input never comes from another CUDA stage), then the whole block
+end to end on each workload, at the sizes the oracle finishes in seconds and
+at full size on sampled sequences.  Cache-row placement is bit-exact: after a
+call exactly the slot of each sequence's position has changed.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_block_gb300 import build_lib, synth
+from helpers import MAX_ABS, REL_L2, assert_close, err_stats, np_weights, oracle_geom
+
+pytestmark = pytest.mark.gpu
+
+D = 256
+N_Q, N_KV = 16, 4
+Q_DIM, KV_DIM = N_Q * D, N_KV * D
+QKVG_LD = Q_DIM + 2 * KV_DIM + N_Q
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build_lib.build()
+    from decode_attention_block_gb300 import binding
+    binding.load()
+    return binding
+
+
+class SeqCaches:
+    """Per-sequence host copies of a cache, indexable like [batch][rows]."""
+
+    def __init__(self, rows: dict, dtype):
+        self.rows = rows
+        self.dtype = dtype
+
+    def __getitem__(self, b):
+        return self.rows[b]
+
+
+def f64(x):
+    return oracle.cache_rows_to_f64(np.asarray(x)) if np.asarray(x).dtype == np.uint16 \
+        else np.asarray(x, dtype=np.float64)
+
+
+def _gen(seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return g
+
+
+def assert_rows_within_one_ulp(got: torch.Tensor, want: np.ndarray, what: str):
+    """Cache rows written by the kernel vs the oracle's rounded rows: the two
+    round differently-computed values of one real number, so they may differ by
+    one unit in the last place where that number lies next to a tie."""
+    g = synth.to_numpy(got)
+    if g.dtype == np.uint16:
+        gi = g.astype(np.int32)
+        wi = np.asarray(want).astype(np.int32)
+        same_sign = (gi >> 15) == (wi >> 15)
+        diff = np.where(same_sign, np.abs(gi - wi), 99)
+        assert np.all(diff <= 1), f"{what}: {int(np.sum(diff > 1))} elements differ by more than 1 ulp"
+        assert np.mean(diff == 0) > 0.99, f"{what}: only {np.mean(diff == 0):.4f} bit-identical"
+    else:
+        np.testing.assert_allclose(g.astype(np.float64), np.asarray(want, dtype=np.float64),
+                                   rtol=2e-6, atol=1e-6, err_msg=what)
+
+
+def assert_only_slot_changed(before: torch.Tensor, after: torch.Tensor, b: int, slot: int, what: str):
+    assert torch.equal(before[b, :slot], after[b, :slot]), f"{what}: rows below slot {slot} changed"
+    assert torch.equal(before[b, slot + 1:], after[b, slot + 1:]), f"{what}: rows above slot {slot} changed"
+
+
+# ---------------------------------------------------------------------------
+# stage 1: RMSNorm + q_k_v_proj + g_proj
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,batch", [("bf16", 1), ("bf16", 3), ("f32", 2), ("bf16", 6), ("bf16", 70)])
+def test_qkv_gate_matches_oracle(B, dtype, batch):
+    wl = synth.Workload("t", "", dtype, [0] * batch, [synth.LayerSpec(True)], seed=200 + batch)
+    w = synth.make_weights(wl, 0, "cuda")
+    h = synth.make_h(wl, "cuda")
+    geom = B.spark_geom_default()
+    qkvg = torch.full((batch, QKVG_LD), float("nan"), device="cuda")
+    B.spark_dbg_qkv_gate(geom, h, B.LayerWeights(**w), qkvg)
+    torch.cuda.synchronize()
+    wn = np_weights(w)
+    hn = synth.to_numpy(h)
+    got = qkvg.cpu().numpy()
+    for b in range(batch) if batch <= 6 else (0, 33, 69):
+        x = oracle.rms_norm(hn[b], f64(wn["norm_w"]), 1e-6)
+        assert_close(got[b, :Q_DIM + 2 * KV_DIM], oracle.project(f64(wn["qkv_w"]), x), f"qkv b={b}")
+        assert_close(got[b, Q_DIM + 2 * KV_DIM:], oracle.project(f64(wn["g_w"]), x), f"g b={b}")
+
+
+# ---------------------------------------------------------------------------
+# stage 2: split + per-class rope + cache-row write
+# ---------------------------------------------------------------------------
+
+SLOT_POSITIONS = [0, 40, 511, 512, 513, 700, 1023, 1024]
+
+
+@pytest.mark.parametrize("is_full", [True, False])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("positions", [SLOT_POSITIONS, [131072]])
+def test_split_rope_and_cache_slots(B, is_full, dtype, positions):
+    batch = len(positions)
+    ring = 0 if is_full else 512
+    wl = synth.Workload("t", "", dtype, positions, [synth.LayerSpec(is_full, ring)], seed=300)
+    kc, vc = synth.make_cache(wl, 0, "cuda")
+    kc0, vc0 = kc.clone(), vc.clone()
+    qkvg = torch.randn((batch, QKVG_LD), generator=_gen(301), device="cuda")
+    q_rot = torch.empty((batch, Q_DIM), device="cuda")
+    geom = B.spark_geom_default()
+    cls = B.SPARK_FULL if is_full else B.SPARK_SLIDING
+    B.spark_dbg_split_rope(geom, qkvg, B.KvLayer(kc, vc, ring), cls, positions, q_rot)
+    torch.cuda.synchronize()
+    r, theta = oracle.rope_params_for(is_full, 64, 256, 5e6, 1e4)
+    qn = qkvg.cpu().numpy().astype(np.float64)
+    got_q = q_rot.cpu().numpy()
+    round_ = (lambda x: oracle.f64_to_bf16_bits(x)) if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    for b, p in enumerate(positions):
+        q = oracle.rope_neox(qn[b, :Q_DIM].reshape(N_Q, D), p, r, theta)
+        k = oracle.rope_neox(qn[b, Q_DIM:Q_DIM + KV_DIM].reshape(N_KV, D), p, r, theta)
+        v = qn[b, Q_DIM + KV_DIM:Q_DIM + 2 * KV_DIM].reshape(N_KV, D)
+        # rope angles reach 131072 rad: the kernel reduces them in fp64
+        assert_close(got_q[b], q.reshape(-1), f"q b={b} p={p}", max_abs=1e-4, rel_l2=1e-5)
+        slot = oracle.write_slot(p, ring)
+        assert_rows_within_one_ulp(kc[b, slot], round_(k), f"k row b={b} p={p}")
+        want_v = round_(v)
+        got_v = synth.to_numpy(vc[b, slot])
+        assert np.array_equal(got_v, want_v), f"v row b={b} p={p} not bit-exact"
+        assert_only_slot_changed(kc0, kc, b, slot, f"K b={b} p={p}")
+        assert_only_slot_changed(vc0, vc, b, slot, f"V b={b} p={p}")
+
+
+def test_rope_class_selection_reaches_the_kernel(B):
+    """Swapping the classes' (width, theta) must change q: the full class
+    leaves dims 64..255 untouched, the sliding class does not."""
+    positions = [700]
+    qkvg = torch.randn((1, QKVG_LD), generator=_gen(302), device="cuda")
+    geom = B.spark_geom_default()
+    out = {}
+    for is_full in (True, False):
+        wl = synth.Workload("t", "", "bf16", positions, [synth.LayerSpec(is_full, 0 if is_full else 512)], seed=303)
+        kc, vc = synth.make_cache(wl, 0, "cuda")
+        q_rot = torch.empty((1, Q_DIM), device="cuda")
+        B.spark_dbg_split_rope(geom, qkvg, B.KvLayer(kc, vc, 0 if is_full else 512),
+                               B.SPARK_FULL if is_full else B.SPARK_SLIDING, positions, q_rot)
+        out[is_full] = q_rot.view(N_Q, D).cpu()
+    src = qkvg[0, :Q_DIM].view(N_Q, D).cpu()
+    assert torch.equal(out[True][:, 64:], src[:, 64:])
+    assert (out[False][:, 64:] - src[:, 64:]).abs().max() > 0.1
+
+
+# ---------------------------------------------------------------------------
+# stage 3: split-K GQA decode attention
+# ---------------------------------------------------------------------------
+
+ATTN_CASES = [
+    # id, is_full, ring, capacity (None: max position + 1), positions, n_ctas, dtype
+    ("single_row", True, 0, None, [0], 0, "bf16"),
+    ("full_p40", True, 0, None, [40], 0, "bf16"),
+    ("full_p700_f32", True, 0, None, [700], 0, "f32"),
+    ("sliding_ring_wrapped", False, 512, 512, [700], 0, "bf16"),
+    ("sliding_ring_unwrapped", False, 512, 512, [40], 0, "f32"),
+    ("sliding_linear_window", False, 0, 2048, [1500], 0, "bf16"),
+    ("full_ragged", True, 0, None, [5, 700, 3000], 0, "bf16"),
+    ("sliding_ring_edges", False, 512, 512, [0, 511, 512, 513, 1024, 131072], 0, "bf16"),
+    ("split1", True, 0, None, [3000], 1, "bf16"),
+    ("split2", True, 0, None, [3000], 2, "bf16"),
+    ("split7", True, 0, None, [3000], 7, "bf16"),
+    ("split64_ragged", True, 0, None, [5, 700, 3000, 17, 1], 64, "bf16"),
+    ("split1000_ragged", True, 0, None, [5, 700, 3000, 17, 1], 1000, "bf16"),
+    ("big_batch_bucket", False, 512, 512, list(range(0, 2000, 10)), 0, "bf16"),
+]
+
+
+def _attention_oracle(q, kc_np, vc_np, positions, is_full, ring, window=512):
+    out = []
+    for b, p in enumerate(positions):
+        seq_len, kv_start, active = oracle.window_params(p, is_full, window, ring)
+        slots = [oracle.read_slot(j, active) for j in range(kv_start, seq_len)]
+        out.append(oracle.attention_decode(q[b].reshape(N_Q, D), f64(kc_np[b][slots]),
+                                           f64(vc_np[b][slots]), 1 / 16, N_KV).reshape(-1))
+    return np.stack(out)
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=[c[0] for c in ATTN_CASES])
+def test_attention_matches_oracle(B, case):
+    _, is_full, ring, cap, positions, n_ctas, dtype = case
+    batch = len(positions)
+    wl = synth.Workload("t", "", dtype, positions, [synth.LayerSpec(is_full, ring)], seed=400 + batch)
+    if cap is not None and ring == 0:
+        wl.positions = positions
+        kc, vc = synth.make_cache(wl, 0, "cuda")
+        extra = cap - kc.shape[1]
+        if extra > 0:
+            pad = torch.randn((batch, extra, N_KV, D), generator=_gen(401), device="cuda").to(kc.dtype)
+            kc = torch.cat([kc, pad], 1).contiguous()
+            vc = torch.cat([vc, pad.flip(0)], 1).contiguous()
+    else:
+        kc, vc = synth.make_cache(wl, 0, "cuda")
+    q = torch.randn((batch, Q_DIM), generator=_gen(402), device="cuda")
+    a = torch.full((batch, Q_DIM), float("nan"), device="cuda")
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, batch)
+    B.spark_dbg_attention(geom, q, B.KvLayer(kc, vc, ring), B.SPARK_FULL if is_full else B.SPARK_SLIDING,
+                          positions, a, ws, n_ctas=n_ctas)
+    assert B.spark_attn_error_word(ws) == 0
+    got = a.cpu().numpy()
+    want = _attention_oracle(q.cpu().numpy().astype(np.float64), synth.to_numpy(kc), synth.to_numpy(vc),
+                             positions, is_full, ring)
+    assert_close(got, want, "attention")
+    if positions == [0]:
+        # one row: softmax weight 1, the output is that row's v, exactly
+        v0 = vc[0, 0].float().cpu().numpy()
+        for h in range(N_Q):
+            assert np.array_equal(got[0, h * D:(h + 1) * D], v0[h // 4])
+
+
+def test_attention_split_count_invariance_and_reuse(B):
+    """The result does not depend on how many CTAs share the rows, and the
+    merge tickets are reset so a workspace serves call after call."""
+    positions = [3000, 9, 4097]
+    wl = synth.Workload("t", "", "bf16", positions, [synth.LayerSpec(True)], seed=410)
+    kc, vc = synth.make_cache(wl, 0, "cuda")
+    q = torch.randn((3, Q_DIM), generator=_gen(411), device="cuda")
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, 3)
+    results = []
+    for n in (1, 2, 7, 64, 0, 64, 1000, 3):
+        a = torch.empty((3, Q_DIM), device="cuda")
+        B.spark_dbg_attention(geom, q, B.KvLayer(kc, vc, 0), B.SPARK_FULL, positions, a, ws, n_ctas=n)
+        results.append(a.cpu().numpy())
+    assert B.spark_attn_error_word(ws) == 0
+    for r in results[1:]:
+        ma, _ = err_stats(r, results[0])
+        assert ma < 1e-5
+    ws_host = ws.cpu()
+    assert int(ws_host[256:256 + 4 * 3 * 4].view(torch.int32).abs().sum()) == 0   # tickets back at 0
+
+
+# ---------------------------------------------------------------------------
+# stage 4: head gate + o_proj + residual
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,batch", [("bf16", 1), ("bf16", 5), ("f32", 2)])
+def test_gate_oproj_matches_oracle(B, dtype, batch):
+    wl = synth.Workload("t", "", dtype, [0] * batch, [synth.LayerSpec(True)], seed=500 + batch)
+    w = synth.make_weights(wl, 0, "cuda")
+    h = synth.make_h(wl, "cuda")
+    a = torch.randn((batch, Q_DIM), generator=_gen(501), device="cuda")
+    qkvg = torch.randn((batch, QKVG_LD), generator=_gen(502), device="cuda") * 2
+    out = torch.empty_like(h)
+    geom = B.spark_geom_default()
+    B.spark_dbg_gate_oproj(geom, a, qkvg, h, B.LayerWeights(**w), out)
+    # in place: out aliases h
+    h2 = h.clone()
+    B.spark_dbg_gate_oproj(geom, a, qkvg, h2, B.LayerWeights(**w), h2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, h2)
+    wo = f64(np_weights(w)["o_w"])
+    an, gn, hn = a.cpu().numpy(), qkvg.cpu().numpy(), h.cpu().numpy().astype(np.float64)
+    for b in range(batch):
+        gated = oracle.head_gate(an[b].reshape(N_Q, D), gn[b, Q_DIM + 2 * KV_DIM:].astype(np.float64))
+        o = oracle.project(wo, gated.reshape(-1))
+        assert_close(out[b].cpu().numpy() - hn[b], o, f"o b={b}")
+
+
+# ---------------------------------------------------------------------------
+# the whole block, end to end through spark_attn_decode
+# ---------------------------------------------------------------------------
+
+def run_workload_parity(B, wl: synth.Workload, sample=None, layers=None):
+    """Decode one step through every layer of the workload (each layer's input
+    is the previous layer's output), on the GPU and in the oracle, and compare
+    each layer's contribution o = out - in, the written cache rows, and the
+    untouched rest of the caches."""
+    seqs = list(range(wl.batch)) if sample is None else list(sample)
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, wl.batch)
+    ogeom = oracle_geom(wl)
+    cur = synth.make_h(wl, "cuda")
+    cur_np = {b: synth.to_numpy(cur[b]).astype(np.float64) for b in seqs}
+    h0 = {b: cur_np[b].copy() for b in seqs}
+    worst = (0.0, 0.0)
+    for li in (range(len(wl.layers)) if layers is None else layers):
+        spec = wl.layers[li]
+        w = synth.make_weights(wl, li, "cuda")
+        kc, vc = synth.make_cache(wl, li, "cuda")
+        kc0, vc0 = kc.clone(), vc.clone()
+        k_np = SeqCaches({b: synth.to_numpy(kc[b]) for b in seqs}, np.uint16 if wl.dtype == "bf16" else np.float32)
+        v_np = SeqCaches({b: synth.to_numpy(vc[b]) for b in seqs}, k_np.dtype)
+        out = torch.empty_like(cur)
+        cls = B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING
+        B.spark_attn_decode(geom, cur, B.LayerWeights(**w), B.KvLayer(kc, vc, spec.ring_capacity), cls,
+                            wl.positions, out, ws)
+        torch.cuda.synchronize()
+        h_in = np.zeros((wl.batch, wl.hidden))
+        for b in seqs:
+            h_in[b] = cur_np[b]
+        res = oracle.decode_step(ogeom, h_in, np_weights(w), k_np, v_np, spec.is_full, wl.positions,
+                                 spec.ring_capacity, sequences=seqs)
+        got_out = out.cpu().numpy().astype(np.float64)
+        got_in = cur.cpu().numpy().astype(np.float64)
+        for i, b in enumerate(seqs):
+            ma, rel = assert_close(got_out[b] - got_in[b], res["o"][i], f"layer {li} o b={b}")
+            worst = (max(worst[0], ma), max(worst[1], rel))
+            slot = res["slot"][i]
+            assert_rows_within_one_ulp(kc[b, slot], res["k_row"][i], f"layer {li} k row b={b}")
+            assert_rows_within_one_ulp(vc[b, slot], res["v_row"][i], f"layer {li} v row b={b}")
+            cur_np[b] = res["out"][i]
+        for b in range(wl.batch):
+            slot = oracle.write_slot(wl.positions[b], spec.ring_capacity)
+            assert_only_slot_changed(kc0, kc, b, slot, f"layer {li} K b={b}")
+            assert_only_slot_changed(vc0, vc, b, slot, f"layer {li} V b={b}")
+        cur = out
+        del kc, vc, kc0, vc0
+    assert B.spark_attn_error_word(ws) == 0
+    got_final = cur.cpu().numpy().astype(np.float64)
+    for b in seqs:
+        assert_close(got_final[b] - h0[b], cur_np[b] - h0[b], f"stack output b={b}")
+    return worst
+
+
+WORKLOADS = synth.workloads()
+
+
+def test_decode_sliding_f32_b1_pos40(B):
+    run_workload_parity(B, WORKLOADS["sliding_f32_b1_pos40"])
+
+
+def test_decode_full_sliding_bf16_b1_pos700(B):
+    wl = WORKLOADS["full+sliding_bf16_b1_pos700"]
+    run_workload_parity(B, wl)                 # full then sliding, chained
+    run_workload_parity(B, wl, layers=[1])     # the sliding layer alone on the same h
+
+
+def test_decode_stack36_bf16_b1_ctx8192(B):
+    run_workload_parity(B, WORKLOADS["stack36_bf16_b1_ctx8192"])
+
+
+def test_decode_ragged_b64(B):
+    wl = WORKLOADS["full+sliding_bf16_b64_ctx512-32768"]
+    pos = np.array(wl.positions)
+    sample = sorted({int(pos.argmin()), int(pos.argmax()), 7, 31, 50})
+    run_workload_parity(B, wl, sample=sample)
+
+
+def test_decode_long_context_b8_ctx131072(B):
+    run_workload_parity(B, WORKLOADS["full+sliding_bf16_b8_ctx131072"], sample=[0, 5])
+
+
+def test_decode_position_zero_and_small_batch_edges(B):
+    wl = synth.Workload("edges", "", "bf16", [0, 1, 2, 513], [synth.LayerSpec(True, 0), synth.LayerSpec(False, 512)],
+                        seed=600)
+    run_workload_parity(B, wl)
+
+
+def test_zero_o_proj_returns_h_exactly(B):
+    wl = synth.Workload("t", "", "bf16", [100, 3], [synth.LayerSpec(True)], seed=610)
+    w = synth.make_weights(wl, 0, "cuda")
+    w["o_w"].zero_()
+    kc, vc = synth.make_cache(wl, 0, "cuda")
+    h = synth.make_h(wl, "cuda")
+    out = torch.empty_like(h)
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, 2)
+    B.spark_attn_decode(geom, h, B.LayerWeights(**w), B.KvLayer(kc, vc, 0), B.SPARK_FULL, wl.positions, out, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, h)

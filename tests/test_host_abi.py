@@ -1,0 +1,148 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library loads and exports every entry point ``include/spark_attn.h``
+declares; invalid arguments are rejected with the documented status before
+anything touches a device (so these calls are safe without a GPU).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from decode_attention_block_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    build_lib.build()
+    from decode_attention_block_gb300 import binding
+    binding.load()
+    return binding
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "spark_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(spark_[a-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported_and_bound(B):
+    declared = _declared_functions()
+    assert len(declared) >= 10
+    lib = ctypes.CDLL(build_lib.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in spark_attn.h but not exported"
+    assert sorted(B.declared_symbols()) == declared
+
+
+def test_abi_version_and_status_strings(B):
+    assert B.spark_attn_abi_version() == 1
+    for code in range(-7, 1):
+        s = B.spark_attn_status_string(code)
+        assert s and s != "unknown status"
+    assert B.spark_attn_status_string(-99) == "unknown status"
+
+
+def test_geometry_default_is_spark2_5(B):
+    g = B.spark_geom_default()
+    assert (g.hidden, g.n_q, g.n_kv, g.head_dim, g.full_rotary_dim, g.window) == (2560, 16, 4, 256, 64, 512)
+    assert g.full_theta == 5e6 and g.sliding_theta == 1e4
+    assert abs(g.eps - 1e-6) < 1e-12 and g.scale == 0.0625
+
+
+def test_workspace_bytes(B):
+    g = B.spark_geom_default()
+    sizes = [B.spark_attn_workspace_bytes(g, b) for b in (1, 2, 64, 1024)]
+    assert all(s > 0 and s % 256 == 0 for s in sizes)
+    assert sizes == sorted(sizes)
+    assert B.spark_attn_workspace_bytes(g, 0) == 0
+    assert B.spark_attn_workspace_bytes(g, 1025) == 0
+    bad = B.spark_geom_default()
+    bad.head_dim = 128
+    assert B.spark_attn_workspace_bytes(bad, 1) == 0
+
+
+# -- argument validation, all rejected on the host ---------------------------
+
+FAKE = 1 << 40          # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _call(B, geom=None, weights=None, kv=None, cls=1, positions=(5,), batch=None, h=FAKE,
+          out=FAKE, ws=FAKE, ws_bytes=None):
+    lib = B.load()
+    g = geom or B.spark_geom_default()
+    w = weights or B.SparkLayerWeights(FAKE, FAKE, FAKE, FAKE, B.SPARK_BF16)
+    k = kv or B.SparkKvLayer(FAKE, FAKE, 1024, 0, B.SPARK_BF16)
+    n = len(positions) if batch is None else batch
+    pos = (ctypes.c_int32 * max(1, len(positions)))(*positions)
+    if ws_bytes is None:
+        ws_bytes = B.spark_attn_workspace_bytes(g, max(1, min(n, 1024))) or (1 << 30)
+    return lib.spark_attn_decode(ctypes.byref(g), h, ctypes.byref(w), ctypes.byref(k), cls, pos, n,
+                                 out, ws, ws_bytes, None)
+
+
+def test_rejects_null_and_misaligned_pointers(B):
+    assert _call(B, h=0) == -1
+    assert _call(B, out=0) == -1
+    assert _call(B, h=FAKE + 4) == -1
+    assert _call(B, weights=B.SparkLayerWeights(FAKE, 0, FAKE, FAKE, B.SPARK_BF16)) == -1
+    assert _call(B, weights=B.SparkLayerWeights(FAKE, FAKE + 8, FAKE, FAKE, B.SPARK_BF16)) == -1
+    assert _call(B, kv=B.SparkKvLayer(0, FAKE, 1024, 0, B.SPARK_BF16)) == -1
+
+
+def test_rejects_bad_enums_and_batch(B):
+    assert _call(B, cls=2) == -1
+    assert _call(B, weights=B.SparkLayerWeights(FAKE, FAKE, FAKE, FAKE, 7)) == -1
+    assert _call(B, kv=B.SparkKvLayer(FAKE, FAKE, 1024, 0, 5)) == -1
+    assert _call(B, positions=(1,), batch=0) == -1
+    assert _call(B, positions=tuple([1] * 1025)) == -1
+
+
+def test_rejects_positions_outside_the_cache(B):
+    assert _call(B, positions=(1024,)) == -2            # linear cache of 1024 rows: 0..1023
+    assert _call(B, positions=(-1,)) == -2
+    assert _call(B, positions=(3, 2000, 4)) == -2
+    # a ring layer keeps any position (row p mod ring)
+    ring = B.SparkKvLayer(FAKE, FAKE, 512, 512, B.SPARK_BF16)
+    assert _call(B, kv=ring, cls=0, positions=(131072,), ws=FAKE + 16) == -4  # passes kv checks, fails ws
+
+
+def test_rejects_bad_rings(B):
+    g = B.spark_geom_default()
+    # a full layer has no ring
+    assert _call(B, kv=B.SparkKvLayer(FAKE, FAKE, 512, 512, B.SPARK_BF16), cls=1) == -3
+    # a ring shorter than the window would evict rows the window still reads
+    assert _call(B, kv=B.SparkKvLayer(FAKE, FAKE, 512, 256, B.SPARK_BF16), cls=0) == -3
+    # a ring larger than the buffer
+    assert _call(B, kv=B.SparkKvLayer(FAKE, FAKE, 512, 1024, B.SPARK_BF16), cls=0) == -1
+    assert g.window == 512
+
+
+def test_rejects_small_or_misaligned_workspace(B):
+    g = B.spark_geom_default()
+    need = B.spark_attn_workspace_bytes(g, 1)
+    assert _call(B, ws_bytes=need - 1) == -4
+    assert _call(B, ws=FAKE + 16) == -4
+    assert _call(B, ws=0) == -4
+
+
+def test_rejects_unsupported_geometry(B):
+    for field, val in (("head_dim", 128), ("n_q", 8), ("n_kv", 16), ("hidden", 2564),
+                       ("full_rotary_dim", 63), ("full_rotary_dim", 512)):
+        g = B.spark_geom_default()
+        setattr(g, field, val)
+        if field == "n_kv":
+            g.n_q = 4 * val
+        assert _call(B, geom=g) == -5, field
+    g = B.spark_geom_default()
+    g.window = 0
+    assert _call(B, geom=g) == -1
+    g = B.spark_geom_default()
+    g.scale = float("nan")
+    assert _call(B, geom=g) == -1
