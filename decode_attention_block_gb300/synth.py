@@ -111,6 +111,10 @@ def workloads() -> dict:
                  "8 sequences at context 131072, one full layer (rotary 64 @ 5e6) and one sliding "
                  "layer (ring 512 wrapped many times), bf16",
                  "bf16", [131072] * 8, [LayerSpec(True, 0), LayerSpec(False, RING)], seed=1004),
+        Workload("full_bf16_b1_ctx131072",
+                 "one full layer (rotary 64 @ 5e6), bf16, one sequence at context 131072 "
+                 "(a single long-context attention)",
+                 "bf16", [131072], [LayerSpec(True, 0)], seed=1005),
     ]
     return {w.name: w for w in wl}
 

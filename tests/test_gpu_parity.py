@@ -314,8 +314,10 @@ def run_workload_parity(B, wl: synth.Workload, sample=None, layers=None):
             ma, rel = assert_close(got_out[b] - got_in[b], res["o"][i], f"layer {li} o b={b}")
             worst = (max(worst[0], ma), max(worst[1], rel))
             slot = res["slot"][i]
-            assert_rows_within_one_ulp(kc[b, slot], res["k_row"][i], f"layer {li} k row b={b}")
-            assert_rows_within_one_ulp(vc[b, slot], res["v_row"][i], f"layer {li} v row b={b}")
+            # the rows are projections of the layer input, computed in fp32 here
+            # and fp64 there, then rounded: compared as float outputs
+            assert_close(f64(synth.to_numpy(kc[b, slot])), f64(res["k_row"][i]), f"layer {li} k row b={b}")
+            assert_close(f64(synth.to_numpy(vc[b, slot])), f64(res["v_row"][i]), f"layer {li} v row b={b}")
             cur_np[b] = res["out"][i]
         for b in range(wl.batch):
             slot = oracle.write_slot(wl.positions[b], spec.ring_capacity)
