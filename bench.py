@@ -165,7 +165,7 @@ class ClockSampler:
 class Copy:
     """One full set of a workload's inputs resident on the device."""
 
-    def __init__(self, wl, B, device, ring_geom):
+    def __init__(self, wl, B, device):
         self.layers = []
         for li, spec in enumerate(wl.layers):
             w = synth.make_weights(wl, li, device)
@@ -175,7 +175,8 @@ class Copy:
         self.buf = [torch.empty_like(self.h), torch.empty_like(self.h)]
 
 
-def run_step(B, geom, wl, cp, ws, stream):
+def run_step(B, geom, wl, cp, ws, stream=None):
+    """One decode step of every layer through the public call."""
     cur = cp.h
     for i, (spec, w, kv) in enumerate(cp.layers):
         out = cp.buf[i % 2]
@@ -185,37 +186,40 @@ def run_step(B, geom, wl, cp, ws, stream):
     return cur
 
 
-def run_step_staged(B, geom, wl, cp, ws, bufs, stream, ev):
-    """The same work as run_step, launched stage by stage with CUDA events
-    around each kernel on the launching stream."""
-    cur = cp.h
-    for i, (spec, w, kv) in enumerate(cp.layers):
-        out = cp.buf[i % 2]
-        cls = B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING
-        ev.mark("qkv_gate", stream, lambda: B.spark_dbg_qkv_gate(geom, cur, w, bufs["qkvg"], stream))
-        ev.mark("split_rope", stream, lambda: B.spark_dbg_split_rope(geom, bufs["qkvg"], kv, cls, wl.positions,
-                                                                      bufs["q_rot"], stream))
-        ev.mark("attention", stream, lambda: B.spark_dbg_attention(geom, bufs["q_rot"], kv, cls, wl.positions,
-                                                                    bufs["a"], ws, 0, stream))
-        ev.mark("gate_oproj", stream, lambda: B.spark_dbg_gate_oproj(geom, bufs["a"], bufs["qkvg"], cur, w, out,
-                                                                      stream))
-        cur = out
+STAGES = ("qkv_rope", "attention", "gate_oproj")
 
 
-class KernelEvents:
-    def __init__(self):
-        self.pairs = {}
+def stage_launcher(B, geom, wl, cp, ws, bufs, stage):
+    """Launch one stage kernel for every layer of a copy (the same work that
+    stage does inside run_step)."""
+    def go():
+        cur = cp.h
+        for i, (spec, w, kv) in enumerate(cp.layers):
+            out = cp.buf[i % 2]
+            cls = B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING
+            if stage == "qkv_rope":
+                B.spark_dbg_qkv_rope(geom, cur, w, kv, cls, wl.positions, bufs["q_rot"], bufs["g"])
+            elif stage == "attention":
+                B.spark_dbg_attention(geom, bufs["q_rot"], kv, cls, wl.positions, bufs["a"], ws, 0)
+            else:
+                B.spark_dbg_gate_oproj(geom, bufs["a"], bufs["g"], cur, w, out)
+            cur = out
+    return go
 
-    def mark(self, name, stream, launch):
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        launch()
-        e.record(stream)
-        self.pairs.setdefault(name, []).append((s, e))
 
-    def avg_ms(self):
-        return {k: sum(s.elapsed_time(e) for s, e in v) / len(v) for k, v in self.pairs.items()}
+def capture(fn):
+    """Record fn's launches (made on the current stream) in a CUDA graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()                      # first call outside capture (function attributes)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        fn()
+    torch.cuda.synchronize()
+    return g
 
 
 def bench_ours(args, wl, rank, local, world):
@@ -228,29 +232,37 @@ def bench_ours(args, wl, rank, local, world):
     geom = B.spark_geom_default()
     stream = torch.cuda.current_stream(device)
     sb = step_bytes(wl)
+    L = len(wl.layers)
     l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
     copies = args.copies or max(1, math.ceil(4 * l2 / sb["total"]))
-    cps = [Copy(wl, B, device, geom) for _ in range(copies)]
+    cps = [Copy(wl, B, device) for _ in range(copies)]
     ws = B.make_workspace(geom, wl.batch, device)
     H, q_dim = wl.hidden, wl.n_q * wl.head_dim
-    bufs = {"qkvg": torch.empty((wl.batch, q_dim + 2 * wl.n_kv * wl.head_dim + wl.n_q), device=device),
-            "q_rot": torch.empty((wl.batch, q_dim), device=device),
+    bufs = {"q_rot": torch.empty((wl.batch, q_dim), device=device),
+            "g": torch.empty((wl.batch, wl.n_q), device=device),
             "a": torch.empty((wl.batch, q_dim), device=device)}
     torch.cuda.synchronize()
 
-    # warm-up
+    # one CUDA graph per copy: a step's launches replayed without host overhead
+    use_graph = not args.no_graph
+    if use_graph:
+        graphs = [capture(lambda cp=cp: run_step(B, geom, wl, cp, ws)) for cp in cps]
+        step = lambda i: graphs[i % copies].replay()  # noqa: E731
+    else:
+        step = lambda i: run_step(B, geom, wl, cps[i % copies], ws, stream)  # noqa: E731
+
     for i in range(args.warmup):
-        run_step(B, geom, wl, cps[i % copies], ws, stream)
+        step(i)
     torch.cuda.synchronize()
 
     steps = args.steps
     if steps <= 0:   # auto: about two seconds of timed work
         t0 = time.perf_counter()
         for i in range(20):
-            run_step(B, geom, wl, cps[i % copies], ws, stream)
+            step(i)
         torch.cuda.synchronize()
         per = (time.perf_counter() - t0) / 20
-        steps = int(min(20000, max(50, 2.0 / max(per, 1e-6))))
+        steps = int(min(50000, max(50, 2.0 / max(per, 1e-6))))
 
     # timed region: exactly `steps` steps
     sampler = ClockSampler(local)
@@ -262,30 +274,40 @@ def bench_ours(args, wl, rank, local, world):
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(steps):
-            run_step(B, geom, wl, cps[i % copies], ws, stream)
+            step(i)
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
     clocks = sampler.summary()
-    ms_total = start.elapsed_time(end)
-    ms_total = max_over_ranks(ms_total, world, device)
+    ms_total = max_over_ranks(start.elapsed_time(end), world, device)
     ms_per_step = ms_total / steps
-    kernels_per_step = 4 * len(wl.layers)
+    chunks = -(-wl.batch // 4)           # the projection kernels take up to 4 sequences each
+    kernels_per_step = L * (2 * chunks + 1)
 
-    # per-kernel durations: the same steps launched stage by stage with events
-    ev = KernelEvents()
-    ksteps = min(steps, max(20, 2000 // max(1, len(wl.layers))))
-    for i in range(ksteps):
-        run_step_staged(B, geom, wl, cps[i % copies], ws, bufs, stream, ev)
-    torch.cuda.synchronize()
-    kavg = ev.avg_ms()   # ms per launch
-    launches_per_step = {k: len(wl.layers) for k in kavg}
-    share = {k: kavg[k] * launches_per_step[k] for k in kavg}
+    # per-kernel durations: each stage's launches (all layers, all copies)
+    # replayed back to back in a graph between two events on this stream
+    kavg = {}
+    for stage in STAGES:
+        fns = [stage_launcher(B, geom, wl, cp, ws, bufs, stage) for cp in cps]
+        g = capture(lambda: [f() for f in fns])
+        reps = max(3, min(200, int(2000 / (L * copies))))
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        kavg[stage] = e0.elapsed_time(e1) / (reps * L * copies)   # ms per launch
+    share = {k: kavg[k] * L for k in kavg}
     tot = sum(share.values())
     top = max(share, key=share.get)
-    per_launch_bytes = sb["per_kernel"][top] / len(wl.layers)
+    bytes_key = {"qkv_rope": "qkv_gate", "attention": "attention", "gate_oproj": "gate_oproj"}
+    per_launch = {k: sb["per_kernel"][bytes_key[k]] / L for k in STAGES}
     peaks = measured_peaks()
-    achieved = per_launch_bytes / (kavg[top] * 1e-3) / 1e9
+    achieved = per_launch[top] / (kavg[top] * 1e-3) / 1e9
 
     # end to end through the public call: h from pinned host, out read back
     h_host = [synth.make_h(wl, "cpu").pin_memory() for _ in range(2)]
@@ -299,15 +321,15 @@ def bench_ours(args, wl, rank, local, world):
         cp.h.copy_(h_host[i % 2], non_blocking=True)
         res = run_step(B, geom, wl, cp, ws, stream)
         out_host.copy_(res, non_blocking=True)
-        torch.cuda.current_stream(device).synchronize()
-    e2e_s = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_s, world, device)
+        stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
     err = B.spark_attn_error_word(ws)
     if err != 0:
         raise RuntimeError(f"device error word {err:#x}")
 
     tokens = wl.batch * world
     value = tokens * steps / (ms_total * 1e-3)
+    gbs = sb["total"] / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -324,30 +346,28 @@ def bench_ours(args, wl, rank, local, world):
         "config": {"workload": wl.name, "description": wl.description, "batch": wl.batch,
                    "positions": wl.positions if wl.batch <= 8 else
                    {"min": min(wl.positions), "max": max(wl.positions), "sum": sum(wl.positions)},
+                   "n_layers": L,
                    "layers": ["full" if s.is_full else "sliding" for s in wl.layers][:8]
-                   + (["..."] if len(wl.layers) > 8 else []),
-                   "n_layers": len(wl.layers),
+                   + (["..."] if L > 8 else []),
                    "parallelism": f"replicas x{world} (independent sequences, no collective)",
+                   "launch": "CUDA graph per step" if use_graph else "direct calls",
                    "l2": f"{copies} rotating copies of weights+caches ({copies * sb['total'] / 1e6:.0f} MB) "
                          f"vs {l2 / 1e6:.0f} MB L2"},
         "steps_per_s": round(1e3 / ms_per_step * world, 3),
         "hbm_bytes_per_step": sb["total"],
-        "hbm_gbs": round(sb["total"] / (ms_per_step * 1e-3) / 1e9, 1),
-        "hbm_frac": round(sb["total"] / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-        "hbm_peak_gbs": peaks["hbm_gbs"],
-        "hbm_peak_source": peaks["source"],
+        "hbm_gbs": round(gbs, 1),
+        "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
         "roofline": {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "bytes_per_launch": per_launch_bytes,
+                     "bytes_per_launch": int(per_launch[top]),
                      "avg_launch_us": round(kavg[top] * 1e3, 3)},
-        "kernels": {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": launches_per_step[k],
-                        "share": round(share[k] / tot, 4),
-                        "bytes_per_launch": sb["per_kernel"][k] // len(wl.layers),
-                        "gbs": round(sb["per_kernel"][k] / len(wl.layers) / (kavg[k] * 1e-3) / 1e9, 1)}
-                    for k in kavg},
+        "kernels": {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": L,
+                        "share": round(share[k] / tot, 4), "bytes_per_launch": int(per_launch[k]),
+                        "gbs": round(per_launch[k] / (kavg[k] * 1e-3) / 1e9, 1)} for k in STAGES},
         "e2e": {"value": round(tokens * e2e_steps / e2e_s, 3), "unit": "tokens/s",
-                "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * H * 4},
+                "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * H * 4,
+                "launch": "direct calls, synchronised every step"},
         "gpu_launches": kernels_per_step * steps,
         "clocks": clocks,
     }
@@ -422,6 +442,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--copies", type=int, default=0, help="rotating input copies (0: enough to beat L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch steps directly instead of graph replay")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, local, world = dist_env()

@@ -80,11 +80,9 @@ _SIGNATURES = {
                                          ctypes.POINTER(SparkKvLayer), ctypes.c_int32,
                                          ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P,
                                          ctypes.c_size_t, _P]),
-    "spark_dbg_qkv_gate": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkLayerWeights),
-                                          ctypes.c_int32, _P, _P]),
-    "spark_dbg_split_rope": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
-                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
-                                            _P, _P]),
+    "spark_dbg_qkv_rope": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkLayerWeights),
+                                          ctypes.POINTER(SparkKvLayer), ctypes.c_int32,
+                                          ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P, _P]),
     "spark_dbg_attention": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                            _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
@@ -238,21 +236,15 @@ def spark_attn_decode(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, k
                                     _stream(stream)), "spark_attn_decode")
 
 
-def spark_dbg_qkv_gate(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, qkvg: torch.Tensor,
+def spark_dbg_qkv_rope(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, kv: KvLayer,
+                       layer_class: int, positions, q_rot: torch.Tensor, g_logits: torch.Tensor,
                        stream=None) -> None:
-    wc = weights.to_c()
-    _check(load().spark_dbg_qkv_gate(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32), ctypes.byref(wc),
-                                     int(h.shape[0]), _dev_ptr(qkvg, "qkvg", torch.float32),
-                                     _stream(stream)), "spark_dbg_qkv_gate")
-
-
-def spark_dbg_split_rope(geom: SparkGeom, qkvg: torch.Tensor, kv: KvLayer, layer_class: int, positions,
-                         q_rot: torch.Tensor, stream=None) -> None:
-    kc, pos = kv.to_c(), _positions(positions)
-    _check(load().spark_dbg_split_rope(ctypes.byref(geom), _dev_ptr(qkvg, "qkvg", torch.float32),
-                                       ctypes.byref(kc), int(layer_class), pos, len(positions),
-                                       _dev_ptr(q_rot, "q_rot", torch.float32), _stream(stream)),
-           "spark_dbg_split_rope")
+    wc, kc, pos = weights.to_c(), kv.to_c(), _positions(positions)
+    _check(load().spark_dbg_qkv_rope(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32), ctypes.byref(wc),
+                                     ctypes.byref(kc), int(layer_class), pos, len(positions),
+                                     _dev_ptr(q_rot, "q_rot", torch.float32),
+                                     _dev_ptr(g_logits, "g_logits", torch.float32), _stream(stream)),
+           "spark_dbg_qkv_rope")
 
 
 def spark_dbg_attention(geom: SparkGeom, q_rot: torch.Tensor, kv: KvLayer, layer_class: int, positions,
@@ -265,13 +257,14 @@ def spark_dbg_attention(geom: SparkGeom, q_rot: torch.Tensor, kv: KvLayer, layer
                                       _stream(stream)), "spark_dbg_attention")
 
 
-def spark_dbg_gate_oproj(geom: SparkGeom, a: torch.Tensor, qkvg: torch.Tensor, h: torch.Tensor,
+def spark_dbg_gate_oproj(geom: SparkGeom, a: torch.Tensor, g_logits: torch.Tensor, h: torch.Tensor,
                          weights: LayerWeights, out: torch.Tensor, stream=None) -> None:
     wc = weights.to_c()
     _check(load().spark_dbg_gate_oproj(ctypes.byref(geom), _dev_ptr(a, "a", torch.float32),
-                                       _dev_ptr(qkvg, "qkvg", torch.float32), _dev_ptr(h, "h", torch.float32),
-                                       ctypes.byref(wc), int(h.shape[0]), _dev_ptr(out, "out", torch.float32),
-                                       _stream(stream)), "spark_dbg_gate_oproj")
+                                       _dev_ptr(g_logits, "g_logits", torch.float32),
+                                       _dev_ptr(h, "h", torch.float32), ctypes.byref(wc), int(h.shape[0]),
+                                       _dev_ptr(out, "out", torch.float32), _stream(stream)),
+           "spark_dbg_gate_oproj")
 
 
 def spark_attn_status_string(status: int) -> str:

@@ -157,32 +157,24 @@ int spark_attn_error_word(void* workspace, size_t workspace_bytes, uint32_t* wor
   return cuda_status(e);
 }
 
-int spark_dbg_qkv_gate(const spark_geom* g, const float* h, const spark_layer_weights* w,
-                       int32_t batch, float* qkvg, void* stream) {
+int spark_dbg_qkv_rope(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                       const spark_kv_layer* kv, int32_t layer_class, const int32_t* positions,
+                       int32_t batch, float* q_rot, float* g_logits, void* stream) {
   int s;
   if ((s = check_geom(g)) != SPARK_OK) return s;
   if ((s = check_weights(w, true, false)) != SPARK_OK) return s;
   if ((s = check_batch(batch)) != SPARK_OK) return s;
-  if (!h || !qkvg || !aligned16(h) || !aligned16(qkvg)) return SPARK_ERR_INVALID_ARG;
-  return cuda_status(launch_qkv_gate(w->dtype, h, w->norm_w, w->qkv_w, w->g_w, qkvg, g->hidden,
-                                     g->n_q, g->n_kv, batch, g->eps, (cudaStream_t)stream));
-}
-
-int spark_dbg_split_rope(const spark_geom* g, const float* qkvg, const spark_kv_layer* kv,
-                         int32_t layer_class, const int32_t* positions, int32_t batch,
-                         float* q_rot, void* stream) {
-  int s;
-  if ((s = check_geom(g)) != SPARK_OK) return s;
-  if ((s = check_batch(batch)) != SPARK_OK) return s;
   if ((s = check_kv(g, kv, layer_class, positions, batch)) != SPARK_OK) return s;
-  if (!qkvg || !q_rot || !aligned16(qkvg) || !aligned16(q_rot)) return SPARK_ERR_INVALID_ARG;
-  // no workspace here: the kernel's own bounds check has no error word to set
+  if (!h || !q_rot || !g_logits || !aligned16(h) || !aligned16(q_rot) || !aligned16(g_logits))
+    return SPARK_ERR_INVALID_ARG;
   int rotary_dim;
   double theta;
   rope_for(g, layer_class, &rotary_dim, &theta);
-  return cuda_status(launch_split_rope(kv->dtype, qkvg, q_rot, kv->k, kv->v, g->n_q, g->n_kv,
-                                       kv->capacity, kv->ring_capacity, rotary_dim, theta,
-                                       positions, batch, nullptr, (cudaStream_t)stream));
+  // no workspace here: the kernel's own bounds check has no error word to set
+  return cuda_status(launch_qkv_rope(w->dtype, kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot,
+                                     kv->k, kv->v, g_logits, nullptr, g->hidden, g->n_q, g->n_kv,
+                                     batch, kv->capacity, kv->ring_capacity, rotary_dim, theta,
+                                     g->eps, positions, (cudaStream_t)stream));
 }
 
 int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_layer* kv,
@@ -200,20 +192,21 @@ int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_
       kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity, kv->ring_capacity,
       layer_class == SPARK_FULL, g->window, g->scale, positions, batch, a,
       ws_at<float>(workspace, L.part), ws_at<uint32_t>(workspace, L.counters),
-      ws_at<uint32_t>(workspace, L.err), n_ctas, (cudaStream_t)stream));
+      ws_at<uint32_t>(workspace, L.err), n_ctas, nullptr, 0, (cudaStream_t)stream));
 }
 
-int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* qkvg, const float* h,
-                         const spark_layer_weights* w, int32_t batch, float* out, void* stream) {
+int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* g_logits,
+                         const float* h, const spark_layer_weights* w, int32_t batch, float* out,
+                         void* stream) {
   int s;
   if ((s = check_geom(g)) != SPARK_OK) return s;
   if ((s = check_weights(w, false, true)) != SPARK_OK) return s;
   if ((s = check_batch(batch)) != SPARK_OK) return s;
-  if (!a || !qkvg || !h || !out || !aligned16(a) || !aligned16(qkvg) || !aligned16(h) ||
+  if (!a || !g_logits || !h || !out || !aligned16(a) || !aligned16(g_logits) || !aligned16(h) ||
       !aligned16(out))
     return SPARK_ERR_INVALID_ARG;
-  return cuda_status(launch_gate_oproj(w->dtype, a, qkvg, h, w->o_w, out, g->hidden, g->n_q,
-                                       g->n_kv, batch, (cudaStream_t)stream));
+  return cuda_status(launch_oproj(w->dtype, a, g_logits, h, w->o_w, out, nullptr, g->hidden, g->n_q,
+                                  batch, (cudaStream_t)stream));
 }
 
 int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_weights* w,
@@ -229,25 +222,26 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
   if (!h || !out || !aligned16(h) || !aligned16(out)) return SPARK_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(g->n_q, g->n_kv, batch);
   cudaStream_t st = (cudaStream_t)stream;
-  float* qkvg = ws_at<float>(workspace, L.qkvg);
+  float* g_logits = ws_at<float>(workspace, L.g);
   float* q_rot = ws_at<float>(workspace, L.q_rot);
   float* a = ws_at<float>(workspace, L.a);
   uint32_t* err = ws_at<uint32_t>(workspace, L.err);
   int rotary_dim;
   double theta;
   rope_for(g, layer_class, &rotary_dim, &theta);
-  cudaError_t e = launch_qkv_gate(w->dtype, h, w->norm_w, w->qkv_w, w->g_w, qkvg, g->hidden,
-                                  g->n_q, g->n_kv, batch, g->eps, st);
-  if (e == cudaSuccess)
-    e = launch_split_rope(kv->dtype, qkvg, q_rot, kv->k, kv->v, g->n_q, g->n_kv, kv->capacity,
-                          kv->ring_capacity, rotary_dim, theta, positions, batch, err, st);
+  const size_t wbytes = w->dtype == SPARK_BF16 ? 2 : 4;
+  cudaError_t e = launch_qkv_rope(w->dtype, kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot,
+                                  kv->k, kv->v, g_logits, err, g->hidden, g->n_q, g->n_kv, batch,
+                                  kv->capacity, kv->ring_capacity, rotary_dim, theta, g->eps,
+                                  positions, st);
   if (e == cudaSuccess)
     e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity,
                          kv->ring_capacity, layer_class == SPARK_FULL, g->window, g->scale,
                          positions, batch, a, ws_at<float>(workspace, L.part),
-                         ws_at<uint32_t>(workspace, L.counters), err, 0, st);
+                         ws_at<uint32_t>(workspace, L.counters), err, 0, w->o_w,
+                         (size_t)g->hidden * g->n_q * g->head_dim * wbytes, st);
   if (e == cudaSuccess)
-    e = launch_gate_oproj(w->dtype, a, qkvg, h, w->o_w, out, g->hidden, g->n_q, g->n_kv, batch, st);
+    e = launch_oproj(w->dtype, a, g_logits, h, w->o_w, out, err, g->hidden, g->n_q, batch, st);
   return cuda_status(e);
 }
 

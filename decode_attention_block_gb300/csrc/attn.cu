@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float* __restrict__ q_rot, float* __restrict__ a_out,
                   float* __restrict__ part, uint32_t* __restrict__ counters, uint32_t* err,
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
-                  int window, float scale_log2, const __grid_constant__ AttnArgs<MAXB> args) {
+                  int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
+                  const __grid_constant__ AttnArgs<MAXB> args) {
   using S = Smem<CT>;
   constexpr int NS = S::kStages;
   extern __shared__ unsigned char smem_raw[];
@@ -166,8 +167,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
+    // A hint for the kernel after this one: its weights (o_proj) do not
+    // depend on attention, so this CTA pulls its share of them into L2 while
+    // HBM is otherwise idle.
+    if (l2_pf_bytes > 0) {
+      const int64_t lo = (l2_pf_bytes * blockIdx.x / gridDim.x) & ~int64_t(15);
+      const int64_t hi = (l2_pf_bytes * (blockIdx.x + 1) / gridDim.x) & ~int64_t(15);
+      for (int64_t o = lo; o < hi; o += 65536) {
+        const int64_t n = hi - o < 65536 ? hi - o : 65536;
+        bulk_prefetch_l2(l2_pf + o, (uint32_t)n);
+      }
+    }
   }
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // q_rot and the new cache rows come from the previous kernel
 
   const int64_t total = (int64_t)n_kv * args.prefix[batch];
   const int G = gridDim.x, c = blockIdx.x;
@@ -495,7 +509,8 @@ template <typename CT, int MAXB>
 cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_kv,
                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
                      const int32_t* positions, int batch, float* a, float* part,
-                     uint32_t* counters, uint32_t* err, int n_ctas, cudaStream_t st) {
+                     uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
+                     size_t l2_pf_bytes, cudaStream_t st) {
   using S = Smem<CT>;
   AttnArgs<MAXB> args;
   args.prefix[0] = 0;
@@ -521,26 +536,26 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<G, kThreads, S::kAlloc, st>>>(mk, mv, q_rot, a, part, counters, err, batch, n_kv,
-                                       capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
-                                       args);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(G), dim3(kThreads), S::kAlloc, st, mk, mv, q_rot, a, part, counters,
+                    err, batch, n_kv, capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
+                    static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
 }
 
 template <typename CT>
 cudaError_t launch_ct(const float* q_rot, const void* kc, const void* vc, int n_kv,
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
-                      uint32_t* counters, uint32_t* err, int n_ctas, cudaStream_t st) {
+                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
+                      size_t l2_pf_bytes, cudaStream_t st) {
   if (batch <= 8)
     return launch_t<CT, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                           positions, batch, a, part, counters, err, n_ctas, st);
+                           positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
   if (batch <= 64)
     return launch_t<CT, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                            positions, batch, a, part, counters, err, n_ctas, st);
+                            positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
   return launch_t<CT, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
                                        window, scale, positions, batch, a, part, counters, err,
-                                       n_ctas, st);
+                                       n_ctas, l2_pf, l2_pf_bytes, st);
 }
 
 }  // namespace
@@ -549,12 +564,12 @@ cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, con
                              int n_kv, int64_t capacity, int ring_capacity, bool full,
                              int window, float scale, const int32_t* positions, int batch,
                              float* a, float* part, uint32_t* counters, uint32_t* err,
-                             int n_ctas, cudaStream_t st) {
+                             int n_ctas, const void* l2_pf, size_t l2_pf_bytes, cudaStream_t st) {
   if (cdtype == SPARK_BF16)
     return launch_ct<__nv_bfloat16>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
-                                    scale, positions, batch, a, part, counters, err, n_ctas, st);
+                                    scale, positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
   return launch_ct<float>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                          positions, batch, a, part, counters, err, n_ctas, st);
+                          positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
 }
 
 }  // namespace spark

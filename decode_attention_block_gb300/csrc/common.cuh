@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/spark_attn.h"
 
 namespace spark {
@@ -66,16 +68,14 @@ __host__ __device__ inline int64_t write_slot_of(int64_t position, int64_t ring_
 struct WsLayout {
   size_t err = 0;       // uint32 error word
   size_t counters = 0;  // uint32 [batch * n_kv] merge tickets
-  size_t qkvg = 0;      // f32 [batch][qkvg_ld]
-  size_t q_rot = 0;     // f32 [batch][q_dim]
-  size_t a = 0;         // f32 [batch][q_dim]
+  size_t g = 0;         // f32 [batch][n_q] gate logits
+  size_t q_rot = 0;     // f32 [batch][q_dim] rotated queries
+  size_t a = 0;         // f32 [batch][q_dim] attention output
   size_t part = 0;      // f32 [kMaxAttnCtas + batch * n_kv][kPartFloats]
   size_t total = 0;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-inline int qkvg_ld(int n_q, int n_kv) { return n_q * kHeadDim + 2 * n_kv * kHeadDim + n_q; }
 
 inline WsLayout ws_layout(int n_q, int n_kv, int batch) {
   WsLayout L;
@@ -83,8 +83,8 @@ inline WsLayout ws_layout(int n_q, int n_kv, int batch) {
   L.err = 0;
   L.counters = off;
   off = align_up(off + sizeof(uint32_t) * (size_t)batch * n_kv, 256);
-  L.qkvg = off;
-  off = align_up(off + sizeof(float) * (size_t)batch * qkvg_ld(n_q, n_kv), 256);
+  L.g = off;
+  off = align_up(off + sizeof(float) * (size_t)batch * n_q, 256);
   L.q_rot = off;
   off = align_up(off + sizeof(float) * (size_t)batch * n_q * kHeadDim, 256);
   L.a = off;
@@ -93,6 +93,25 @@ inline WsLayout ws_layout(int n_q, int n_kv, int batch) {
   off = align_up(off + sizeof(float) * (size_t)(kMaxAttnCtas + (size_t)batch * n_kv) * kPartFloats, 256);
   L.total = off;
   return L;
+}
+
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while its predecessor in the stream finishes; it calls pdl_wait() before
+// touching anything the predecessor writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------
@@ -171,6 +190,37 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+
+// 1-D bulk copy global -> shared of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Hint: bring `bytes` (multiple of 16) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Hint: bring one tile of a tensor map into L2.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible (a no-op without PDL) ...
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and let the next grid in the stream start launching its prologue.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

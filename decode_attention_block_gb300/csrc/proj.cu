@@ -1,289 +1,570 @@
-// proj.cu -- the block's two weight-streaming projections.
+// proj.cu -- the block's two weight-streaming projections, each fused with
+// the small steps around it.
 //
-//  * qkv_gate: input RMSNorm fused with the q_k_v_proj GEMV and the g_proj
-//    GEMV (turbospark-runtime 0.3.0, src/families/spark/attn.rs,
-//    encode_attention_block: "the fused projection, as one GEMV" and "the
-//    gate's projection" that reads the same normed x; src/families/spark/
-//    mod.rs, "One decoder layer, transcribed": x = rms(h, w, 1e-6), plain w).
-//  * gate_oproj: the headwise sigmoid gate fused with the o_proj GEMV and the
-//    raw residual add (attn.rs: encode_sigmoid_head_gate_mul before o_proj;
-//    mod.rs: encode_residual_add).
+//  * qkv_rope: input RMSNorm + q_k_v_proj + g_proj + the split + per-class
+//    NeoX rope + the cache-row write of k and v (turbospark-runtime 0.3.0,
+//    src/families/spark/attn.rs, encode_attention_block: the fused
+//    projection, the gate's projection reading the same normed x,
+//    encode_split_qkv with k and v landing in their cache slots,
+//    encode_rope_neox_subdim on q and on the k slot; module doc items 1-2;
+//    src/families/spark/mod.rs, "One decoder layer, transcribed":
+//    x = rms(h, w, 1e-6) with a plain w).
+//  * oproj: the headwise sigmoid gate + o_proj + the raw residual add
+//    (attn.rs: encode_sigmoid_head_gate_mul before o_proj; mod.rs:
+//    encode_residual_add).
 //
-// Both are HBM-bound at small batch: each weight byte is read once and used
-// for `batch` FMAs.  One warp owns kRowsPerWarp rows, streams them with
-// 16-byte non-allocating loads and keeps the normalised activation vector of
-// up to kBatchChunk sequences in shared memory; larger batches are processed
-// in chunks of kBatchChunk.
+// Both are HBM-bound at small batch: every weight byte is read once and used
+// for `nb` multiply-adds.  Each CTA (one per SM) owns an equal contiguous
+// share of the weight rows.  Every warp streams its rows with 1-D bulk copies
+// (cp.async.bulk) into a private double buffer in shared memory, so a whole
+// CTA keeps ~160 KB of weights in flight, and the first copies are issued
+// before the kernel waits for its predecessor (programmatic dependent
+// launch): the weight stream does not depend on the previous kernel.
+//
+// The RMSNorm needs no pass before the GEMV: rms(h) scales every output of a
+// row by the same 1/sqrt(mean(h^2) + eps), so the warps dot the rows with
+// h * w and the scale is applied in the epilogue.
+//
+// qkv_rope processes rows in pairs.  For a rotated q or k head the pair is
+// (i, i + r/2) -- the two rows NeoX rope mixes -- so the epilogue rotates the
+// two finished dot products and writes q (fp32) or k (cache type) directly;
+// v rows, rows past the rotary width and g rows are paired as neighbours.
+#include <math.h>
+
 #include "launch.h"
 
 namespace spark {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerWarp = 2;
-constexpr int kBatchChunk = 4;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr size_t kSmemBudget = 220 * 1024;
 
 template <typename WT>
 struct Chunk;
 template <>
 struct Chunk<float> {
   static constexpr int kElems = 4;
-  __device__ __forceinline__ static void unpack(uint4 v, float* f) {
-    f[0] = __uint_as_float(v.x);
-    f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z);
-    f[3] = __uint_as_float(v.w);
-  }
 };
 template <>
 struct Chunk<__nv_bfloat16> {
   static constexpr int kElems = 8;
-  __device__ __forceinline__ static void unpack(uint4 v, float* f) {
-    float2 a = bf16x2_to_f32x2(v.x), b = bf16x2_to_f32x2(v.y);
-    float2 c = bf16x2_to_f32x2(v.z), d = bf16x2_to_f32x2(v.w);
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
-  }
 };
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_elem(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  v = warp_sum(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int i = 0; i < kWarps; ++i) t += red[i];
-  return t;
+// Activation vectors live in shared memory permuted so that lane l's values
+// for its 16-byte weight chunk c = l + 32 i are read as consecutive float4s
+// across lanes (no bank conflicts): element n of chunk c sits at float4
+// ((i * E/4 + (n % E) / 4) * 32 + l), component n % 4.
+template <int E>
+__device__ __forceinline__ int xperm_index(int n) {
+  const int c = n / E, l = c & 31, i = c >> 5, hq = (n % E) >> 2;
+  return ((i * (E / 4) + hq) * 32 + l) * 4 + (n & 3);
 }
 
-// acc[r][b] += W[row0 + r, :] . xs[b, :] for r < nrows, b < nb; the warp's
-// lanes stride over 16-byte chunks of the rows, four chunks in flight per row.
+// sum over the chunk of w[k] * x[k], accumulated pairwise into acc
 template <typename WT>
-__device__ __forceinline__ void warp_rows_dot(const WT* __restrict__ W, int64_t ld, int row0,
-                                              int nrows, const float* __restrict__ xs, int cols,
-                                              int nb, float (&acc)[kRowsPerWarp][kBatchChunk]) {
+__device__ __forceinline__ void dot_chunk(uint4 w, const float4* xp, float2& acc);
+
+template <>
+__device__ __forceinline__ void dot_chunk<__nv_bfloat16>(uint4 w, const float4* xp, float2& acc) {
+  const float4 x0 = xp[0], x1 = xp[32];
+  acc = ffma2(bf16x2_to_f32x2(w.x), make_float2(x0.x, x0.y), acc);
+  acc = ffma2(bf16x2_to_f32x2(w.y), make_float2(x0.z, x0.w), acc);
+  acc = ffma2(bf16x2_to_f32x2(w.z), make_float2(x1.x, x1.y), acc);
+  acc = ffma2(bf16x2_to_f32x2(w.w), make_float2(x1.z, x1.w), acc);
+}
+
+template <>
+__device__ __forceinline__ void dot_chunk<float>(uint4 w, const float4* xp, float2& acc) {
+  const float4 x0 = xp[0];
+  acc = ffma2(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), make_float2(x0.x, x0.y), acc);
+  acc = ffma2(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), make_float2(x0.z, x0.w), acc);
+}
+
+// cos / sin of position * inv_freq with the product reduced modulo 2*pi in
+// fp64 (at position 131072 an fp32 angle would be off by ~1e-2 rad)
+__device__ __forceinline__ void rope_cos_sin(int32_t pos, double inv_freq, float* c, float* s) {
+  constexpr double kTwoPiHi = 6.283185307179586232;    // 2*pi rounded to double
+  constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
+  constexpr double kInvTwoPi = 0.15915494309189533577;
+  const double phi = (double)pos * inv_freq;
+  const double n = rint(phi * kInvTwoPi);
+  double r = fma(-n, kTwoPiHi, phi);
+  r = fma(-n, kTwoPiLo, r);
+  sincosf((float)r, s, c);
+}
+
+template <int NB>
+struct QkvArgs {
+  double inv_freq[kHeadDim / 2];  // theta^(-2i/r), i < r/2
+  int32_t pos[NB];
+};
+
+enum RowKind { kQ = 0, kK = 1, kV = 2, kG = 3 };
+
+struct Unit {
+  int row_a, row_b;  // rows of [q_k_v_proj; g_proj]
+  int kind, head;    // head index within its kind
+  int da, db;        // output dims of the two rows (within the head, or g index)
+  int pair;          // rope pair index (-1: no rotation)
+};
+
+__device__ __forceinline__ Unit unit_of(int u, int n_q, int n_kv, int rotary_dim) {
+  Unit x;
+  const int n_heads = n_q + 2 * n_kv;
+  if (u < n_heads * (kHeadDim / 2)) {
+    const int hd = u / (kHeadDim / 2), t = u % (kHeadDim / 2);
+    x.kind = hd < n_q ? kQ : (hd < n_q + n_kv ? kK : kV);
+    x.head = x.kind == kQ ? hd : (x.kind == kK ? hd - n_q : hd - n_q - n_kv);
+    const int half = rotary_dim / 2;
+    if (x.kind != kV && t < half) {
+      x.da = t;
+      x.db = t + half;
+      x.pair = t;
+    } else {
+      x.da = x.kind == kV ? 2 * t : rotary_dim + 2 * (t - half);
+      x.db = x.da + 1;
+      x.pair = -1;
+    }
+    x.row_a = hd * kHeadDim + x.da;
+    x.row_b = hd * kHeadDim + x.db;
+  } else {
+    const int gi = u - n_heads * (kHeadDim / 2);
+    x.kind = kG;
+    x.head = 0;
+    x.da = 2 * gi;
+    x.db = 2 * gi + 1;
+    x.pair = -1;
+    x.row_a = n_heads * kHeadDim + x.da;
+    x.row_b = x.row_a + 1;
+  }
+  return x;
+}
+
+// ---------------------------------------------------------------------------
+// per-warp row streaming shared by both kernels
+// ---------------------------------------------------------------------------
+
+// Wait for this warp's stage, bounded; on time-out raise the block's abort
+// flag and the error word.  Returns false if the stage must not be read.
+__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           uint32_t* err) {
+  if (mbar_wait_bounded(bar, parity, abort_flag, kWaitLimitNs)) return true;
+  if ((threadIdx.x & 31) == 0 && !*abort_flag) {
+    *abort_flag = 1;
+    if (err) atomicOr(err, kErrWaitTimeout);
+  }
+  return false;
+}
+
+// acc[b] (b < NB) += row . x_b for one weight row held in shared memory
+template <typename WT, int NB>
+__device__ __forceinline__ void row_dot(const unsigned char* row, const float* xs, int xfloats,
+                                        int nchunk, float2 (&acc)[NB]) {
   constexpr int E = Chunk<WT>::kElems;
-  constexpr int U = 4;
   const int lane = threadIdx.x & 31;
-  const int nchunk = cols / E;
-  const WT* rp[kRowsPerWarp];
+  for (int c = lane, i = 0; c < nchunk; c += 32, ++i) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + (size_t)c * 16);
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) rp[r] = W + (int64_t)(row0 + (r < nrows ? r : 0)) * ld;
+    for (int b = 0; b < NB; ++b) {
+      const float4* xp = reinterpret_cast<const float4*>(xs + b * xfloats) + i * (E / 4) * 32 + lane;
+      dot_chunk<WT>(w, xp, acc[b]);
+    }
+  }
+}
 
-  int c = lane;
-  for (; c + 32 * (U - 1) < nchunk; c += 32 * U) {
-    uint4 wv[U][kRowsPerWarp];
+// two rows sharing one pass over the activation
+template <typename WT, int NB>
+__device__ __forceinline__ void row_dot2(const unsigned char* ra, const unsigned char* rb,
+                                         const float* xs, int xfloats, int nchunk,
+                                         float2 (&acc_a)[NB], float2 (&acc_b)[NB]) {
+  constexpr int E = Chunk<WT>::kElems;
+  const int lane = threadIdx.x & 31;
+#pragma unroll 2
+  for (int c = lane, i = 0; c < nchunk; c += 32, ++i) {
+    const uint4 wa = *reinterpret_cast<const uint4*>(ra + (size_t)c * 16);
+    const uint4 wb = *reinterpret_cast<const uint4*>(rb + (size_t)c * 16);
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int b = 0; b < NB; ++b) {
+      const float4* xp = reinterpret_cast<const float4*>(xs + b * xfloats) + i * (E / 4) * 32 + lane;
+      dot_chunk<WT>(wa, xp, acc_a[b]);
+      dot_chunk<WT>(wb, xp, acc_b[b]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm + q_k_v_proj + g_proj + rope + cache write
+// ---------------------------------------------------------------------------
+template <typename WT, typename CT, int NB>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_qkv_rope(const float* __restrict__ h, const WT* __restrict__ norm_w,
+               const WT* __restrict__ qkv_w, const WT* __restrict__ g_w, float* __restrict__ q_rot,
+               CT* __restrict__ kc, CT* __restrict__ vc, float* __restrict__ g_out, uint32_t* err,
+               int hidden, int n_q, int n_kv, int nb, int64_t capacity, int ring_capacity,
+               int rotary_dim, int stages, float eps, const __grid_constant__ QkvArgs<NB> args) {
+  constexpr int E = Chunk<WT>::kElems;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = hidden / E;
+  const int xfloats = ((nchunk + 31) / 32) * 32 * E;  // one permuted activation vector
+  const size_t row_bytes = (size_t)hidden * sizeof(WT);
+  float* xs = reinterpret_cast<float*>(smem);         // [NB][xfloats]
+  unsigned char* my_stages =
+      smem + sizeof(float) * NB * xfloats + (size_t)warp * stages * 2 * row_bytes;
+  __shared__ uint64_t bars[kWarps][2];
+  __shared__ float red[kWarps][NB];
+  __shared__ float inv_rms[NB];
+  __shared__ int abort_flag;
+
+  const int n_heads = n_q + 2 * n_kv;
+  const int n_units = n_heads * (kHeadDim / 2) + n_q / 2;
+  const int rows_qkv = n_heads * kHeadDim;
+  const int u0 = (int)((int64_t)n_units * blockIdx.x / gridDim.x);
+  const int u1 = (int)((int64_t)n_units * (blockIdx.x + 1) / gridDim.x);
+  const int my_first = u0 + warp;
+  const int my_count = my_first < u1 ? (u1 - my_first + kWarps - 1) / kWarps : 0;
+
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w)
+      for (int s = 0; s < 2; ++s) mbar_init(&bars[w][s], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto row_ptr = [&](int r) -> const WT* {
+    return r < rows_qkv ? qkv_w + (int64_t)r * hidden : g_w + (int64_t)(r - rows_qkv) * hidden;
+  };
+  auto issue = [&](int i) {  // lane 0: bring unit i of this warp into stage i % stages
+    const Unit un = unit_of(my_first + i * kWarps, n_q, n_kv, rotary_dim);
+    const int s = i % stages;
+    unsigned char* dst = my_stages + (size_t)s * 2 * row_bytes;
+    mbar_arrive_expect_tx(&bars[warp][s], (uint32_t)(2 * row_bytes));
+    bulk_load(dst, row_ptr(un.row_a), (uint32_t)row_bytes, &bars[warp][s]);
+    bulk_load(dst + row_bytes, row_ptr(un.row_b), (uint32_t)row_bytes, &bars[warp][s]);
+  };
+
+  // the weight stream does not depend on the previous kernel: start it now
+  if (lane == 0)
+    for (int i = 0; i < stages && i < my_count; ++i) issue(i);
+  pdl_trigger();
+  pdl_wait();
+
+  // activations: x = h * w (unscaled) and sum(h^2) per sequence
+  float ss[NB];
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) wv[u][r] = ld_stream_u4(rp[r] + (c + 32 * u) * E);
+  for (int b = 0; b < NB; ++b) ss[b] = 0.f;
+  for (int n = threadIdx.x; n < hidden; n += kThreads) {
+    const float w = to_f32(norm_w[n]);
+    const int pi = xperm_index<E>(n);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float wf[kRowsPerWarp][E];
+    for (int b = 0; b < NB; ++b) {
+      const float v = b < nb ? h[(int64_t)b * hidden + n] : 0.f;
+      ss[b] = fmaf(v, v, ss[b]);
+      xs[b * xfloats + pi] = v * w;
+    }
+  }
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) Chunk<WT>::unpack(wv[u][r], wf[r]);
+  for (int b = 0; b < NB; ++b) {
+    const float v = warp_sum(ss[b]);
+    if (lane == 0) red[warp][b] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < NB) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += red[w][threadIdx.x];
+    inv_rms[threadIdx.x] = 1.0f / sqrtf(t / (float)hidden + eps);
+  }
+  __syncthreads();
+
+  for (int i = 0; i < my_count; ++i) {
+    const int s = i % stages;
+    const uint32_t parity = (uint32_t)((i / stages) & 1);
+    const Unit un = unit_of(my_first + i * kWarps, n_q, n_kv, rotary_dim);
+    float2 acc_a[NB], acc_b[NB];
 #pragma unroll
-      for (int b = 0; b < kBatchChunk; ++b) {
-        if (b < nb) {
-          const float* xp = xs + b * cols + (c + 32 * u) * E;
+    for (int b = 0; b < NB; ++b) acc_a[b] = acc_b[b] = make_float2(0.f, 0.f);
+    const bool ok = wait_stage(&bars[warp][s], parity, &abort_flag, err);
+    if (ok) {
+      const unsigned char* st = my_stages + (size_t)s * 2 * row_bytes;
+      row_dot2<WT, NB>(st, st + row_bytes, xs, xfloats, nchunk, acc_a, acc_b);
+    }
+    __syncwarp();
+    if (ok && lane == 0 && i + stages < my_count) issue(i + stages);
+    if (!ok) continue;
+    float va = 0.f, vb = 0.f;
 #pragma unroll
-          for (int e = 0; e < E; e += 4) {
-            const float4 x4 = *reinterpret_cast<const float4*>(xp + e);
-#pragma unroll
-            for (int r = 0; r < kRowsPerWarp; ++r) {
-              acc[r][b] = fmaf(wf[r][e + 0], x4.x, acc[r][b]);
-              acc[r][b] = fmaf(wf[r][e + 1], x4.y, acc[r][b]);
-              acc[r][b] = fmaf(wf[r][e + 2], x4.z, acc[r][b]);
-              acc[r][b] = fmaf(wf[r][e + 3], x4.w, acc[r][b]);
-            }
-          }
+    for (int b = 0; b < NB; ++b) {
+      const float sa = warp_sum(acc_a[b].x + acc_a[b].y);
+      const float sb = warp_sum(acc_b[b].x + acc_b[b].y);
+      if (lane == b) {
+        va = sa * inv_rms[b];
+        vb = sb * inv_rms[b];
+      }
+    }
+    if (lane < nb) {
+      const int b = lane;
+      if (un.pair >= 0) {
+        float c, sn;
+        rope_cos_sin(args.pos[b], args.inv_freq[un.pair], &c, &sn);
+        const float ra = va * c - vb * sn;
+        const float rb = vb * c + va * sn;
+        va = ra;
+        vb = rb;
+      }
+      if (un.kind == kQ) {
+        float* dst = q_rot + ((int64_t)b * n_q + un.head) * kHeadDim;
+        dst[un.da] = va;
+        dst[un.db] = vb;
+      } else if (un.kind == kG) {
+        g_out[(int64_t)b * n_q + un.da] = va;
+        g_out[(int64_t)b * n_q + un.db] = vb;
+      } else {
+        const int64_t slot = write_slot_of(args.pos[b], ring_capacity);
+        if (args.pos[b] < 0 || slot >= capacity) {  // rejected on the host; never write out of bounds
+          if (err) atomicOr(err, kErrIndex);
+        } else {
+          CT* dst = (un.kind == kK ? kc : vc) + (((int64_t)b * capacity + slot) * n_kv + un.head) * kHeadDim;
+          store_elem(dst + un.da, va);
+          store_elem(dst + un.db, vb);
         }
       }
     }
   }
-  for (; c < nchunk; c += 32) {
-    float wf[kRowsPerWarp][E];
+}
+
+// ---------------------------------------------------------------------------
+// head gate + o_proj + residual
+// ---------------------------------------------------------------------------
+template <typename WT, int NB>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_oproj(const float* __restrict__ a, const float* __restrict__ g, const float* h,
+            const WT* __restrict__ o_w, float* out, uint32_t* err, int hidden, int q_dim, int n_q,
+            int nb, int stages) {
+  constexpr int E = Chunk<WT>::kElems;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = q_dim / E;
+  const int xfloats = ((nchunk + 31) / 32) * 32 * E;
+  const size_t row_bytes = (size_t)q_dim * sizeof(WT);
+  float* xs = reinterpret_cast<float*>(smem);  // [NB][xfloats]
+  unsigned char* my_stages = smem + sizeof(float) * NB * xfloats + (size_t)warp * stages * row_bytes;
+  __shared__ uint64_t bars[kWarps][2];
+  __shared__ int abort_flag;
+
+  const int r0 = (int)((int64_t)hidden * blockIdx.x / gridDim.x);
+  const int r1 = (int)((int64_t)hidden * (blockIdx.x + 1) / gridDim.x);
+  const int my_first = r0 + warp;
+  const int my_count = my_first < r1 ? (r1 - my_first + kWarps - 1) / kWarps : 0;
+
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w)
+      for (int s = 0; s < 2; ++s) mbar_init(&bars[w][s], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int i) {
+    const int s = i % stages;
+    mbar_arrive_expect_tx(&bars[warp][s], (uint32_t)row_bytes);
+    bulk_load(my_stages + (size_t)s * row_bytes, o_w + (int64_t)(my_first + i * kWarps) * q_dim,
+              (uint32_t)row_bytes, &bars[warp][s]);
+  };
+  if (lane == 0)
+    for (int i = 0; i < stages && i < my_count; ++i) issue(i);
+  pdl_trigger();
+  pdl_wait();
+
+  // gated attention output: a * sigmoid(g), one gate scalar per head
+  for (int n = threadIdx.x; n < q_dim; n += kThreads) {
+    const int pi = xperm_index<E>(n);
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) Chunk<WT>::unpack(ld_stream_u4(rp[r] + c * E), wf[r]);
-#pragma unroll
-    for (int b = 0; b < kBatchChunk; ++b) {
+    for (int b = 0; b < NB; ++b) {
+      float v = 0.f;
       if (b < nb) {
-        const float* xp = xs + b * cols + c * E;
-#pragma unroll
-        for (int e = 0; e < E; e += 4) {
-          const float4 x4 = *reinterpret_cast<const float4*>(xp + e);
-#pragma unroll
-          for (int r = 0; r < kRowsPerWarp; ++r) {
-            acc[r][b] = fmaf(wf[r][e + 0], x4.x, acc[r][b]);
-            acc[r][b] = fmaf(wf[r][e + 1], x4.y, acc[r][b]);
-            acc[r][b] = fmaf(wf[r][e + 2], x4.z, acc[r][b]);
-            acc[r][b] = fmaf(wf[r][e + 3], x4.w, acc[r][b]);
-          }
-        }
+        const float z = g[(int64_t)b * n_q + n / kHeadDim];
+        v = a[(int64_t)b * q_dim + n] * (1.0f / (1.0f + expf(-z)));
       }
+      xs[b * xfloats + pi] = v;
+    }
+  }
+  __syncthreads();
+
+  for (int i = 0; i < my_count; ++i) {
+    const int s = i % stages;
+    const uint32_t parity = (uint32_t)((i / stages) & 1);
+    float2 acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = make_float2(0.f, 0.f);
+    const bool ok = wait_stage(&bars[warp][s], parity, &abort_flag, err);
+    if (ok) row_dot<WT, NB>(my_stages + (size_t)s * row_bytes, xs, xfloats, nchunk, acc);
+    __syncwarp();
+    if (ok && lane == 0 && i + stages < my_count) issue(i + stages);
+    if (!ok) continue;
+    const int r = my_first + i * kWarps;
+    float v = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float sb = warp_sum(acc[b].x + acc[b].y);
+      if (lane == b) v = sb;
+    }
+    if (lane < nb) {
+      const int64_t idx = (int64_t)lane * hidden + r;
+      out[idx] = h[idx] + v;  // read and written by the same thread: out may alias h
     }
   }
 }
 
-// Rows [0, rows_qkv) come from q_k_v_proj, rows [rows_qkv, rows_qkv + n_q)
-// from g_proj; rows_qkv is a multiple of kRowsPerWarp, so a warp never
-// straddles the two matrices.
-template <typename WT>
-__global__ void __launch_bounds__(kThreads)
-    k_qkv_gate(const float* __restrict__ h, const WT* __restrict__ norm_w,
-               const WT* __restrict__ qkv_w, const WT* __restrict__ g_w,
-               float* __restrict__ qkvg, int hidden, int rows_qkv, int rows_g, int batch,
-               float eps) {
-  extern __shared__ float4 smem_f4[];
-  float* xs = reinterpret_cast<float*>(smem_f4);  // [kBatchChunk][hidden]
-  __shared__ float red[kWarps];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows_total = rows_qkv + rows_g;
-  const int ld_out = rows_total;
-  const int row0 = (blockIdx.x * kWarps + warp) * kRowsPerWarp;
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
 
-  for (int b0 = 0; b0 < batch; b0 += kBatchChunk) {
-    const int nb = min(kBatchChunk, batch - b0);
-    __syncthreads();
-    for (int bb = 0; bb < nb; ++bb) {
-      const float* hb = h + (int64_t)(b0 + bb) * hidden;
-      float ss = 0.f;
-      for (int i = threadIdx.x; i < hidden; i += kThreads) {
-        const float v = hb[i];
-        ss = fmaf(v, v, ss);
-      }
-      ss = block_sum(ss, red);
-      const float inv = 1.0f / sqrtf(ss / (float)hidden + eps);
-      for (int i = threadIdx.x; i < hidden; i += kThreads)
-        xs[bb * hidden + i] = hb[i] * inv * to_f32(norm_w[i]);
-    }
-    __syncthreads();
-    if (row0 < rows_total) {
-      float acc[kRowsPerWarp][kBatchChunk];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-        for (int b = 0; b < kBatchChunk; ++b) acc[r][b] = 0.f;
-      const bool is_g = row0 >= rows_qkv;
-      const WT* W = is_g ? g_w : qkv_w;
-      const int wrow0 = is_g ? row0 - rows_qkv : row0;
-      const int nrows = min(kRowsPerWarp, (is_g ? rows_g : rows_qkv) - wrow0);
-      warp_rows_dot<WT>(W, hidden, wrow0, nrows, xs, hidden, nb, acc);
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-        for (int b = 0; b < kBatchChunk; ++b) {
-          const float v = warp_sum(acc[r][b]);
-          if (lane == 0 && r < nrows && b < nb) qkvg[(int64_t)(b0 + b) * ld_out + row0 + r] = v;
-        }
-    }
-  }
+// stages per warp that fit next to the activations (1 or 2), 0 if none fits
+int stages_for(size_t stage_bytes, size_t x_bytes) {
+  if (x_bytes + kWarps * 2 * stage_bytes <= kSmemBudget) return 2;
+  if (x_bytes + kWarps * stage_bytes <= kSmemBudget) return 1;
+  return 0;
 }
 
 template <typename WT>
-__global__ void __launch_bounds__(kThreads)
-    k_gate_oproj(const float* __restrict__ a, const float* __restrict__ qkvg, int qkvg_ld,
-                 int g_col, const float* h, const WT* __restrict__ o_w, float* out, int hidden,
-                 int q_dim, int batch) {
-  extern __shared__ float4 smem_f4[];
-  float* xs = reinterpret_cast<float*>(smem_f4);  // [kBatchChunk][q_dim]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = (blockIdx.x * kWarps + warp) * kRowsPerWarp;
-
-  for (int b0 = 0; b0 < batch; b0 += kBatchChunk) {
-    const int nb = min(kBatchChunk, batch - b0);
-    __syncthreads();
-    for (int bb = 0; bb < nb; ++bb) {
-      const float* ab = a + (int64_t)(b0 + bb) * q_dim;
-      const float* gb = qkvg + (int64_t)(b0 + bb) * qkvg_ld + g_col;
-      for (int i = threadIdx.x; i < q_dim; i += kThreads) {
-        const float z = gb[i / kHeadDim];
-        xs[bb * q_dim + i] = ab[i] * (1.0f / (1.0f + expf(-z)));
-      }
-    }
-    __syncthreads();
-    if (row0 < hidden) {
-      float acc[kRowsPerWarp][kBatchChunk];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-        for (int b = 0; b < kBatchChunk; ++b) acc[r][b] = 0.f;
-      const int nrows = min(kRowsPerWarp, hidden - row0);
-      warp_rows_dot<WT>(o_w, q_dim, row0, nrows, xs, q_dim, nb, acc);
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-        for (int b = 0; b < kBatchChunk; ++b) {
-          const float v = warp_sum(acc[r][b]);
-          if (lane == 0 && r < nrows && b < nb) {
-            const int64_t i = (int64_t)(b0 + b) * hidden + row0 + r;
-            out[i] = h[i] + v;  // each element read and written by the same thread: out may alias h
-          }
-        }
-    }
-  }
+size_t xbytes(int cols, int nb) {
+  constexpr int E = Chunk<WT>::kElems;
+  const int nchunk = cols / E;
+  return sizeof(float) * (size_t)nb * ((nchunk + 31) / 32) * 32 * E;
 }
 
-template <typename Kern>
-cudaError_t set_smem(Kern k, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+template <typename WT, typename CT, int NB>
+cudaError_t qkv_launch(const float* h, const void* norm_w, const void* qkv_w, const void* g_w,
+                       float* q_rot, void* kc, void* vc, float* g_out, uint32_t* err, int hidden,
+                       int n_q, int n_kv, int nb, int64_t capacity, int ring_capacity,
+                       int rotary_dim, double theta, float eps, const int32_t* positions,
+                       cudaStream_t st) {
+  QkvArgs<NB> args;
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    args.inv_freq[i] = i < rotary_dim / 2 ? pow(theta, -2.0 * i / (double)rotary_dim) : 0.0;
+  for (int b = 0; b < NB; ++b) args.pos[b] = b < nb ? positions[b] : 0;
+  const size_t row_bytes = (size_t)hidden * sizeof(WT);
+  const size_t xb = xbytes<WT>(hidden, NB);
+  const int stages = stages_for(2 * row_bytes, xb);
+  if (stages == 0) return cudaErrorInvalidConfiguration;
+  const size_t smem = xb + (size_t)kWarps * stages * 2 * row_bytes;
+  auto kern = k_qkv_rope<WT, CT, NB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int n_units = (n_q + 2 * n_kv) * (kHeadDim / 2) + n_q / 2;
+  int grid = device_sm_count();
+  if (grid > n_units) grid = n_units;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, h, (const WT*)norm_w,
+                    (const WT*)qkv_w, (const WT*)g_w, q_rot, (CT*)kc, (CT*)vc, g_out, err, hidden,
+                    n_q, n_kv, nb, capacity, ring_capacity, rotary_dim, stages, eps, args);
 }
+
+template <typename WT, typename CT>
+cudaError_t qkv_chunk(int nb, const float* h, const void* norm_w, const void* qkv_w,
+                      const void* g_w, float* q_rot, void* kc, void* vc, float* g_out,
+                      uint32_t* err, int hidden, int n_q, int n_kv, int64_t capacity,
+                      int ring_capacity, int rotary_dim, double theta, float eps,
+                      const int32_t* positions, cudaStream_t st) {
+#define SPARK_QKV(NBV)                                                                           \
+  return qkv_launch<WT, CT, NBV>(h, norm_w, qkv_w, g_w, q_rot, kc, vc, g_out, err, hidden, n_q, \
+                                 n_kv, nb, capacity, ring_capacity, rotary_dim, theta, eps,     \
+                                 positions, st)
+  if (nb == 1) SPARK_QKV(1);
+  if (nb == 2) SPARK_QKV(2);
+  SPARK_QKV(4);
+#undef SPARK_QKV
+}
+
+template <typename WT, int NB>
+cudaError_t oproj_launch(const float* a, const float* g, const float* h, const void* o_w,
+                         float* out, uint32_t* err, int hidden, int n_q, int nb, cudaStream_t st) {
+  const int q_dim = n_q * kHeadDim;
+  const size_t row_bytes = (size_t)q_dim * sizeof(WT);
+  const size_t xb = xbytes<WT>(q_dim, NB);
+  const int stages = stages_for(row_bytes, xb);
+  if (stages == 0) return cudaErrorInvalidConfiguration;
+  const size_t smem = xb + (size_t)kWarps * stages * row_bytes;
+  auto kern = k_oproj<WT, NB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = device_sm_count();
+  if (grid > hidden) grid = hidden;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, a, g, h, (const WT*)o_w, out, err,
+                    hidden, q_dim, n_q, nb, stages);
+}
+
+template <typename WT>
+cudaError_t oproj_chunk(int nb, const float* a, const float* g, const float* h, const void* o_w,
+                        float* out, uint32_t* err, int hidden, int n_q, cudaStream_t st) {
+  if (nb == 1) return oproj_launch<WT, 1>(a, g, h, o_w, out, err, hidden, n_q, nb, st);
+  if (nb == 2) return oproj_launch<WT, 2>(a, g, h, o_w, out, err, hidden, n_q, nb, st);
+  return oproj_launch<WT, 4>(a, g, h, o_w, out, err, hidden, n_q, nb, st);
+}
+
+constexpr int kMaxChunk = 4;
 
 }  // namespace
 
-cudaError_t launch_qkv_gate(int wdtype, const float* h, const void* norm_w, const void* qkv_w,
-                            const void* g_w, float* qkvg, int hidden, int n_q, int n_kv,
-                            int batch, float eps, cudaStream_t st) {
-  const int rows_qkv = n_q * kHeadDim + 2 * n_kv * kHeadDim;
-  const int rows_total = rows_qkv + n_q;
-  const int rows_per_block = kWarps * kRowsPerWarp;
-  const dim3 grid((rows_total + rows_per_block - 1) / rows_per_block);
-  const size_t smem = sizeof(float) * (size_t)kBatchChunk * hidden;
-  cudaError_t e;
-  if (wdtype == SPARK_BF16) {
-    auto k = k_qkv_gate<__nv_bfloat16>;
-    if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, st>>>(h, (const __nv_bfloat16*)norm_w,
-                                    (const __nv_bfloat16*)qkv_w, (const __nv_bfloat16*)g_w,
-                                    qkvg, hidden, rows_qkv, n_q, batch, eps);
-  } else {
-    auto k = k_qkv_gate<float>;
-    if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, st>>>(h, (const float*)norm_w, (const float*)qkv_w,
-                                    (const float*)g_w, qkvg, hidden, rows_qkv, n_q, batch, eps);
+cudaError_t launch_qkv_rope(int wdtype, int cdtype, const float* h, const void* norm_w,
+                            const void* qkv_w, const void* g_w, float* q_rot, void* kc, void* vc,
+                            float* g_out, uint32_t* err, int hidden, int n_q, int n_kv, int batch,
+                            int64_t capacity, int ring_capacity, int rotary_dim, double theta,
+                            float eps, const int32_t* positions, cudaStream_t st) {
+  const size_t ce = cdtype == SPARK_BF16 ? 2 : 4;
+  for (int b0 = 0; b0 < batch; b0 += kMaxChunk) {
+    const int nb = batch - b0 < kMaxChunk ? batch - b0 : kMaxChunk;
+    const float* hb = h + (int64_t)b0 * hidden;
+    float* qb = q_rot + (int64_t)b0 * n_q * kHeadDim;
+    float* gb = g_out + (int64_t)b0 * n_q;
+    const int64_t coff = (int64_t)b0 * capacity * n_kv * kHeadDim * ce;
+    void* kb = static_cast<unsigned char*>(kc) + coff;
+    void* vb = static_cast<unsigned char*>(vc) + coff;
+    cudaError_t e;
+    if (wdtype == SPARK_BF16 && cdtype == SPARK_BF16)
+      e = qkv_chunk<__nv_bfloat16, __nv_bfloat16>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err,
+                                                  hidden, n_q, n_kv, capacity, ring_capacity,
+                                                  rotary_dim, theta, eps, positions + b0, st);
+    else if (wdtype == SPARK_BF16)
+      e = qkv_chunk<__nv_bfloat16, float>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden,
+                                          n_q, n_kv, capacity, ring_capacity, rotary_dim, theta,
+                                          eps, positions + b0, st);
+    else if (cdtype == SPARK_BF16)
+      e = qkv_chunk<float, __nv_bfloat16>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden,
+                                          n_q, n_kv, capacity, ring_capacity, rotary_dim, theta,
+                                          eps, positions + b0, st);
+    else
+      e = qkv_chunk<float, float>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden, n_q,
+                                  n_kv, capacity, ring_capacity, rotary_dim, theta, eps,
+                                  positions + b0, st);
+    if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
-cudaError_t launch_gate_oproj(int wdtype, const float* a, const float* qkvg, const float* h,
-                              const void* o_w, float* out, int hidden, int n_q, int n_kv,
-                              int batch, cudaStream_t st) {
+cudaError_t launch_oproj(int wdtype, const float* a, const float* g, const float* h,
+                         const void* o_w, float* out, uint32_t* err, int hidden, int n_q, int batch,
+                         cudaStream_t st) {
   const int q_dim = n_q * kHeadDim;
-  const int ld = qkvg_ld(n_q, n_kv);
-  const int g_col = n_q * kHeadDim + 2 * n_kv * kHeadDim;
-  const int rows_per_block = kWarps * kRowsPerWarp;
-  const dim3 grid((hidden + rows_per_block - 1) / rows_per_block);
-  const size_t smem = sizeof(float) * (size_t)kBatchChunk * q_dim;
-  cudaError_t e;
-  if (wdtype == SPARK_BF16) {
-    auto k = k_gate_oproj<__nv_bfloat16>;
-    if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, st>>>(a, qkvg, ld, g_col, h, (const __nv_bfloat16*)o_w, out,
-                                    hidden, q_dim, batch);
-  } else {
-    auto k = k_gate_oproj<float>;
-    if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, st>>>(a, qkvg, ld, g_col, h, (const float*)o_w, out, hidden,
-                                    q_dim, batch);
+  for (int b0 = 0; b0 < batch; b0 += kMaxChunk) {
+    const int nb = batch - b0 < kMaxChunk ? batch - b0 : kMaxChunk;
+    const float* ab = a + (int64_t)b0 * q_dim;
+    const float* gb = g + (int64_t)b0 * n_q;
+    const float* hb = h + (int64_t)b0 * hidden;
+    float* ob = out + (int64_t)b0 * hidden;
+    cudaError_t e = wdtype == SPARK_BF16
+                        ? oproj_chunk<__nv_bfloat16>(nb, ab, gb, hb, o_w, ob, err, hidden, n_q, st)
+                        : oproj_chunk<float>(nb, ab, gb, hb, o_w, ob, err, hidden, n_q, st);
+    if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace spark

@@ -161,27 +161,23 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
 
 /* ---- the block's stages, one kernel each (same conventions) ------------- */
 
-/* Input RMSNorm + q_k_v_proj + g_proj (attn.rs: the fused projection and
- * the gate's projection, which read the same normed x).
- *   qkvg [batch][n_q*d + 2*n_kv*d + n_q] fp32 device: q | k | v | g-logits. */
-int spark_dbg_qkv_gate(const spark_geom* g, const float* h, const spark_layer_weights* w,
-                       int32_t batch, float* qkvg, void* stream);
-
-/* Split + per-class NeoX rope + cache write (attn.rs: encode_split_qkv and
- * encode_rope_neox_subdim on q and on k in its slot).
- *   qkvg  as produced by spark_dbg_qkv_gate (read only).
- *   q_rot [batch][n_q*d] fp32 device: rotated queries.
- *   kv    row slot(p) of K receives rope(k), of V receives v. */
-int spark_dbg_split_rope(const spark_geom* g, const float* qkvg, const spark_kv_layer* kv,
-                         int32_t layer_class, const int32_t* positions, int32_t batch,
-                         float* q_rot, void* stream);
+/* Input RMSNorm + q_k_v_proj + g_proj + split + per-class NeoX rope + the
+ * cache-row write (attn.rs, encode_attention_block: the fused projection,
+ * the gate's projection reading the same normed x, encode_split_qkv with k
+ * and v landing in their slots, encode_rope_neox_subdim on q and on k).
+ *   q_rot    [batch][n_q*d] fp32 device: rotated queries.
+ *   g_logits [batch][n_q] fp32 device: gate logits (before the sigmoid).
+ *   kv       row slot(p) of K receives rope(k), of V receives v. */
+int spark_dbg_qkv_rope(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                       const spark_kv_layer* kv, int32_t layer_class, const int32_t* positions,
+                       int32_t batch, float* q_rot, float* g_logits, void* stream);
 
 /* GQA decode attention over each sequence's window (attn.rs,
  * encode_attention_block -> kv_write.rs, encode_attention_any), split over
  * the GPU with a log-sum-exp merge.
  *   q_rot [batch][n_q*d] fp32 device.
  *   a     [batch][n_q*d] fp32 device: un-gated attention output.
- *   n_ctas number of thread blocks sharing the work (0 = one per SM); the
+ *   n_ctas number of thread blocks sharing the work (0 = automatic); the
  *          result does not depend on it beyond floating-point reassociation.
  *   workspace as for spark_attn_decode. */
 int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_layer* kv,
@@ -191,10 +187,10 @@ int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_
 
 /* Head gate + o_proj + raw residual (attn.rs: encode_sigmoid_head_gate_mul
  * and the o_proj GEMV; mod.rs: encode_residual_add).
- *   a    [batch][n_q*d] fp32 device, un-gated attention output.
- *   qkvg gate logits are read from column n_q*d + 2*n_kv*d of each row.
- *   h    [batch][hidden] fp32 device; out [batch][hidden], may equal h. */
-int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* qkvg,
+ *   a        [batch][n_q*d] fp32 device, un-gated attention output.
+ *   g_logits [batch][n_q] fp32 device gate logits.
+ *   h        [batch][hidden] fp32 device; out [batch][hidden], may equal h. */
+int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* g_logits,
                          const float* h, const spark_layer_weights* w, int32_t batch,
                          float* out, void* stream);
 

@@ -55,112 +55,101 @@ def _gen(seed):
     return g
 
 
-def assert_rows_within_one_ulp(got: torch.Tensor, want: np.ndarray, what: str):
-    """Cache rows written by the kernel vs the oracle's rounded rows: the two
-    round differently-computed values of one real number, so they may differ by
-    one unit in the last place where that number lies next to a tie."""
-    g = synth.to_numpy(got)
-    if g.dtype == np.uint16:
-        gi = g.astype(np.int32)
-        wi = np.asarray(want).astype(np.int32)
-        same_sign = (gi >> 15) == (wi >> 15)
-        diff = np.where(same_sign, np.abs(gi - wi), 99)
-        assert np.all(diff <= 1), f"{what}: {int(np.sum(diff > 1))} elements differ by more than 1 ulp"
-        assert np.mean(diff == 0) > 0.99, f"{what}: only {np.mean(diff == 0):.4f} bit-identical"
-    else:
-        np.testing.assert_allclose(g.astype(np.float64), np.asarray(want, dtype=np.float64),
-                                   rtol=2e-6, atol=1e-6, err_msg=what)
-
-
 def assert_only_slot_changed(before: torch.Tensor, after: torch.Tensor, b: int, slot: int, what: str):
     assert torch.equal(before[b, :slot], after[b, :slot]), f"{what}: rows below slot {slot} changed"
     assert torch.equal(before[b, slot + 1:], after[b, slot + 1:]), f"{what}: rows above slot {slot} changed"
 
 
 # ---------------------------------------------------------------------------
-# stage 1: RMSNorm + q_k_v_proj + g_proj
-# ---------------------------------------------------------------------------
-
-@pytest.mark.parametrize("dtype,batch", [("bf16", 1), ("bf16", 3), ("f32", 2), ("bf16", 6), ("bf16", 70)])
-def test_qkv_gate_matches_oracle(B, dtype, batch):
-    wl = synth.Workload("t", "", dtype, [0] * batch, [synth.LayerSpec(True)], seed=200 + batch)
-    w = synth.make_weights(wl, 0, "cuda")
-    h = synth.make_h(wl, "cuda")
-    geom = B.spark_geom_default()
-    qkvg = torch.full((batch, QKVG_LD), float("nan"), device="cuda")
-    B.spark_dbg_qkv_gate(geom, h, B.LayerWeights(**w), qkvg)
-    torch.cuda.synchronize()
-    wn = np_weights(w)
-    hn = synth.to_numpy(h)
-    got = qkvg.cpu().numpy()
-    for b in range(batch) if batch <= 6 else (0, 33, 69):
-        x = oracle.rms_norm(hn[b], f64(wn["norm_w"]), 1e-6)
-        assert_close(got[b, :Q_DIM + 2 * KV_DIM], oracle.project(f64(wn["qkv_w"]), x), f"qkv b={b}")
-        assert_close(got[b, Q_DIM + 2 * KV_DIM:], oracle.project(f64(wn["g_w"]), x), f"g b={b}")
-
-
-# ---------------------------------------------------------------------------
-# stage 2: split + per-class rope + cache-row write
+# stage 1: RMSNorm + q_k_v_proj + g_proj + split + rope + cache-row write
 # ---------------------------------------------------------------------------
 
 SLOT_POSITIONS = [0, 40, 511, 512, 513, 700, 1023, 1024]
 
 
+def _qkv_oracle(wl, w_np, h_np, positions, is_full):
+    r, theta = oracle.rope_params_for(is_full, 64, 256, 5e6, 1e4)
+    out = []
+    for b, p in enumerate(positions):
+        x = oracle.rms_norm(h_np[b], f64(w_np["norm_w"]), 1e-6)
+        qkv = oracle.project(f64(w_np["qkv_w"]), x)
+        g = oracle.project(f64(w_np["g_w"]), x)
+        q = oracle.rope_neox(qkv[:Q_DIM].reshape(N_Q, D), p, r, theta)
+        k = oracle.rope_neox(qkv[Q_DIM:Q_DIM + KV_DIM].reshape(N_KV, D), p, r, theta)
+        v = qkv[Q_DIM + KV_DIM:].reshape(N_KV, D)
+        out.append({"q": q, "k": k, "v": v, "g": g, "qkv": qkv})
+    return out
+
+
+def _assert_row_close(got: torch.Tensor, want_f64: np.ndarray, what: str):
+    """A written cache row against the oracle's value: the kernel rounds its
+    fp32 result, so compare as floats, and nearly every element must round to
+    the oracle's own rounding of the exact value."""
+    g = f64(synth.to_numpy(got))
+    assert_close(g, want_f64, what)
+    if got.dtype == torch.bfloat16:
+        same = synth.to_numpy(got) == oracle.f64_to_bf16_bits(want_f64)
+        assert np.mean(same) > 0.97, f"{what}: only {np.mean(same):.3f} bit-identical"
+
+
 @pytest.mark.parametrize("is_full", [True, False])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("positions", [SLOT_POSITIONS, [131072]])
-def test_split_rope_and_cache_slots(B, is_full, dtype, positions):
+@pytest.mark.parametrize("positions", [SLOT_POSITIONS, [131072], [3, 700, 9]])
+def test_qkv_rope_and_cache_slots(B, is_full, dtype, positions):
     batch = len(positions)
     ring = 0 if is_full else 512
-    wl = synth.Workload("t", "", dtype, positions, [synth.LayerSpec(is_full, ring)], seed=300)
+    wl = synth.Workload("t", "", dtype, positions, [synth.LayerSpec(is_full, ring)], seed=300 + batch)
+    w = synth.make_weights(wl, 0, "cuda")
+    h = synth.make_h(wl, "cuda")
     kc, vc = synth.make_cache(wl, 0, "cuda")
     kc0, vc0 = kc.clone(), vc.clone()
-    qkvg = torch.randn((batch, QKVG_LD), generator=_gen(301), device="cuda")
-    q_rot = torch.empty((batch, Q_DIM), device="cuda")
+    q_rot = torch.full((batch, Q_DIM), float("nan"), device="cuda")
+    g_log = torch.full((batch, N_Q), float("nan"), device="cuda")
     geom = B.spark_geom_default()
     cls = B.SPARK_FULL if is_full else B.SPARK_SLIDING
-    B.spark_dbg_split_rope(geom, qkvg, B.KvLayer(kc, vc, ring), cls, positions, q_rot)
+    B.spark_dbg_qkv_rope(geom, h, B.LayerWeights(**w), B.KvLayer(kc, vc, ring), cls, positions, q_rot, g_log)
     torch.cuda.synchronize()
-    r, theta = oracle.rope_params_for(is_full, 64, 256, 5e6, 1e4)
-    qn = qkvg.cpu().numpy().astype(np.float64)
-    got_q = q_rot.cpu().numpy()
-    round_ = (lambda x: oracle.f64_to_bf16_bits(x)) if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    want = _qkv_oracle(wl, np_weights(w), synth.to_numpy(h).astype(np.float64), positions, is_full)
+    got_q, got_g = q_rot.cpu().numpy(), g_log.cpu().numpy()
     for b, p in enumerate(positions):
-        q = oracle.rope_neox(qn[b, :Q_DIM].reshape(N_Q, D), p, r, theta)
-        k = oracle.rope_neox(qn[b, Q_DIM:Q_DIM + KV_DIM].reshape(N_KV, D), p, r, theta)
-        v = qn[b, Q_DIM + KV_DIM:Q_DIM + 2 * KV_DIM].reshape(N_KV, D)
-        # rope angles reach 131072 rad: the kernel reduces them in fp64
-        assert_close(got_q[b], q.reshape(-1), f"q b={b} p={p}", max_abs=1e-4, rel_l2=1e-5)
+        # tighter than the block tolerance: an fp32 rope angle at 131072 would miss by ~1e-2
+        assert_close(got_q[b], want[b]["q"].reshape(-1), f"q b={b} p={p}", max_abs=2e-3, rel_l2=2e-4)
+        assert_close(got_g[b], want[b]["g"], f"g b={b} p={p}", max_abs=2e-3, rel_l2=2e-4)
         slot = oracle.write_slot(p, ring)
-        assert_rows_within_one_ulp(kc[b, slot], round_(k), f"k row b={b} p={p}")
-        want_v = round_(v)
-        got_v = synth.to_numpy(vc[b, slot])
-        assert np.array_equal(got_v, want_v), f"v row b={b} p={p} not bit-exact"
+        _assert_row_close(kc[b, slot], want[b]["k"], f"k row b={b} p={p}")
+        _assert_row_close(vc[b, slot], want[b]["v"], f"v row b={b} p={p}")
         assert_only_slot_changed(kc0, kc, b, slot, f"K b={b} p={p}")
         assert_only_slot_changed(vc0, vc, b, slot, f"V b={b} p={p}")
 
 
 def test_rope_class_selection_reaches_the_kernel(B):
-    """Swapping the classes' (width, theta) must change q: the full class
-    leaves dims 64..255 untouched, the sliding class does not."""
+    """The full class rotates only dims [0, 64) of each head at theta 5e6; the
+    sliding class rotates all 256 at theta 1e4: swapping them must show."""
     positions = [700]
-    qkvg = torch.randn((1, QKVG_LD), generator=_gen(302), device="cuda")
+    wl = synth.Workload("t", "", "bf16", positions, [synth.LayerSpec(True)], seed=303)
+    w = synth.make_weights(wl, 0, "cuda")
+    h = synth.make_h(wl, "cuda")
     geom = B.spark_geom_default()
-    out = {}
+    got = {}
     for is_full in (True, False):
-        wl = synth.Workload("t", "", "bf16", positions, [synth.LayerSpec(is_full, 0 if is_full else 512)], seed=303)
-        kc, vc = synth.make_cache(wl, 0, "cuda")
+        spec = synth.LayerSpec(is_full, 0 if is_full else 512)
+        wl2 = synth.Workload("t", "", "bf16", positions, [spec], seed=304)
+        kc, vc = synth.make_cache(wl2, 0, "cuda")
         q_rot = torch.empty((1, Q_DIM), device="cuda")
-        B.spark_dbg_split_rope(geom, qkvg, B.KvLayer(kc, vc, 0 if is_full else 512),
-                               B.SPARK_FULL if is_full else B.SPARK_SLIDING, positions, q_rot)
-        out[is_full] = q_rot.view(N_Q, D).cpu()
-    src = qkvg[0, :Q_DIM].view(N_Q, D).cpu()
-    assert torch.equal(out[True][:, 64:], src[:, 64:])
-    assert (out[False][:, 64:] - src[:, 64:]).abs().max() > 0.1
+        g_log = torch.empty((1, N_Q), device="cuda")
+        B.spark_dbg_qkv_rope(geom, h, B.LayerWeights(**w), B.KvLayer(kc, vc, spec.ring_capacity),
+                             B.SPARK_FULL if is_full else B.SPARK_SLIDING, positions, q_rot, g_log)
+        got[is_full] = q_rot.view(N_Q, D).cpu().numpy()
+    proj = _qkv_oracle(wl, np_weights(w), synth.to_numpy(h).astype(np.float64), positions, True)[0]["qkv"]
+    proj_q = proj[:Q_DIM].reshape(N_Q, D)
+    assert_close(got[True][:, 64:], proj_q[:, 64:], "full class passes dims 64.. through",
+                 max_abs=1e-3, rel_l2=1e-4)
+    assert np.max(np.abs(got[False][:, 64:] - proj_q[:, 64:])) > 0.1
+    assert np.max(np.abs(got[True][:, :64] - got[False][:, :64])) > 0.1
 
 
 # ---------------------------------------------------------------------------
-# stage 3: split-K GQA decode attention
+# stage 2: split-K GQA decode attention
 # ---------------------------------------------------------------------------
 
 ATTN_CASES = [
@@ -248,28 +237,28 @@ def test_attention_split_count_invariance_and_reuse(B):
 
 
 # ---------------------------------------------------------------------------
-# stage 4: head gate + o_proj + residual
+# stage 3: head gate + o_proj + residual
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("dtype,batch", [("bf16", 1), ("bf16", 5), ("f32", 2)])
+@pytest.mark.parametrize("dtype,batch", [("bf16", 1), ("bf16", 5), ("f32", 2), ("bf16", 4)])
 def test_gate_oproj_matches_oracle(B, dtype, batch):
     wl = synth.Workload("t", "", dtype, [0] * batch, [synth.LayerSpec(True)], seed=500 + batch)
     w = synth.make_weights(wl, 0, "cuda")
     h = synth.make_h(wl, "cuda")
     a = torch.randn((batch, Q_DIM), generator=_gen(501), device="cuda")
-    qkvg = torch.randn((batch, QKVG_LD), generator=_gen(502), device="cuda") * 2
+    g_log = torch.randn((batch, N_Q), generator=_gen(502), device="cuda") * 2
     out = torch.empty_like(h)
     geom = B.spark_geom_default()
-    B.spark_dbg_gate_oproj(geom, a, qkvg, h, B.LayerWeights(**w), out)
+    B.spark_dbg_gate_oproj(geom, a, g_log, h, B.LayerWeights(**w), out)
     # in place: out aliases h
     h2 = h.clone()
-    B.spark_dbg_gate_oproj(geom, a, qkvg, h2, B.LayerWeights(**w), h2)
+    B.spark_dbg_gate_oproj(geom, a, g_log, h2, B.LayerWeights(**w), h2)
     torch.cuda.synchronize()
     assert torch.equal(out, h2)
     wo = f64(np_weights(w)["o_w"])
-    an, gn, hn = a.cpu().numpy(), qkvg.cpu().numpy(), h.cpu().numpy().astype(np.float64)
+    an, gn, hn = a.cpu().numpy(), g_log.cpu().numpy(), h.cpu().numpy().astype(np.float64)
     for b in range(batch):
-        gated = oracle.head_gate(an[b].reshape(N_Q, D), gn[b, Q_DIM + 2 * KV_DIM:].astype(np.float64))
+        gated = oracle.head_gate(an[b].reshape(N_Q, D), gn[b].astype(np.float64))
         o = oracle.project(wo, gated.reshape(-1))
         assert_close(out[b].cpu().numpy() - hn[b], o, f"o b={b}")
 
