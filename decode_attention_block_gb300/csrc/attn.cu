@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A hint for the kernel after this one: its weights (o_proj) do not
     // depend on attention, so this CTA pulls its share of them into L2 while
     // HBM is otherwise idle.
-    if (l2_pf_bytes > 0) {
+    if (l2_pf != nullptr && l2_pf_bytes > 0) {
       const int64_t lo = (l2_pf_bytes * blockIdx.x / gridDim.x) & ~int64_t(15);
       const int64_t hi = (l2_pf_bytes * (blockIdx.x + 1) / gridDim.x) & ~int64_t(15);
       for (int64_t o = lo; o < hi; o += 65536) {

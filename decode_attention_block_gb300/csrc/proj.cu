@@ -15,11 +15,13 @@
 //
 // Both are HBM-bound at small batch: every weight byte is read once and used
 // for `nb` multiply-adds.  Each CTA (one per SM) owns an equal contiguous
-// share of the weight rows.  Every warp streams its rows with 1-D bulk copies
-// (cp.async.bulk) into a private double buffer in shared memory, so a whole
-// CTA keeps ~160 KB of weights in flight, and the first copies are issued
-// before the kernel waits for its predecessor (programmatic dependent
-// launch): the weight stream does not depend on the previous kernel.
+// share of the weight rows and streams them with 1-D bulk copies
+// (cp.async.bulk) into a pool of shared-memory stages, one row unit per
+// stage; the pool holds the CTA's whole share when it fits (~200 KB at
+// spark2_5's size), so every byte is requested at once, and the requests are
+// issued before the kernel waits for its predecessor (programmatic dependent
+// launch): the weight stream does not depend on the previous kernel.  Warps
+// take units round-robin; the warp that frees a stage refills it.
 //
 // The RMSNorm needs no pass before the GEMV: rms(h) scales every output of a
 // row by the same 1/sqrt(mean(h^2) + eps), so the warps dot the rows with
@@ -208,17 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                const WT* __restrict__ qkv_w, const WT* __restrict__ g_w, float* __restrict__ q_rot,
                CT* __restrict__ kc, CT* __restrict__ vc, float* __restrict__ g_out, uint32_t* err,
                int hidden, int n_q, int n_kv, int nb, int64_t capacity, int ring_capacity,
-               int rotary_dim, int stages, float eps, const __grid_constant__ QkvArgs<NB> args) {
+               int rotary_dim, int stages, float eps, const unsigned char* l2_pf,
+               int64_t l2_pf_bytes, const __grid_constant__ QkvArgs<NB> args) {
   constexpr int E = Chunk<WT>::kElems;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = hidden / E;
   const int xfloats = ((nchunk + 31) / 32) * 32 * E;  // one permuted activation vector
   const size_t row_bytes = (size_t)hidden * sizeof(WT);
+  const size_t unit_bytes = 2 * row_bytes;
   float* xs = reinterpret_cast<float*>(smem);         // [NB][xfloats]
-  unsigned char* my_stages =
-      smem + sizeof(float) * NB * xfloats + (size_t)warp * stages * 2 * row_bytes;
-  __shared__ uint64_t bars[kWarps][2];
+  unsigned char* pool = smem + sizeof(float) * NB * xfloats;  // [stages][2 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pool + (size_t)stages * unit_bytes);
   __shared__ float red[kWarps][NB];
   __shared__ float inv_rms[NB];
   __shared__ int abort_flag;
@@ -228,12 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows_qkv = n_heads * kHeadDim;
   const int u0 = (int)((int64_t)n_units * blockIdx.x / gridDim.x);
   const int u1 = (int)((int64_t)n_units * (blockIdx.x + 1) / gridDim.x);
-  const int my_first = u0 + warp;
-  const int my_count = my_first < u1 ? (u1 - my_first + kWarps - 1) / kWarps : 0;
+  const int cnt = u1 - u0;  // this CTA's units: unit k goes to stage k % stages, warp k % nw
+  const int nw = stages < kWarps ? stages : kWarps;  // warps that consume (a stage each at least)
 
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w)
-      for (int s = 0; s < 2; ++s) mbar_init(&bars[w][s], 1);
+    for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -242,18 +244,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto row_ptr = [&](int r) -> const WT* {
     return r < rows_qkv ? qkv_w + (int64_t)r * hidden : g_w + (int64_t)(r - rows_qkv) * hidden;
   };
-  auto issue = [&](int i) {  // lane 0: bring unit i of this warp into stage i % stages
-    const Unit un = unit_of(my_first + i * kWarps, n_q, n_kv, rotary_dim);
-    const int s = i % stages;
-    unsigned char* dst = my_stages + (size_t)s * 2 * row_bytes;
-    mbar_arrive_expect_tx(&bars[warp][s], (uint32_t)(2 * row_bytes));
-    bulk_load(dst, row_ptr(un.row_a), (uint32_t)row_bytes, &bars[warp][s]);
-    bulk_load(dst + row_bytes, row_ptr(un.row_b), (uint32_t)row_bytes, &bars[warp][s]);
+  auto issue = [&](int k) {  // bring unit k of this CTA into stage k % stages
+    const Unit un = unit_of(u0 + k, n_q, n_kv, rotary_dim);
+    const int s = k % stages;
+    unsigned char* dst = pool + (size_t)s * unit_bytes;
+    mbar_arrive_expect_tx(&bars[s], (uint32_t)unit_bytes);
+    bulk_load(dst, row_ptr(un.row_a), (uint32_t)row_bytes, &bars[s]);
+    bulk_load(dst + row_bytes, row_ptr(un.row_b), (uint32_t)row_bytes, &bars[s]);
   };
 
-  // the weight stream does not depend on the previous kernel: start it now
-  if (lane == 0)
-    for (int i = 0; i < stages && i < my_count; ++i) issue(i);
+  // The weight stream does not depend on the previous kernel: request every
+  // stage now (each warp the units it will consume first).
+  if (lane == 0 && warp < nw)
+    for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
+  // A hint for later in the block: o_proj's weights depend on nothing either,
+  // so this CTA asks for its share of them in L2 now and HBM keeps streaming
+  // while attention runs.
+  if (threadIdx.x == 32 && l2_pf != nullptr && l2_pf_bytes > 0) {
+    const int64_t lo = (l2_pf_bytes * blockIdx.x / gridDim.x) & ~int64_t(15);
+    const int64_t hi = (l2_pf_bytes * (blockIdx.x + 1) / gridDim.x) & ~int64_t(15);
+    for (int64_t o = lo; o < hi; o += 65536)
+      bulk_prefetch_l2(l2_pf + o, (uint32_t)(hi - o < 65536 ? hi - o : 65536));
+  }
   pdl_trigger();
   pdl_wait();
 
@@ -284,20 +296,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  for (int i = 0; i < my_count; ++i) {
-    const int s = i % stages;
-    const uint32_t parity = (uint32_t)((i / stages) & 1);
-    const Unit un = unit_of(my_first + i * kWarps, n_q, n_kv, rotary_dim);
+  for (int k = warp; warp < nw && k < cnt; k += nw) {
+    const int s = k % stages;
+    const uint32_t parity = (uint32_t)((k / stages) & 1);
+    const Unit un = unit_of(u0 + k, n_q, n_kv, rotary_dim);
     float2 acc_a[NB], acc_b[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc_a[b] = acc_b[b] = make_float2(0.f, 0.f);
-    const bool ok = wait_stage(&bars[warp][s], parity, &abort_flag, err);
+    const bool ok = wait_stage(&bars[s], parity, &abort_flag, err);
     if (ok) {
-      const unsigned char* st = my_stages + (size_t)s * 2 * row_bytes;
+      const unsigned char* st = pool + (size_t)s * unit_bytes;
       row_dot2<WT, NB>(st, st + row_bytes, xs, xfloats, nchunk, acc_a, acc_b);
     }
     __syncwarp();
-    if (ok && lane == 0 && i + stages < my_count) issue(i + stages);
+    // the stage is free again: refill it with the unit `stages` further on
+    if (ok && lane == 0 && k + stages < cnt) issue(k + stages);
     if (!ok) continue;
     float va = 0.f, vb = 0.f;
 #pragma unroll
@@ -355,31 +368,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int xfloats = ((nchunk + 31) / 32) * 32 * E;
   const size_t row_bytes = (size_t)q_dim * sizeof(WT);
   float* xs = reinterpret_cast<float*>(smem);  // [NB][xfloats]
-  unsigned char* my_stages = smem + sizeof(float) * NB * xfloats + (size_t)warp * stages * row_bytes;
-  __shared__ uint64_t bars[kWarps][2];
+  unsigned char* pool = smem + sizeof(float) * NB * xfloats;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pool + (size_t)stages * row_bytes);
   __shared__ int abort_flag;
 
   const int r0 = (int)((int64_t)hidden * blockIdx.x / gridDim.x);
   const int r1 = (int)((int64_t)hidden * (blockIdx.x + 1) / gridDim.x);
-  const int my_first = r0 + warp;
-  const int my_count = my_first < r1 ? (r1 - my_first + kWarps - 1) / kWarps : 0;
+  const int cnt = r1 - r0;
+  const int nw = stages < kWarps ? stages : kWarps;
 
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w)
-      for (int s = 0; s < 2; ++s) mbar_init(&bars[w][s], 1);
+    for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
     abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  auto issue = [&](int i) {
-    const int s = i % stages;
-    mbar_arrive_expect_tx(&bars[warp][s], (uint32_t)row_bytes);
-    bulk_load(my_stages + (size_t)s * row_bytes, o_w + (int64_t)(my_first + i * kWarps) * q_dim,
-              (uint32_t)row_bytes, &bars[warp][s]);
+  auto issue = [&](int k) {
+    const int s = k % stages;
+    mbar_arrive_expect_tx(&bars[s], (uint32_t)row_bytes);
+    bulk_load(pool + (size_t)s * row_bytes, o_w + (int64_t)(r0 + k) * q_dim, (uint32_t)row_bytes,
+              &bars[s]);
   };
-  if (lane == 0)
-    for (int i = 0; i < stages && i < my_count; ++i) issue(i);
+  if (lane == 0 && warp < nw)
+    for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
   pdl_trigger();
   pdl_wait();
 
@@ -398,18 +410,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  for (int i = 0; i < my_count; ++i) {
-    const int s = i % stages;
-    const uint32_t parity = (uint32_t)((i / stages) & 1);
+  for (int k = warp; warp < nw && k < cnt; k += nw) {
+    const int s = k % stages;
+    const uint32_t parity = (uint32_t)((k / stages) & 1);
     float2 acc[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = make_float2(0.f, 0.f);
-    const bool ok = wait_stage(&bars[warp][s], parity, &abort_flag, err);
-    if (ok) row_dot<WT, NB>(my_stages + (size_t)s * row_bytes, xs, xfloats, nchunk, acc);
+    const bool ok = wait_stage(&bars[s], parity, &abort_flag, err);
+    if (ok) row_dot<WT, NB>(pool + (size_t)s * row_bytes, xs, xfloats, nchunk, acc);
     __syncwarp();
-    if (ok && lane == 0 && i + stages < my_count) issue(i + stages);
+    if (ok && lane == 0 && k + stages < cnt) issue(k + stages);
     if (!ok) continue;
-    const int r = my_first + i * kWarps;
     float v = 0.f;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -417,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == b) v = sb;
     }
     if (lane < nb) {
-      const int64_t idx = (int64_t)lane * hidden + r;
+      const int64_t idx = (int64_t)lane * hidden + r0 + k;
       out[idx] = h[idx] + v;  // read and written by the same thread: out may alias h
     }
   }
@@ -427,11 +438,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-// stages per warp that fit next to the activations (1 or 2), 0 if none fits
-int stages_for(size_t stage_bytes, size_t x_bytes) {
-  if (x_bytes + kWarps * 2 * stage_bytes <= kSmemBudget) return 2;
-  if (x_bytes + kWarps * stage_bytes <= kSmemBudget) return 1;
-  return 0;
+// Stages of the CTA-wide pool: as many units as fit next to the activations
+// and the barriers, at most the CTA's share (0: not even one fits).  With
+// fewer stages than warps only that many warps consume.
+int stages_for(size_t unit_bytes, size_t x_bytes, int max_units) {
+  const size_t room = kSmemBudget - x_bytes;
+  int s = (int)(room / (unit_bytes + 8));
+  if (s > max_units) s = max_units;
+  return s < 1 ? 0 : s;
 }
 
 template <typename WT>
@@ -446,25 +460,26 @@ cudaError_t qkv_launch(const float* h, const void* norm_w, const void* qkv_w, co
                        float* q_rot, void* kc, void* vc, float* g_out, uint32_t* err, int hidden,
                        int n_q, int n_kv, int nb, int64_t capacity, int ring_capacity,
                        int rotary_dim, double theta, float eps, const int32_t* positions,
-                       cudaStream_t st) {
+                       const void* l2_pf, size_t l2_pf_bytes, cudaStream_t st) {
   QkvArgs<NB> args;
   for (int i = 0; i < kHeadDim / 2; ++i)
     args.inv_freq[i] = i < rotary_dim / 2 ? pow(theta, -2.0 * i / (double)rotary_dim) : 0.0;
   for (int b = 0; b < NB; ++b) args.pos[b] = b < nb ? positions[b] : 0;
   const size_t row_bytes = (size_t)hidden * sizeof(WT);
   const size_t xb = xbytes<WT>(hidden, NB);
-  const int stages = stages_for(2 * row_bytes, xb);
-  if (stages == 0) return cudaErrorInvalidConfiguration;
-  const size_t smem = xb + (size_t)kWarps * stages * 2 * row_bytes;
-  auto kern = k_qkv_rope<WT, CT, NB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   const int n_units = (n_q + 2 * n_kv) * (kHeadDim / 2) + n_q / 2;
   int grid = device_sm_count();
   if (grid > n_units) grid = n_units;
+  const int stages = stages_for(2 * row_bytes, xb, (n_units + grid - 1) / grid);
+  if (stages == 0) return cudaErrorInvalidConfiguration;
+  const size_t smem = xb + (size_t)stages * (2 * row_bytes + 8);
+  auto kern = k_qkv_rope<WT, CT, NB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, h, (const WT*)norm_w,
                     (const WT*)qkv_w, (const WT*)g_w, q_rot, (CT*)kc, (CT*)vc, g_out, err, hidden,
-                    n_q, n_kv, nb, capacity, ring_capacity, rotary_dim, stages, eps, args);
+                    n_q, n_kv, nb, capacity, ring_capacity, rotary_dim, stages, eps,
+                    static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
 }
 
 template <typename WT, typename CT>
@@ -472,11 +487,12 @@ cudaError_t qkv_chunk(int nb, const float* h, const void* norm_w, const void* qk
                       const void* g_w, float* q_rot, void* kc, void* vc, float* g_out,
                       uint32_t* err, int hidden, int n_q, int n_kv, int64_t capacity,
                       int ring_capacity, int rotary_dim, double theta, float eps,
-                      const int32_t* positions, cudaStream_t st) {
+                      const int32_t* positions, const void* l2_pf, size_t l2_pf_bytes,
+                      cudaStream_t st) {
 #define SPARK_QKV(NBV)                                                                           \
   return qkv_launch<WT, CT, NBV>(h, norm_w, qkv_w, g_w, q_rot, kc, vc, g_out, err, hidden, n_q, \
                                  n_kv, nb, capacity, ring_capacity, rotary_dim, theta, eps,     \
-                                 positions, st)
+                                 positions, l2_pf, l2_pf_bytes, st)
   if (nb == 1) SPARK_QKV(1);
   if (nb == 2) SPARK_QKV(2);
   SPARK_QKV(4);
@@ -489,14 +505,14 @@ cudaError_t oproj_launch(const float* a, const float* g, const float* h, const v
   const int q_dim = n_q * kHeadDim;
   const size_t row_bytes = (size_t)q_dim * sizeof(WT);
   const size_t xb = xbytes<WT>(q_dim, NB);
-  const int stages = stages_for(row_bytes, xb);
+  int grid = device_sm_count();
+  if (grid > hidden) grid = hidden;
+  const int stages = stages_for(row_bytes, xb, (hidden + grid - 1) / grid);
   if (stages == 0) return cudaErrorInvalidConfiguration;
-  const size_t smem = xb + (size_t)kWarps * stages * row_bytes;
+  const size_t smem = xb + (size_t)stages * (row_bytes + 8);
   auto kern = k_oproj<WT, NB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int grid = device_sm_count();
-  if (grid > hidden) grid = hidden;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, a, g, h, (const WT*)o_w, out, err,
                     hidden, q_dim, n_q, nb, stages);
 }
@@ -517,7 +533,8 @@ cudaError_t launch_qkv_rope(int wdtype, int cdtype, const float* h, const void* 
                             const void* qkv_w, const void* g_w, float* q_rot, void* kc, void* vc,
                             float* g_out, uint32_t* err, int hidden, int n_q, int n_kv, int batch,
                             int64_t capacity, int ring_capacity, int rotary_dim, double theta,
-                            float eps, const int32_t* positions, cudaStream_t st) {
+                            float eps, const int32_t* positions, const void* l2_pf,
+                            size_t l2_pf_bytes, cudaStream_t st) {
   const size_t ce = cdtype == SPARK_BF16 ? 2 : 4;
   for (int b0 = 0; b0 < batch; b0 += kMaxChunk) {
     const int nb = batch - b0 < kMaxChunk ? batch - b0 : kMaxChunk;
@@ -531,19 +548,24 @@ cudaError_t launch_qkv_rope(int wdtype, int cdtype, const float* h, const void* 
     if (wdtype == SPARK_BF16 && cdtype == SPARK_BF16)
       e = qkv_chunk<__nv_bfloat16, __nv_bfloat16>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err,
                                                   hidden, n_q, n_kv, capacity, ring_capacity,
-                                                  rotary_dim, theta, eps, positions + b0, st);
+                                                  rotary_dim, theta, eps, positions + b0,
+                                                  b0 == 0 ? l2_pf : nullptr,
+                                                  b0 == 0 ? l2_pf_bytes : 0, st);
     else if (wdtype == SPARK_BF16)
       e = qkv_chunk<__nv_bfloat16, float>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden,
                                           n_q, n_kv, capacity, ring_capacity, rotary_dim, theta,
-                                          eps, positions + b0, st);
+                                          eps, positions + b0, b0 == 0 ? l2_pf : nullptr,
+                                                  b0 == 0 ? l2_pf_bytes : 0, st);
     else if (cdtype == SPARK_BF16)
       e = qkv_chunk<float, __nv_bfloat16>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden,
                                           n_q, n_kv, capacity, ring_capacity, rotary_dim, theta,
-                                          eps, positions + b0, st);
+                                          eps, positions + b0, b0 == 0 ? l2_pf : nullptr,
+                                                  b0 == 0 ? l2_pf_bytes : 0, st);
     else
       e = qkv_chunk<float, float>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden, n_q,
                                   n_kv, capacity, ring_capacity, rotary_dim, theta, eps,
-                                  positions + b0, st);
+                                  positions + b0, b0 == 0 ? l2_pf : nullptr,
+                                                  b0 == 0 ? l2_pf_bytes : 0, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
