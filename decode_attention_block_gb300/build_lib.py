@@ -40,8 +40,19 @@ def _inputs() -> list[str]:
     return files
 
 
+STAMP = os.path.join(BUILD, "flags.txt")
+
+
+def _extra_flags() -> list[str]:
+    """Extra nvcc flags from SPARK_NVCC_FLAGS (e.g. tuning -D overrides)."""
+    return os.environ.get("SPARK_NVCC_FLAGS", "").split()
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
+        return True
+    old = open(STAMP).read() if os.path.exists(STAMP) else ""
+    if old != " ".join(_extra_flags()):
         return True
     t = os.path.getmtime(LIB_PATH)
     return any(os.path.getmtime(f) > t for f in _inputs())
@@ -64,7 +75,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         return LIB_PATH
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + _extra_flags()
     objs = []
     cmds = []
     for src in SOURCES:
@@ -76,6 +87,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     tmp = LIB_PATH + ".tmp"
     _run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs, verbose)
     os.replace(tmp, LIB_PATH)
+    with open(STAMP, "w") as f:
+        f.write(" ".join(_extra_flags()))
     return LIB_PATH
 
 

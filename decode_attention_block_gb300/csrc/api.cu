@@ -174,7 +174,7 @@ int spark_dbg_qkv_rope(const spark_geom* g, const float* h, const spark_layer_we
   return cuda_status(launch_qkv_rope(w->dtype, kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot,
                                      kv->k, kv->v, g_logits, nullptr, g->hidden, g->n_q, g->n_kv,
                                      batch, kv->capacity, kv->ring_capacity, rotary_dim, theta,
-                                     g->eps, positions, nullptr, 0, (cudaStream_t)stream));
+                                     g->eps, positions, (cudaStream_t)stream));
 }
 
 int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_layer* kv,
@@ -229,12 +229,10 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
   int rotary_dim;
   double theta;
   rope_for(g, layer_class, &rotary_dim, &theta);
-  const size_t wbytes = w->dtype == SPARK_BF16 ? 2 : 4;
   cudaError_t e = launch_qkv_rope(w->dtype, kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot,
                                   kv->k, kv->v, g_logits, err, g->hidden, g->n_q, g->n_kv, batch,
                                   kv->capacity, kv->ring_capacity, rotary_dim, theta, g->eps,
-                                  positions, w->o_w, (size_t)g->hidden * g->n_q * g->head_dim * wbytes,
-                                  st);
+                                  positions, st);
   if (e == cudaSuccess)
     e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity,
                          kv->ring_capacity, layer_class == SPARK_FULL, g->window, g->scale,

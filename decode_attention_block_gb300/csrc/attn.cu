@@ -44,22 +44,32 @@ constexpr int kBarConsumers = 1;              // named barrier id of the consume
 
 template <typename CT>
 struct CacheT;
+// Pipeline depth (a multiple of the consumer count: tile k lives in stage
+// k % NS and belongs to warp k % 4, so each stage always serves one warp and
+// no wait can alias an older mbarrier phase).  Long histories take a deep
+// ring (the kernel runs alone for hundreds of microseconds); short ones a
+// shallow ring, so the kernel's CTAs leave room on each SM for the next
+// kernel's CTAs to start streaming o_proj's weights while attention runs.
 template <>
 struct CacheT<__nv_bfloat16> {
   static constexpr int kLineElems = 64;
-  static constexpr int kStages = 8;
+  static constexpr int kDeep = 8;
+  static constexpr int kShallow = 4;
   static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
 template <>
 struct CacheT<float> {
   static constexpr int kLineElems = 32;
-  static constexpr int kStages = 4;
+  static constexpr int kDeep = 4;
+  static constexpr int kShallow = 4;
   static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 };
+constexpr int64_t kDeepRows = 1 << 16;  // rows (x KV heads) per call from which the deep ring pays
 
-template <typename CT>
+template <typename CT, int NS>
 struct Smem {
-  static constexpr int kStages = CacheT<CT>::kStages;
+  static_assert(NS % kConsumers == 0, "each stage must belong to one consumer warp");
+  static constexpr int kStages = NS;
   static constexpr int kSubs = kHeadDim / CacheT<CT>::kLineElems;
   static constexpr int kHalf = kSubs * kSubBytes;  // the K (or V) half of a stage
   static constexpr int kStage = 2 * kHalf;
@@ -135,7 +145,7 @@ __device__ __forceinline__ Share share_begin(const AttnArgs<MAXB>& args, int bat
   return s;
 }
 
-template <typename CT, int MAXB>
+template <typename CT, int NS, int MAXB>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const float* __restrict__ q_rot, float* __restrict__ a_out,
@@ -143,8 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
                   const __grid_constant__ AttnArgs<MAXB> args) {
-  using S = Smem<CT>;
-  constexpr int NS = S::kStages;
+  using S = Smem<CT, NS>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -505,13 +514,13 @@ bool make_cache_map(CUtensorMap* map, const void* base, int n_kv, int64_t rows) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename CT, int MAXB>
+template <typename CT, int NS, int MAXB>
 cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_kv,
                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
                      const int32_t* positions, int batch, float* a, float* part,
                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
                      size_t l2_pf_bytes, cudaStream_t st) {
-  using S = Smem<CT>;
+  using S = Smem<CT, NS>;
   AttnArgs<MAXB> args;
   args.prefix[0] = 0;
   for (int b = 0; b < MAXB; ++b) {
@@ -532,7 +541,7 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   if (!make_cache_map<CT>(&mk, kc, n_kv, (int64_t)batch * capacity) ||
       !make_cache_map<CT>(&mv, vc, n_kv, (int64_t)batch * capacity))
     return cudaErrorInvalidValue;
-  auto kern = k_attn_decode<CT, MAXB>;
+  auto kern = k_attn_decode<CT, NS, MAXB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = scale * 1.4426950408889634f;
@@ -541,21 +550,38 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
                     static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
 }
 
+template <typename CT, int NS>
+cudaError_t launch_ns(const float* q_rot, const void* kc, const void* vc, int n_kv,
+                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
+                      const int32_t* positions, int batch, float* a, float* part,
+                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
+                      size_t l2_pf_bytes, cudaStream_t st) {
+  if (batch <= 8)
+    return launch_t<CT, NS, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
+                               positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+  if (batch <= 64)
+    return launch_t<CT, NS, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
+                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+  return launch_t<CT, NS, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
+                                           window, scale, positions, batch, a, part, counters, err,
+                                           n_ctas, l2_pf, l2_pf_bytes, st);
+}
+
 template <typename CT>
 cudaError_t launch_ct(const float* q_rot, const void* kc, const void* vc, int n_kv,
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
                       size_t l2_pf_bytes, cudaStream_t st) {
-  if (batch <= 8)
-    return launch_t<CT, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                           positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
-  if (batch <= 64)
-    return launch_t<CT, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                            positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
-  return launch_t<CT, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
-                                       window, scale, positions, batch, a, part, counters, err,
-                                       n_ctas, l2_pf, l2_pf_bytes, st);
+  int64_t rows = 0;
+  for (int b = 0; b < batch; ++b) rows += window_of(positions[b], full, window, ring_capacity).rows;
+  if ((int64_t)n_kv * rows >= kDeepRows)
+    return launch_ns<CT, CacheT<CT>::kDeep>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
+                                      scale, positions, batch, a, part, counters, err, n_ctas,
+                                      l2_pf, l2_pf_bytes, st);
+  return launch_ns<CT, CacheT<CT>::kShallow>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
+                                       scale, positions, batch, a, part, counters, err, n_ctas,
+                                       l2_pf, l2_pf_bytes, st);
 }
 
 }  // namespace

@@ -11,8 +11,7 @@ cudaError_t launch_qkv_rope(int wdtype, int cdtype, const float* h, const void* 
                             const void* qkv_w, const void* g_w, float* q_rot, void* kc, void* vc,
                             float* g_out, uint32_t* err, int hidden, int n_q, int n_kv, int batch,
                             int64_t capacity, int ring_capacity, int rotary_dim, double theta,
-                            float eps, const int32_t* positions, const void* l2_prefetch,
-                            size_t l2_prefetch_bytes, cudaStream_t st);
+                            float eps, const int32_t* positions, cudaStream_t st);
 
 // Head gate + o_proj + raw residual: out[b] = h[b] + W_o (a[b] * sigmoid(g[b])).
 cudaError_t launch_oproj(int wdtype, const float* a, const float* g, const float* h,

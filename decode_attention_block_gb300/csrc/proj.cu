@@ -41,7 +41,13 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr size_t kSmemBudget = 220 * 1024;
+// Shared memory per CTA for the activations and the weight stages (one CTA
+// per SM).  Measured on GB300: a ~100 KB budget that lets the next kernel's
+// CTAs co-reside gains less than the deeper pool loses.
+#ifndef SPARK_GEMV_SMEM_KB
+#define SPARK_GEMV_SMEM_KB 200
+#endif
+constexpr size_t kSmemBudget = SPARK_GEMV_SMEM_KB * 1024;
 
 template <typename WT>
 struct Chunk;
@@ -210,8 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const WT* __restrict__ qkv_w, const WT* __restrict__ g_w, float* __restrict__ q_rot,
                CT* __restrict__ kc, CT* __restrict__ vc, float* __restrict__ g_out, uint32_t* err,
                int hidden, int n_q, int n_kv, int nb, int64_t capacity, int ring_capacity,
-               int rotary_dim, int stages, float eps, const unsigned char* l2_pf,
-               int64_t l2_pf_bytes, const __grid_constant__ QkvArgs<NB> args) {
+               int rotary_dim, int stages, float eps, const __grid_constant__ QkvArgs<NB> args) {
   constexpr int E = Chunk<WT>::kElems;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,15 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stage now (each warp the units it will consume first).
   if (lane == 0 && warp < nw)
     for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
-  // A hint for later in the block: o_proj's weights depend on nothing either,
-  // so this CTA asks for its share of them in L2 now and HBM keeps streaming
-  // while attention runs.
-  if (threadIdx.x == 32 && l2_pf != nullptr && l2_pf_bytes > 0) {
-    const int64_t lo = (l2_pf_bytes * blockIdx.x / gridDim.x) & ~int64_t(15);
-    const int64_t hi = (l2_pf_bytes * (blockIdx.x + 1) / gridDim.x) & ~int64_t(15);
-    for (int64_t o = lo; o < hi; o += 65536)
-      bulk_prefetch_l2(l2_pf + o, (uint32_t)(hi - o < 65536 ? hi - o : 65536));
-  }
   pdl_trigger();
   pdl_wait();
 
@@ -466,7 +462,7 @@ cudaError_t qkv_launch(const float* h, const void* norm_w, const void* qkv_w, co
                        float* q_rot, void* kc, void* vc, float* g_out, uint32_t* err, int hidden,
                        int n_q, int n_kv, int nb, int64_t capacity, int ring_capacity,
                        int rotary_dim, double theta, float eps, const int32_t* positions,
-                       const void* l2_pf, size_t l2_pf_bytes, cudaStream_t st) {
+                       cudaStream_t st) {
   QkvArgs<NB> args;
   for (int i = 0; i < kHeadDim / 2; ++i)
     args.inv_freq[i] = i < rotary_dim / 2 ? pow(theta, -2.0 * i / (double)rotary_dim) : 0.0;
@@ -484,8 +480,7 @@ cudaError_t qkv_launch(const float* h, const void* norm_w, const void* qkv_w, co
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, h, (const WT*)norm_w,
                     (const WT*)qkv_w, (const WT*)g_w, q_rot, (CT*)kc, (CT*)vc, g_out, err, hidden,
-                    n_q, n_kv, nb, capacity, ring_capacity, rotary_dim, stages, eps,
-                    static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
+                    n_q, n_kv, nb, capacity, ring_capacity, rotary_dim, stages, eps, args);
 }
 
 template <typename WT, typename CT>
@@ -493,12 +488,11 @@ cudaError_t qkv_chunk(int nb, const float* h, const void* norm_w, const void* qk
                       const void* g_w, float* q_rot, void* kc, void* vc, float* g_out,
                       uint32_t* err, int hidden, int n_q, int n_kv, int64_t capacity,
                       int ring_capacity, int rotary_dim, double theta, float eps,
-                      const int32_t* positions, const void* l2_pf, size_t l2_pf_bytes,
-                      cudaStream_t st) {
+                      const int32_t* positions, cudaStream_t st) {
 #define SPARK_QKV(NBV)                                                                           \
   return qkv_launch<WT, CT, NBV>(h, norm_w, qkv_w, g_w, q_rot, kc, vc, g_out, err, hidden, n_q, \
                                  n_kv, nb, capacity, ring_capacity, rotary_dim, theta, eps,     \
-                                 positions, l2_pf, l2_pf_bytes, st)
+                                 positions, st)
   if (nb == 1) SPARK_QKV(1);
   if (nb == 2) SPARK_QKV(2);
   SPARK_QKV(4);
@@ -539,8 +533,7 @@ cudaError_t launch_qkv_rope(int wdtype, int cdtype, const float* h, const void* 
                             const void* qkv_w, const void* g_w, float* q_rot, void* kc, void* vc,
                             float* g_out, uint32_t* err, int hidden, int n_q, int n_kv, int batch,
                             int64_t capacity, int ring_capacity, int rotary_dim, double theta,
-                            float eps, const int32_t* positions, const void* l2_pf,
-                            size_t l2_pf_bytes, cudaStream_t st) {
+                            float eps, const int32_t* positions, cudaStream_t st) {
   const size_t ce = cdtype == SPARK_BF16 ? 2 : 4;
   for (int b0 = 0; b0 < batch; b0 += kMaxChunk) {
     const int nb = batch - b0 < kMaxChunk ? batch - b0 : kMaxChunk;
@@ -554,24 +547,19 @@ cudaError_t launch_qkv_rope(int wdtype, int cdtype, const float* h, const void* 
     if (wdtype == SPARK_BF16 && cdtype == SPARK_BF16)
       e = qkv_chunk<__nv_bfloat16, __nv_bfloat16>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err,
                                                   hidden, n_q, n_kv, capacity, ring_capacity,
-                                                  rotary_dim, theta, eps, positions + b0,
-                                                  b0 == 0 ? l2_pf : nullptr,
-                                                  b0 == 0 ? l2_pf_bytes : 0, st);
+                                                  rotary_dim, theta, eps, positions + b0, st);
     else if (wdtype == SPARK_BF16)
       e = qkv_chunk<__nv_bfloat16, float>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden,
                                           n_q, n_kv, capacity, ring_capacity, rotary_dim, theta,
-                                          eps, positions + b0, b0 == 0 ? l2_pf : nullptr,
-                                                  b0 == 0 ? l2_pf_bytes : 0, st);
+                                          eps, positions + b0, st);
     else if (cdtype == SPARK_BF16)
       e = qkv_chunk<float, __nv_bfloat16>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden,
                                           n_q, n_kv, capacity, ring_capacity, rotary_dim, theta,
-                                          eps, positions + b0, b0 == 0 ? l2_pf : nullptr,
-                                                  b0 == 0 ? l2_pf_bytes : 0, st);
+                                          eps, positions + b0, st);
     else
       e = qkv_chunk<float, float>(nb, hb, norm_w, qkv_w, g_w, qb, kb, vb, gb, err, hidden, n_q,
                                   n_kv, capacity, ring_capacity, rotary_dim, theta, eps,
-                                  positions + b0, b0 == 0 ? l2_pf : nullptr,
-                                                  b0 == 0 ? l2_pf_bytes : 0, st);
+                                  positions + b0, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
