@@ -86,6 +86,9 @@ _SIGNATURES = {
     "spark_dbg_attention": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                            _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
+    "spark_dbg_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
+                                                   ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                                   _P, _P]),
     "spark_dbg_gate_oproj": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, _P, _P,
                                             ctypes.POINTER(SparkLayerWeights), ctypes.c_int32, _P, _P]),
     "spark_attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -255,6 +258,17 @@ def spark_dbg_attention(geom: SparkGeom, q_rot: torch.Tensor, kv: KvLayer, layer
                                       _dev_ptr(a, "a", torch.float32), int(n_ctas),
                                       _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
                                       _stream(stream)), "spark_dbg_attention")
+
+
+def spark_dbg_attention_noalloc(geom: SparkGeom, q_rot: torch.Tensor, kv: KvLayer, layer_class: int,
+                                positions, a: torch.Tensor, stream=None) -> None:
+    """spark_dbg_attention without a workspace: the library's fixed scratch
+    array is used instead (for callers that cannot allocate device memory)."""
+    kc, pos = kv.to_c(), _positions(positions)
+    _check(load().spark_dbg_attention_noalloc(ctypes.byref(geom), _dev_ptr(q_rot, "q_rot", torch.float32),
+                                              ctypes.byref(kc), int(layer_class), pos, len(positions),
+                                              _dev_ptr(a, "a", torch.float32), _stream(stream)),
+           "spark_dbg_attention_noalloc")
 
 
 def spark_dbg_gate_oproj(geom: SparkGeom, a: torch.Tensor, g_logits: torch.Tensor, h: torch.Tensor,
