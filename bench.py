@@ -175,8 +175,15 @@ class Copy:
         self.buf = [torch.empty_like(self.h), torch.empty_like(self.h)]
 
 
-def run_step(B, geom, wl, cp, ws, stream=None):
-    """One decode step of every layer through the public call."""
+def run_step(B, geom, wl, cp, ws, stream=None, path="stack"):
+    """One decode step of every layer through the public calls: one
+    spark_attn_decode_stack call for the whole stack, or spark_attn_decode
+    layer by layer."""
+    if path == "stack":
+        B.spark_attn_decode_stack(geom, cp.h, [w for _, w, _ in cp.layers], [kv for _, _, kv in cp.layers],
+                                  [B.SPARK_FULL if s.is_full else B.SPARK_SLIDING for s, _, _ in cp.layers],
+                                  wl.positions, cp.buf[0], ws, stream)
+        return cp.buf[0]
     cur = cp.h
     for i, (spec, w, kv) in enumerate(cp.layers):
         out = cp.buf[i % 2]
@@ -184,6 +191,12 @@ def run_step(B, geom, wl, cp, ws, stream=None):
                             wl.positions, out, ws, stream)
         cur = out
     return cur
+
+
+def stack_is_fused(wl) -> bool:
+    """Whether spark_attn_decode_stack runs this workload as one persistent
+    kernel (bf16, batch <= 4, spark2_5 geometry) rather than layer by layer."""
+    return wl.dtype == "bf16" and wl.batch <= 4
 
 
 STAGES = ("qkv_rope", "attention", "gate_oproj")
@@ -245,11 +258,13 @@ def bench_ours(args, wl, rank, local, world):
 
     # one CUDA graph per copy: a step's launches replayed without host overhead
     use_graph = not args.no_graph
+    path = args.path
+    fused = path == "stack" and stack_is_fused(wl)
     if use_graph:
-        graphs = [capture(lambda cp=cp: run_step(B, geom, wl, cp, ws)) for cp in cps]
+        graphs = [capture(lambda cp=cp: run_step(B, geom, wl, cp, ws, None, path)) for cp in cps]
         step = lambda i: graphs[i % copies].replay()  # noqa: E731
     else:
-        step = lambda i: run_step(B, geom, wl, cps[i % copies], ws, stream)  # noqa: E731
+        step = lambda i: run_step(B, geom, wl, cps[i % copies], ws, stream, path)  # noqa: E731
 
     for i in range(args.warmup):
         step(i)
@@ -282,7 +297,7 @@ def bench_ours(args, wl, rank, local, world):
     ms_total = max_over_ranks(start.elapsed_time(end), world, device)
     ms_per_step = ms_total / steps
     chunks = -(-wl.batch // 4)           # the projection kernels take up to 4 sequences each
-    kernels_per_step = L * (2 * chunks + 1)
+    kernels_per_step = -(-L // 40) if fused else L * (2 * chunks + 1)
 
     # per-kernel durations: each stage's launches (all layers, all copies)
     # replayed back to back in a graph between two events on this stream
@@ -301,11 +316,18 @@ def bench_ours(args, wl, rank, local, world):
         e1.record(stream)
         torch.cuda.synchronize()
         kavg[stage] = e0.elapsed_time(e1) / (reps * L * copies)   # ms per launch
-    share = {k: kavg[k] * L for k in kavg}
-    tot = sum(share.values())
-    top = max(share, key=share.get)
     bytes_key = {"qkv_rope": "qkv_gate", "attention": "attention", "gate_oproj": "gate_oproj"}
     per_launch = {k: sb["per_kernel"][bytes_key[k]] / L for k in STAGES}
+    launches = {k: L for k in STAGES}
+    if fused:
+        # one persistent kernel per step (per 40 layers): its duration is the step
+        kavg = {"decode_stack": ms_per_step / kernels_per_step, **{"layer_" + k: v for k, v in kavg.items()}}
+        per_launch = {"decode_stack": sb["total"] / kernels_per_step,
+                      **{"layer_" + k: v for k, v in per_launch.items()}}
+        launches = {"decode_stack": kernels_per_step, **{"layer_" + k: 0 for k in STAGES}}
+    share = {k: kavg[k] * launches[k] for k in kavg}
+    tot = sum(share.values())
+    top = max(share, key=share.get)
     peaks = measured_peaks()
     achieved = per_launch[top] / (kavg[top] * 1e-3) / 1e9
 
@@ -319,7 +341,7 @@ def bench_ours(args, wl, rank, local, world):
     for i in range(e2e_steps):
         cp = cps[i % copies]
         cp.h.copy_(h_host[i % 2], non_blocking=True)
-        res = run_step(B, geom, wl, cp, ws, stream)
+        res = run_step(B, geom, wl, cp, ws, stream, path)
         out_host.copy_(res, non_blocking=True)
         stream.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
@@ -351,6 +373,8 @@ def bench_ours(args, wl, rank, local, world):
                    + (["..."] if L > 8 else []),
                    "parallelism": f"replicas x{world} (independent sequences, no collective)",
                    "launch": "CUDA graph per step" if use_graph else "direct calls",
+                   "path": ("one persistent kernel per step (spark_attn_decode_stack)" if fused
+                            else "three kernels per layer"),
                    "l2": f"{copies} rotating copies of weights+caches ({copies * sb['total'] / 1e6:.0f} MB) "
                          f"vs {l2 / 1e6:.0f} MB L2"},
         "steps_per_s": round(1e3 / ms_per_step * world, 3),
@@ -362,9 +386,10 @@ def bench_ours(args, wl, rank, local, world):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
                      "bytes_per_launch": int(per_launch[top]),
                      "avg_launch_us": round(kavg[top] * 1e3, 3)},
-        "kernels": {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": L,
-                        "share": round(share[k] / tot, 4), "bytes_per_launch": int(per_launch[k]),
-                        "gbs": round(per_launch[k] / (kavg[k] * 1e-3) / 1e9, 1)} for k in STAGES},
+        "kernels": {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": launches[k],
+                        "share": round(share[k] / tot, 4) if tot else None,
+                        "bytes_per_launch": int(per_launch[k]),
+                        "gbs": round(per_launch[k] / (kavg[k] * 1e-3) / 1e9, 1)} for k in kavg},
         "e2e": {"value": round(tokens * e2e_steps / e2e_s, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * H * 4,
                 "launch": "direct calls, synchronised every step"},
@@ -443,6 +468,8 @@ def main():
     ap.add_argument("--copies", type=int, default=0, help="rotating input copies (0: enough to beat L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch steps directly instead of graph replay")
+    ap.add_argument("--path", default="layers", choices=["stack", "layers"],
+                    help="one call per layer (default, the faster path measured) or the whole step in one call")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, local, world = dist_env()

@@ -80,6 +80,10 @@ _SIGNATURES = {
                                          ctypes.POINTER(SparkKvLayer), ctypes.c_int32,
                                          ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P,
                                          ctypes.c_size_t, _P]),
+    "spark_attn_decode_stack": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.c_int32,
+                                               ctypes.POINTER(SparkLayerWeights), ctypes.POINTER(SparkKvLayer),
+                                               ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                               ctypes.c_int32, _P, _P, ctypes.c_size_t, _P]),
     "spark_dbg_qkv_rope": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkLayerWeights),
                                           ctypes.POINTER(SparkKvLayer), ctypes.c_int32,
                                           ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P, _P]),
@@ -237,6 +241,23 @@ def spark_attn_decode(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, k
                                     batch, _dev_ptr(out, "out", torch.float32),
                                     _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
                                     _stream(stream)), "spark_attn_decode")
+
+
+def spark_attn_decode_stack(geom: SparkGeom, h: torch.Tensor, weights: list, kvs: list, layer_classes,
+                            positions, out: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """One decode step through len(weights) layers (each layer's output is the
+    next one's input); ``out`` receives the last layer's output."""
+    n = len(weights)
+    if len(kvs) != n or len(layer_classes) != n:
+        raise ValueError("weights, kvs and layer_classes must have one entry per layer")
+    wc = (SparkLayerWeights * n)(*[w.to_c() for w in weights])
+    kc = (SparkKvLayer * n)(*[k.to_c() for k in kvs])
+    cls = (ctypes.c_int32 * n)(*[int(c) for c in layer_classes])
+    pos = _positions(positions)
+    _check(load().spark_attn_decode_stack(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32), n, wc, kc, cls,
+                                          pos, len(positions), _dev_ptr(out, "out", torch.float32),
+                                          _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                          _stream(stream)), "spark_attn_decode_stack")
 
 
 def spark_dbg_qkv_rope(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, kv: KvLayer,

@@ -26,52 +26,22 @@
 // states are merged through shared memory.
 #include <math.h>
 
+#include "attn_parts.cuh"
 #include "launch.h"
 
 namespace spark {
 namespace {
 
-constexpr int kTile = 16;                     // KV rows per pipeline stage
-constexpr int kConsumers = 4;                 // consumer warps (== kGroup: one head each in the merge)
 constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kConsumerThreads = kConsumers * 32;
-constexpr int kQStride = 4 * 64 + 4;          // floats per 64-dim q slice (4 heads) + bank shift
-constexpr int kLine = 128;                    // bytes per swizzled smem line
-constexpr int kSubBytes = kTile * kLine;      // one TMA box: kTile rows x 128 bytes
 constexpr int kMinRowsPerCta = 64;            // default grid: at least this many rows per CTA
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kBarConsumers = 1;              // named barrier id of the consumer warps
-
-template <typename CT>
-struct CacheT;
-// Pipeline depth (a multiple of the consumer count: tile k lives in stage
-// k % NS and belongs to warp k % 4, so each stage always serves one warp and
-// no wait can alias an older mbarrier phase).  Long histories take a deep
-// ring (the kernel runs alone for hundreds of microseconds); short ones a
-// shallow ring, so the kernel's CTAs leave room on each SM for the next
-// kernel's CTAs to start streaming o_proj's weights while attention runs.
-template <>
-struct CacheT<__nv_bfloat16> {
-  static constexpr int kLineElems = 64;
-  static constexpr int kDeep = 8;
-  static constexpr int kShallow = 4;
-  static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-};
-template <>
-struct CacheT<float> {
-  static constexpr int kLineElems = 32;
-  static constexpr int kDeep = 4;
-  static constexpr int kShallow = 4;
-  static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-};
-constexpr int64_t kDeepRows = 1 << 16;  // rows (x KV heads) per call from which the deep ring pays
+constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from which the deep ring pays
 
 template <typename CT, int NS>
 struct Smem {
   static_assert(NS % kConsumers == 0, "each stage must belong to one consumer warp");
   static constexpr int kStages = NS;
   static constexpr int kSubs = kHeadDim / CacheT<CT>::kLineElems;
-  static constexpr int kHalf = kSubs * kSubBytes;  // the K (or V) half of a stage
+  static constexpr int kHalf = kv_half_bytes<CT>();  // the K (or V) half of a stage
   static constexpr int kStage = 2 * kHalf;
   static constexpr int kQ = kStages * kStage;
   static constexpr int kP = kQ + 4 * kQStride * 4;
@@ -89,37 +59,6 @@ struct AttnArgs {
   int64_t prefix[MAXB + 1];  // rows read by sequences before b
   int32_t pos[MAXB];
 };
-
-// 8 consecutive dims [d0, d0 + 8) of tile row t of a K or V half-stage, as
-// four fp32 pairs.  The TMA 128-byte swizzle stores 16-byte chunk q of row t
-// at chunk q ^ (t & 7) of the row's line.
-template <typename CT>
-__device__ __forceinline__ void load8(const unsigned char* half, int t, int d0, float2 (&v)[4]);
-
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const unsigned char* half, int t, int d0,
-                                                     float2 (&v)[4]) {
-  const int sub = d0 >> 6, ch = (d0 & 63) >> 3;
-  const uint4 w = *reinterpret_cast<const uint4*>(half + sub * kSubBytes + t * kLine +
-                                                  ((ch ^ (t & 7)) << 4));
-  v[0] = bf16x2_to_f32x2(w.x);
-  v[1] = bf16x2_to_f32x2(w.y);
-  v[2] = bf16x2_to_f32x2(w.z);
-  v[3] = bf16x2_to_f32x2(w.w);
-}
-
-template <>
-__device__ __forceinline__ void load8<float>(const unsigned char* half, int t, int d0,
-                                             float2 (&v)[4]) {
-  const int sub = d0 >> 5, ch = (d0 & 31) >> 2;
-  const unsigned char* row = half + sub * kSubBytes + t * kLine;
-  const float4 a = *reinterpret_cast<const float4*>(row + ((ch ^ (t & 7)) << 4));
-  const float4 b = *reinterpret_cast<const float4*>(row + (((ch + 1) ^ (t & 7)) << 4));
-  v[0] = make_float2(a.x, a.y);
-  v[1] = make_float2(a.z, a.w);
-  v[2] = make_float2(b.x, b.y);
-  v[3] = make_float2(b.z, b.w);
-}
 
 // Enumerates, identically for the producer and the consumers, the groups a
 // CTA's share meets and the tiles of each.
@@ -243,14 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------ consumers
-  const int sl = lane >> 3, ri = lane & 7;
-  const int cta_last = G - 1;
-  auto cta_of = [&](int64_t x) -> int {
-    const int64_t cc = ((x + 1) * G - 1) / total;
-    return (int)(cc < cta_last ? cc : cta_last);
-  };
+  const MergeSmem msm{ms, ls, os};
   uint32_t k = 0;
   Share sh = share_begin(args, batch, n_kv, f0, f1);
+  AttnState st;
   while (sh.f < sh.f1) {
     const int b = sh.b, j = sh.j;
     const int64_t rows = args.prefix[b + 1] - args.prefix[b];
@@ -259,24 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Window w = window_of(pos[b], full != 0, window, ring_capacity);
 
     named_bar_sync(kBarConsumers, kConsumerThreads);  // the previous group's merge is done
-    {
-      const float* qg = q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
-      for (int e = tid; e < kGroup * kHeadDim; e += kConsumerThreads) {
-        const int h = e >> 8, d = e & 255;
-        q_s[(d >> 6) * kQStride + h * 64 + (d & 63)] = qg[e];
-      }
-    }
+    attn_load_q(q_s, q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, tid);
     named_bar_sync(kBarConsumers, kConsumerThreads);
-
-    float m[4], l[4];
-    float2 o[4][4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[h][i] = make_float2(0.f, 0.f);
-    }
+    st.reset();
 
     for (int64_t r = r0; r < r1;) {
       int64_t e = min(r1, r + kTile);
@@ -293,91 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           const unsigned char* kst = stages + s * S::kStage;
-          const unsigned char* vst = kst + S::kHalf;
-          // ---- scores: lanes (sl, ri) cover dims [64 sl, 64 sl + 64) of rows ri, ri + 8
-          float2 acc[2][4];
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-            for (int h = 0; h < 4; ++h) acc[rr][h] = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const float* qp = q_s + sl * kQStride + cc * 8;
-            float4 qa[4], qb[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              qa[h] = *reinterpret_cast<const float4*>(qp + h * 64);
-              qb[h] = *reinterpret_cast<const float4*>(qp + h * 64 + 4);
-            }
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              float2 kk[4];
-              load8<CT>(kst, ri + 8 * rr, sl * 64 + cc * 8, kk);
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                acc[rr][h] = ffma2(kk[0], make_float2(qa[h].x, qa[h].y), acc[rr][h]);
-                acc[rr][h] = ffma2(kk[1], make_float2(qa[h].z, qa[h].w), acc[rr][h]);
-                acc[rr][h] = ffma2(kk[2], make_float2(qb[h].x, qb[h].y), acc[rr][h]);
-                acc[rr][h] = ffma2(kk[3], make_float2(qb[h].z, qb[h].w), acc[rr][h]);
-              }
-            }
-          }
-          float sc[2][4];
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              float v = acc[rr][h].x + acc[rr][h].y;
-              v += __shfl_xor_sync(0xffffffffu, v, 8);
-              v += __shfl_xor_sync(0xffffffffu, v, 16);
-              sc[rr][h] = (ri + 8 * rr) < n ? v * scale_log2 : -INFINITY;
-            }
-          // ---- online softmax (base 2), per warp
-          float pr[2][4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            float mx = fmaxf(sc[0][h], sc[1][h]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            const float mn = fmaxf(m[h], mx);
-            const float corr = exp2f(m[h] - mn);
-            m[h] = mn;
-            l[h] *= corr;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              o[h][i].x *= corr;
-              o[h][i].y *= corr;
-            }
-            pr[0][h] = exp2f(sc[0][h] - mn);
-            pr[1][h] = exp2f(sc[1][h] - mn);
-            if (sl == 0) l[h] += pr[0][h] + pr[1][h];
-          }
-          if (sl < 2) {
-            const float4 pw = sl == 0 ? make_float4(pr[0][0], pr[0][1], pr[0][2], pr[0][3])
-                                      : make_float4(pr[1][0], pr[1][1], pr[1][2], pr[1][3]);
-            p_s[warp * kTile + ri + 8 * sl] = pw;
-          }
-          __syncwarp();
-          // ---- p.v: lane owns dims [8 lane, 8 lane + 8)
-          auto pv_row = [&](int t) {
-            const float4 pp = p_s[warp * kTile + t];
-            float2 vv[4];
-            load8<CT>(vst, t, 8 * lane, vv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              o[0][i] = ffma2(vv[i], make_float2(pp.x, pp.x), o[0][i]);
-              o[1][i] = ffma2(vv[i], make_float2(pp.y, pp.y), o[1][i]);
-              o[2][i] = ffma2(vv[i], make_float2(pp.z, pp.z), o[2][i]);
-              o[3][i] = ffma2(vv[i], make_float2(pp.w, pp.w), o[3][i]);
-            }
-          };
-          if (n == kTile) {
-#pragma unroll 4
-            for (int t = 0; t < kTile; ++t) pv_row(t);
-          } else {
-            for (int t = 0; t < n; ++t) pv_row(t);
-          }
+          attn_tile<CT>(kst, kst + S::kHalf, n, q_s, p_s + warp * kTile, scale_log2, st);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -386,92 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       r = e;
     }
 
-    // ---- merge the four warps' states of this group
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float lw = warp_sum(l[h]);
-      if (lane == 0) {
-        ms[warp * 4 + h] = m[h];
-        ls[warp * 4 + h] = lw;
-      }
-      float4* dst = reinterpret_cast<float4*>(os + (warp * 4 + h) * kHeadDim + 8 * lane);
-      dst[0] = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
-      dst[1] = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
-    }
-    named_bar_sync(kBarConsumers, kConsumerThreads);
-    const int h = warp;  // in the merge, warp w finishes query head 4j + w, lane its 8 dims
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kConsumers; ++ww) M = fmaxf(M, ms[ww * 4 + h]);
-    float L = 0.f, O[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) O[i] = 0.f;
-#pragma unroll
-    for (int ww = 0; ww < kConsumers; ++ww) {
-      const float mw = ms[ww * 4 + h];
-      const float scl = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      L = fmaf(ls[ww * 4 + h], scl, L);
-      const float4* src = reinterpret_cast<const float4*>(os + (ww * 4 + h) * kHeadDim + 8 * lane);
-      const float4 x0 = src[0], x1 = src[1];
-      O[0] = fmaf(x0.x, scl, O[0]); O[1] = fmaf(x0.y, scl, O[1]);
-      O[2] = fmaf(x0.z, scl, O[2]); O[3] = fmaf(x0.w, scl, O[3]);
-      O[4] = fmaf(x1.x, scl, O[4]); O[5] = fmaf(x1.y, scl, O[5]);
-      O[6] = fmaf(x1.z, scl, O[6]); O[7] = fmaf(x1.w, scl, O[7]);
-    }
     const int g = b * n_kv + j;
-    const int c_first = cta_of(gs), c_last = cta_of(gs + rows - 1);
-    const int cnt = c_last - c_first + 1;
-    float* a_dst = a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j + h) * kHeadDim + 8 * lane;
-    if (cnt == 1) {
-      if (!flags[0]) {
-        const float inv = 1.0f / L;
-        reinterpret_cast<float4*>(a_dst)[0] = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-        reinterpret_cast<float4*>(a_dst)[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
-      }
-    } else {
-      float* P = part + (int64_t)(c + g) * kPartFloats;
-      if (!flags[0]) {
-        float4* po = reinterpret_cast<float4*>(P + 8 + h * kHeadDim + 8 * lane);
-        po[0] = make_float4(O[0], O[1], O[2], O[3]);
-        po[1] = make_float4(O[4], O[5], O[6], O[7]);
-        if (lane == 0) {
-          P[h] = M;
-          P[4 + h] = L;
-        }
-      }
-      __threadfence();
-      named_bar_sync(kBarConsumers, kConsumerThreads);
-      if (tid == 0) {
-        int last = 0;
-        if (!flags[0]) last = atomicAdd(&counters[g], 1u) == (uint32_t)(cnt - 1);
-        flags[1] = last;
-      }
-      named_bar_sync(kBarConsumers, kConsumerThreads);
-      if (flags[1]) {
-        __threadfence();
-        const float* P0 = part + (int64_t)(c_first + g) * kPartFloats;
-        float M2 = -INFINITY;
-        for (int q = 0; q < cnt; ++q) M2 = fmaxf(M2, __ldcg(P0 + (int64_t)q * kPartFloats + h));
-        float L2 = 0.f, O2[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) O2[i] = 0.f;
-        for (int q = 0; q < cnt; ++q) {
-          const float* Pq = P0 + (int64_t)q * kPartFloats;
-          const float scl = exp2f(__ldcg(Pq + h) - M2);
-          L2 = fmaf(__ldcg(Pq + 4 + h), scl, L2);
-          const float4 x0 = __ldcg(reinterpret_cast<const float4*>(Pq + 8 + h * kHeadDim + 8 * lane));
-          const float4 x1 = __ldcg(reinterpret_cast<const float4*>(Pq + 8 + h * kHeadDim + 8 * lane + 4));
-          O2[0] = fmaf(x0.x, scl, O2[0]); O2[1] = fmaf(x0.y, scl, O2[1]);
-          O2[2] = fmaf(x0.z, scl, O2[2]); O2[3] = fmaf(x0.w, scl, O2[3]);
-          O2[4] = fmaf(x1.x, scl, O2[4]); O2[5] = fmaf(x1.y, scl, O2[5]);
-          O2[6] = fmaf(x1.z, scl, O2[6]); O2[7] = fmaf(x1.w, scl, O2[7]);
-        }
-        const float inv = 1.0f / L2;
-        reinterpret_cast<float4*>(a_dst)[0] = make_float4(O2[0] * inv, O2[1] * inv, O2[2] * inv, O2[3] * inv);
-        reinterpret_cast<float4*>(a_dst)[1] = make_float4(O2[4] * inv, O2[5] * inv, O2[6] * inv, O2[7] * inv);
-        if (tid == 0) counters[g] = 0;  // ready for the next call
-      }
-    }
+    const int c_first = cta_of(gs, total, G), c_last = cta_of(gs + rows - 1, total, G);
+    attn_finish_group<kConsumers>(st, msm, flags, part, counters,
+                      a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, g, c, c_first,
+                      c_last - c_first + 1);
     sh.f = gs + r1;
     if (++sh.j == n_kv) { sh.j = 0; ++sh.b; }
   }

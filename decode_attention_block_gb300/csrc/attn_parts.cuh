@@ -1,0 +1,361 @@
+// attn_parts.cuh -- the pieces of split-K GQA decode attention shared by the
+// per-layer attention kernel (attn.cu) and the persistent decode kernel
+// (stack.cu): the shared-memory tile layout, one warp's work on one 16-row
+// tile (q.k, online softmax, p.v) and the merge of a group's partial states
+// (turbospark-runtime 0.3.0, src/families/spark/attn.rs,
+// encode_attention_block -> src/kv_write.rs, encode_attention_any: GQA decode
+// attention over [kv_start, seq_len), scale 256^-0.5, no sinks).
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+
+namespace spark {
+
+constexpr int kTile = 16;                 // KV rows per pipeline stage
+constexpr int kConsumers = 4;             // consumer warps (== kGroup: one head each in the merge)
+constexpr int kConsumerThreads = kConsumers * 32;
+constexpr int kQStride = 4 * 64 + 4;      // floats per 64-dim q slice (4 heads) + bank shift
+constexpr int kLine = 128;                // bytes per swizzled smem line
+constexpr int kSubBytes = kTile * kLine;  // one TMA box: kTile rows x 128 bytes
+constexpr int kBarConsumers = 1;          // named barrier id of the warps that hold attention states
+constexpr int kBarMerge = 3;              // named barrier id of warps 0-3 while they merge a group
+
+template <typename CT>
+struct CacheT;
+// Pipeline depth of the per-layer kernel (a multiple of the consumer count:
+// tile k lives in stage k % NS and belongs to warp k % 4, so each stage always
+// serves one warp and no wait can alias an older mbarrier phase).  Long
+// histories take a deep ring (the kernel runs alone for hundreds of
+// microseconds); short ones a shallow ring.
+template <>
+struct CacheT<__nv_bfloat16> {
+  static constexpr int kLineElems = 64;
+  static constexpr int kDeep = 8;
+  static constexpr int kShallow = 4;
+  static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+};
+template <>
+struct CacheT<float> {
+  static constexpr int kLineElems = 32;
+  static constexpr int kDeep = 4;
+  static constexpr int kShallow = 4;
+  static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+};
+
+// bytes of one K (or V) half-stage: 16 rows x 256 elements as 128-byte boxes
+template <typename CT>
+__host__ __device__ constexpr int kv_half_bytes() {
+  return (kHeadDim / CacheT<CT>::kLineElems) * kSubBytes;
+}
+
+#if defined(__CUDACC__)
+
+// 8 consecutive dims [d0, d0 + 8) of tile row t of a K or V half-stage, as
+// four fp32 pairs.  The TMA 128-byte swizzle stores 16-byte chunk q of row t
+// at chunk q ^ (t & 7) of the row's line.
+template <typename CT>
+__device__ __forceinline__ void load8(const unsigned char* half, int t, int d0, float2 (&v)[4]);
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const unsigned char* half, int t, int d0,
+                                                     float2 (&v)[4]) {
+  const int sub = d0 >> 6, ch = (d0 & 63) >> 3;
+  const uint4 w = *reinterpret_cast<const uint4*>(half + sub * kSubBytes + t * kLine +
+                                                  ((ch ^ (t & 7)) << 4));
+  v[0] = bf16x2_to_f32x2(w.x);
+  v[1] = bf16x2_to_f32x2(w.y);
+  v[2] = bf16x2_to_f32x2(w.z);
+  v[3] = bf16x2_to_f32x2(w.w);
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const unsigned char* half, int t, int d0,
+                                             float2 (&v)[4]) {
+  const int sub = d0 >> 5, ch = (d0 & 31) >> 2;
+  const unsigned char* row = half + sub * kSubBytes + t * kLine;
+  const float4 a = *reinterpret_cast<const float4*>(row + ((ch ^ (t & 7)) << 4));
+  const float4 b = *reinterpret_cast<const float4*>(row + (((ch + 1) ^ (t & 7)) << 4));
+  v[0] = make_float2(a.x, a.y);
+  v[1] = make_float2(a.z, a.w);
+  v[2] = make_float2(b.x, b.y);
+  v[3] = make_float2(b.z, b.w);
+}
+
+// One warp's running softmax state for the 4 query heads of a KV head: max
+// and sum per head (base 2), and the unnormalised output, lane l holding dims
+// [8 l, 8 l + 8) of each head.
+struct AttnState {
+  float m[4], l[4];
+  float2 o[4][4];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[h][i] = make_float2(0.f, 0.f);
+    }
+  }
+};
+
+// q of the group's 4 heads into shared memory, in the slice layout attn_tile
+// reads (consumer threads only).  Every thread issues all its loads before it
+// stores anything, so the copy costs one L2 round trip, not eight.  q comes
+// from another CTA or kernel: loads bypass L1.
+template <int NT = kConsumerThreads>
+__device__ __forceinline__ void attn_load_q(float* q_s, const float* qg, int tid) {
+  constexpr int kF4 = kGroup * kHeadDim / 4;  // float4 of q
+  constexpr int kPer = (kF4 + NT - 1) / NT;
+  float4 v[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k)
+    if (tid + k * NT < kF4) v[k] = __ldcg(reinterpret_cast<const float4*>(qg) + tid + k * NT);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    if (tid + k * NT < kF4) {
+      const int e = 4 * (tid + k * NT);
+      const int h = e >> 8, d = e & 255;
+      *reinterpret_cast<float4*>(q_s + (d >> 6) * kQStride + h * 64 + (d & 63)) = v[k];
+    }
+  }
+}
+
+// One warp folds an n-row tile (rows 0..n-1 of the K and V half-stages) into
+// its state.  q.k: lanes (sl, ri) cover dims [64 sl, 64 sl + 64) of rows ri
+// and ri + 8 with packed fp32x2 FMAs, then sum over the four slices by
+// shuffles; p.v: lane l owns dims [8 l, 8 l + 8).  p_w is the warp's 16-row
+// probability scratch in shared memory.
+template <typename CT>
+__device__ __forceinline__ void attn_tile(const unsigned char* kst, const unsigned char* vst, int n,
+                                          const float* q_s, float4* p_w, float scale_log2,
+                                          AttnState& st) {
+  const int lane = threadIdx.x & 31;
+  const int sl = lane >> 3, ri = lane & 7;
+  float2 acc[2][4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) acc[rr][h] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    const float* qp = q_s + sl * kQStride + cc * 8;
+    float4 qa[4], qb[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      qa[h] = *reinterpret_cast<const float4*>(qp + h * 64);
+      qb[h] = *reinterpret_cast<const float4*>(qp + h * 64 + 4);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      float2 kk[4];
+      load8<CT>(kst, ri + 8 * rr, sl * 64 + cc * 8, kk);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        acc[rr][h] = ffma2(kk[0], make_float2(qa[h].x, qa[h].y), acc[rr][h]);
+        acc[rr][h] = ffma2(kk[1], make_float2(qa[h].z, qa[h].w), acc[rr][h]);
+        acc[rr][h] = ffma2(kk[2], make_float2(qb[h].x, qb[h].y), acc[rr][h]);
+        acc[rr][h] = ffma2(kk[3], make_float2(qb[h].z, qb[h].w), acc[rr][h]);
+      }
+    }
+  }
+  float sc[2][4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float v = acc[rr][h].x + acc[rr][h].y;
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      sc[rr][h] = (ri + 8 * rr) < n ? v * scale_log2 : -INFINITY;
+    }
+  // online softmax (base 2)
+  float pr[2][4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    float mx = fmaxf(sc[0][h], sc[1][h]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    const float mn = fmaxf(st.m[h], mx);
+    const float corr = exp2f(st.m[h] - mn);
+    st.m[h] = mn;
+    st.l[h] *= corr;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      st.o[h][i].x *= corr;
+      st.o[h][i].y *= corr;
+    }
+    pr[0][h] = exp2f(sc[0][h] - mn);
+    pr[1][h] = exp2f(sc[1][h] - mn);
+    if (sl == 0) st.l[h] += pr[0][h] + pr[1][h];
+  }
+  if (sl < 2) {
+    const float4 pw = sl == 0 ? make_float4(pr[0][0], pr[0][1], pr[0][2], pr[0][3])
+                              : make_float4(pr[1][0], pr[1][1], pr[1][2], pr[1][3]);
+    p_w[ri + 8 * sl] = pw;
+  }
+  __syncwarp();
+  auto pv_row = [&](int t) {
+    const float4 pp = p_w[t];
+    float2 vv[4];
+    load8<CT>(vst, t, 8 * lane, vv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      st.o[0][i] = ffma2(vv[i], make_float2(pp.x, pp.x), st.o[0][i]);
+      st.o[1][i] = ffma2(vv[i], make_float2(pp.y, pp.y), st.o[1][i]);
+      st.o[2][i] = ffma2(vv[i], make_float2(pp.z, pp.z), st.o[2][i]);
+      st.o[3][i] = ffma2(vv[i], make_float2(pp.w, pp.w), st.o[3][i]);
+    }
+  };
+  if (n == kTile) {
+#pragma unroll 4
+    for (int t = 0; t < kTile; ++t) pv_row(t);
+  } else {
+    for (int t = 0; t < n; ++t) pv_row(t);
+  }
+}
+
+// The CTA that holds the last row of flat position x, for a grid of G CTAs
+// sharing `total` rows equally (CTA c owns [total c / G, total (c+1) / G)).
+__device__ __forceinline__ int cta_of(int64_t x, int64_t total, int G) {
+  const int64_t cc = ((x + 1) * G - 1) / total;
+  return (int)(cc < G - 1 ? cc : G - 1);
+}
+
+// Shared memory of the group merge: per warp holding a state, the max and
+// the sum of each head and the unnormalised output of each head.
+struct MergeSmem {
+  float* ms;  // [NW][4]
+  float* ls;  // [NW][4]
+  float* os;  // [NW][4][256]
+};
+
+// Finish one group (sequence b, KV head j) of this CTA's share.  The NW warps
+// holding states (NW * 32 threads, all of them call this) put their states in
+// shared memory; warps 0-3 then merge them, warp w producing query head 4j + w
+// (lane l its dims [8 l, 8 l + 8)).  If the group lies inside this CTA
+// (cnt == 1) they write the normalised output, else this CTA's partial into
+// slot c + g, take a ticket, and if it is the last of the group's cnt CTAs
+// merge all the partials (slots c_first + g ...) into the output in one pass
+// with a running max, loading eight partials per round trip.  flags[0] is the
+// block's abort flag, flags[1] a scratch word.  a_head0 points at the output
+// of the group's first query head.
+template <int NW>
+__device__ __forceinline__ void attn_finish_group(const AttnState& st, const MergeSmem& sm,
+                                                  volatile int* flags, float* part,
+                                                  uint32_t* counters, float* a_head0, int g, int c,
+                                                  int c_first, int cnt) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const float lw = warp_sum(st.l[h]);
+    if (lane == 0) {
+      sm.ms[warp * 4 + h] = st.m[h];
+      sm.ls[warp * 4 + h] = lw;
+    }
+    float4* dst = reinterpret_cast<float4*>(sm.os + (warp * 4 + h) * kHeadDim + 8 * lane);
+    dst[0] = make_float4(st.o[h][0].x, st.o[h][0].y, st.o[h][1].x, st.o[h][1].y);
+    dst[1] = make_float4(st.o[h][2].x, st.o[h][2].y, st.o[h][3].x, st.o[h][3].y);
+  }
+  named_bar_sync(kBarConsumers, NW * 32);
+  if (warp >= kGroup) return;
+  const int h = warp;
+  float M = -INFINITY;
+#pragma unroll
+  for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, sm.ms[ww * 4 + h]);
+  float L = 0.f, O[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) O[i] = 0.f;
+#pragma unroll
+  for (int ww = 0; ww < NW; ++ww) {
+    const float mw = sm.ms[ww * 4 + h];
+    const float scl = mw == -INFINITY ? 0.f : exp2f(mw - M);
+    L = fmaf(sm.ls[ww * 4 + h], scl, L);
+    const float4* src = reinterpret_cast<const float4*>(sm.os + (ww * 4 + h) * kHeadDim + 8 * lane);
+    const float4 x0 = src[0], x1 = src[1];
+    O[0] = fmaf(x0.x, scl, O[0]); O[1] = fmaf(x0.y, scl, O[1]);
+    O[2] = fmaf(x0.z, scl, O[2]); O[3] = fmaf(x0.w, scl, O[3]);
+    O[4] = fmaf(x1.x, scl, O[4]); O[5] = fmaf(x1.y, scl, O[5]);
+    O[6] = fmaf(x1.z, scl, O[6]); O[7] = fmaf(x1.w, scl, O[7]);
+  }
+  float* a_dst = a_head0 + h * kHeadDim + 8 * lane;
+  if (cnt == 1) {
+    if (!flags[0]) {
+      const float inv = 1.0f / L;
+      reinterpret_cast<float4*>(a_dst)[0] = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+      reinterpret_cast<float4*>(a_dst)[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
+    }
+    return;
+  }
+  float* P = part + (int64_t)(c + g) * kPartFloats;
+  if (!flags[0]) {
+    float4* po = reinterpret_cast<float4*>(P + 8 + h * kHeadDim + 8 * lane);
+    po[0] = make_float4(O[0], O[1], O[2], O[3]);
+    po[1] = make_float4(O[4], O[5], O[6], O[7]);
+    if (lane == 0) {
+      P[h] = M;
+      P[4 + h] = L;
+    }
+  }
+  __threadfence();
+  named_bar_sync(kBarMerge, kGroup * 32);
+  if (tid == 0) {
+    int last = 0;
+    if (!flags[0]) last = atomicAdd(&counters[g], 1u) == (uint32_t)(cnt - 1);
+    flags[1] = last;
+  }
+  named_bar_sync(kBarMerge, kGroup * 32);
+  if (flags[1]) {
+    __threadfence();
+    const float* P0 = part + (int64_t)(c_first + g) * kPartFloats;
+    float M2 = -INFINITY, L2 = 0.f, O2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) O2[i] = 0.f;
+    constexpr int kBatch = 8;
+    for (int q0 = 0; q0 < cnt; q0 += kBatch) {
+      float mq[kBatch], lq[kBatch];
+      float4 x0[kBatch], x1[kBatch];
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        if (q0 + t < cnt) {
+          const float* Pq = P0 + (int64_t)(q0 + t) * kPartFloats;
+          mq[t] = __ldcg(Pq + h);
+          lq[t] = __ldcg(Pq + 4 + h);
+          x0[t] = __ldcg(reinterpret_cast<const float4*>(Pq + 8 + h * kHeadDim + 8 * lane));
+          x1[t] = __ldcg(reinterpret_cast<const float4*>(Pq + 8 + h * kHeadDim + 8 * lane + 4));
+        } else {
+          mq[t] = -INFINITY;
+          lq[t] = 0.f;
+          x0[t] = x1[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float mb = M2;
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) mb = fmaxf(mb, mq[t]);
+      const float rs = M2 == -INFINITY ? 0.f : exp2f(M2 - mb);  // rescale what came before
+      L2 *= rs;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) O2[i] *= rs;
+      M2 = mb;
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        const float scl = mq[t] == -INFINITY ? 0.f : exp2f(mq[t] - M2);
+        L2 = fmaf(lq[t], scl, L2);
+        O2[0] = fmaf(x0[t].x, scl, O2[0]); O2[1] = fmaf(x0[t].y, scl, O2[1]);
+        O2[2] = fmaf(x0[t].z, scl, O2[2]); O2[3] = fmaf(x0[t].w, scl, O2[3]);
+        O2[4] = fmaf(x1[t].x, scl, O2[4]); O2[5] = fmaf(x1[t].y, scl, O2[5]);
+        O2[6] = fmaf(x1[t].z, scl, O2[6]); O2[7] = fmaf(x1[t].w, scl, O2[7]);
+      }
+    }
+    const float inv = 1.0f / L2;
+    reinterpret_cast<float4*>(a_dst)[0] = make_float4(O2[0] * inv, O2[1] * inv, O2[2] * inv, O2[3] * inv);
+    reinterpret_cast<float4*>(a_dst)[1] = make_float4(O2[4] * inv, O2[5] * inv, O2[6] * inv, O2[7] * inv);
+    if (tid == 0) counters[g] = 0;  // ready for the next call
+  }
+}
+
+#endif  // __CUDACC__
+
+}  // namespace spark

@@ -20,6 +20,9 @@ constexpr int kGroup = 4;            // query heads per KV head
 constexpr int kMaxAttnCtas = 1024;   // partial-result slots reserved for CTAs
 constexpr int kPartFloats = 2 * kGroup + kGroup * kHeadDim;  // m[4], l[4], o[4][256]
 
+// every bounded wait in the kernels gives up after this long
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // device error word bits
 constexpr uint32_t kErrWaitTimeout = 1u;
 constexpr uint32_t kErrIndex = 2u;
@@ -67,20 +70,26 @@ __host__ __device__ inline int64_t write_slot_of(int64_t position, int64_t ring_
 // ---------------------------------------------------------------------------
 struct WsLayout {
   size_t err = 0;       // uint32 error word
+  size_t gbar = 0;      // uint32 [2] grid barrier of the persistent decode kernel
   size_t counters = 0;  // uint32 [batch * n_kv] merge tickets
   size_t g = 0;         // f32 [batch][n_q] gate logits
   size_t q_rot = 0;     // f32 [batch][q_dim] rotated queries
   size_t a = 0;         // f32 [batch][q_dim] attention output
+  size_t hbuf = 0;      // f32 [2][batch][hidden] residual stream between layers
   size_t part = 0;      // f32 [kMaxAttnCtas + batch * n_kv][kPartFloats]
+  size_t trace = 0;     // u64 [kTraceWords] phase timestamps of the persistent kernel (opt-in)
   size_t total = 0;
 };
 
+constexpr int kTraceWords = 4096;
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int n_q, int n_kv, int batch) {
+inline WsLayout ws_layout(int hidden, int n_q, int n_kv, int batch) {
   WsLayout L;
-  size_t off = 256;
   L.err = 0;
+  L.gbar = 64;
+  size_t off = 256;
   L.counters = off;
   off = align_up(off + sizeof(uint32_t) * (size_t)batch * n_kv, 256);
   L.g = off;
@@ -89,8 +98,12 @@ inline WsLayout ws_layout(int n_q, int n_kv, int batch) {
   off = align_up(off + sizeof(float) * (size_t)batch * n_q * kHeadDim, 256);
   L.a = off;
   off = align_up(off + sizeof(float) * (size_t)batch * n_q * kHeadDim, 256);
+  L.hbuf = off;
+  off = align_up(off + sizeof(float) * 2 * (size_t)batch * hidden, 256);
   L.part = off;
   off = align_up(off + sizeof(float) * (size_t)(kMaxAttnCtas + (size_t)batch * n_kv) * kPartFloats, 256);
+  L.trace = off;
+  off = align_up(off + sizeof(uint64_t) * kTraceWords, 256);
   L.total = off;
   return L;
 }

@@ -23,6 +23,8 @@
 // launch): the weight stream does not depend on the previous kernel.  Warps
 // take units round-robin; the warp that frees a stage refills it.
 //
+// The rope angles' cos and sin come from the host, computed in double.
+//
 // The RMSNorm needs no pass before the GEMV: rms(h) scales every output of a
 // row by the same 1/sqrt(mean(h^2) + eps), so the warps dot the rows with
 // h * w and the scale is applied in the epilogue.
@@ -33,6 +35,8 @@
 // v rows, rows past the rotary width and g rows are paired as neighbours.
 #include <math.h>
 
+#include "checks.h"
+#include "gemv_parts.cuh"
 #include "launch.h"
 
 namespace spark {
@@ -40,7 +44,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kMaxPer = 8192 / 4 / kThreads;  // float4 of an activation vector per thread
 // Shared memory per CTA for the activations and the weight stages (one CTA
 // per SM).  Measured on GB300: a ~100 KB budget that lets the next kernel's
 // CTAs co-reside gains less than the deeper pool loses.
@@ -49,163 +53,11 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 #endif
 constexpr size_t kSmemBudget = SPARK_GEMV_SMEM_KB * 1024;
 
-template <typename WT>
-struct Chunk;
-template <>
-struct Chunk<float> {
-  static constexpr int kElems = 4;
-};
-template <>
-struct Chunk<__nv_bfloat16> {
-  static constexpr int kElems = 8;
-};
-
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ void store_elem(float* p, float v) { *p = v; }
-__device__ __forceinline__ void store_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
-
-// Activation vectors live in shared memory permuted so that lane l's values
-// for its 16-byte weight chunk c = l + 32 i are read as consecutive float4s
-// across lanes (no bank conflicts): element n of chunk c sits at float4
-// ((i * E/4 + (n % E) / 4) * 32 + l), component n % 4.
-template <int E>
-__device__ __forceinline__ int xperm_index(int n) {
-  const int c = n / E, l = c & 31, i = c >> 5, hq = (n % E) >> 2;
-  return ((i * (E / 4) + hq) * 32 + l) * 4 + (n & 3);
-}
-
-// sum over the chunk of w[k] * x[k], accumulated pairwise into acc
-template <typename WT>
-__device__ __forceinline__ void dot_chunk(uint4 w, const float4* xp, float2& acc);
-
-template <>
-__device__ __forceinline__ void dot_chunk<__nv_bfloat16>(uint4 w, const float4* xp, float2& acc) {
-  const float4 x0 = xp[0], x1 = xp[32];
-  acc = ffma2(bf16x2_to_f32x2(w.x), make_float2(x0.x, x0.y), acc);
-  acc = ffma2(bf16x2_to_f32x2(w.y), make_float2(x0.z, x0.w), acc);
-  acc = ffma2(bf16x2_to_f32x2(w.z), make_float2(x1.x, x1.y), acc);
-  acc = ffma2(bf16x2_to_f32x2(w.w), make_float2(x1.z, x1.w), acc);
-}
-
-template <>
-__device__ __forceinline__ void dot_chunk<float>(uint4 w, const float4* xp, float2& acc) {
-  const float4 x0 = xp[0];
-  acc = ffma2(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), make_float2(x0.x, x0.y), acc);
-  acc = ffma2(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), make_float2(x0.z, x0.w), acc);
-}
-
-// cos / sin of position * inv_freq with the product reduced modulo 2*pi in
-// fp64 (at position 131072 an fp32 angle would be off by ~1e-2 rad)
-__device__ __forceinline__ void rope_cos_sin(int32_t pos, double inv_freq, float* c, float* s) {
-  constexpr double kTwoPiHi = 6.283185307179586232;    // 2*pi rounded to double
-  constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
-  constexpr double kInvTwoPi = 0.15915494309189533577;
-  const double phi = (double)pos * inv_freq;
-  const double n = rint(phi * kInvTwoPi);
-  double r = fma(-n, kTwoPiHi, phi);
-  r = fma(-n, kTwoPiLo, r);
-  sincosf((float)r, s, c);
-}
-
 template <int NB>
 struct QkvArgs {
-  double inv_freq[kHeadDim / 2];  // theta^(-2i/r), i < r/2
+  float2 cs[NB][kHeadDim / 2];  // (cos, sin) of the rope angle of pair i for sequence b
   int32_t pos[NB];
 };
-
-enum RowKind { kQ = 0, kK = 1, kV = 2, kG = 3 };
-
-struct Unit {
-  int row_a, row_b;  // rows of [q_k_v_proj; g_proj]
-  int kind, head;    // head index within its kind
-  int da, db;        // output dims of the two rows (within the head, or g index)
-  int pair;          // rope pair index (-1: no rotation)
-};
-
-__device__ __forceinline__ Unit unit_of(int u, int n_q, int n_kv, int rotary_dim) {
-  Unit x;
-  const int n_heads = n_q + 2 * n_kv;
-  if (u < n_heads * (kHeadDim / 2)) {
-    const int hd = u / (kHeadDim / 2), t = u % (kHeadDim / 2);
-    x.kind = hd < n_q ? kQ : (hd < n_q + n_kv ? kK : kV);
-    x.head = x.kind == kQ ? hd : (x.kind == kK ? hd - n_q : hd - n_q - n_kv);
-    const int half = rotary_dim / 2;
-    if (x.kind != kV && t < half) {
-      x.da = t;
-      x.db = t + half;
-      x.pair = t;
-    } else {
-      x.da = x.kind == kV ? 2 * t : rotary_dim + 2 * (t - half);
-      x.db = x.da + 1;
-      x.pair = -1;
-    }
-    x.row_a = hd * kHeadDim + x.da;
-    x.row_b = hd * kHeadDim + x.db;
-  } else {
-    const int gi = u - n_heads * (kHeadDim / 2);
-    x.kind = kG;
-    x.head = 0;
-    x.da = 2 * gi;
-    x.db = 2 * gi + 1;
-    x.pair = -1;
-    x.row_a = n_heads * kHeadDim + x.da;
-    x.row_b = x.row_a + 1;
-  }
-  return x;
-}
-
-// ---------------------------------------------------------------------------
-// per-warp row streaming shared by both kernels
-// ---------------------------------------------------------------------------
-
-// Wait for this warp's stage, bounded; on time-out raise the block's abort
-// flag and the error word.  Returns false if the stage must not be read.
-__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           uint32_t* err) {
-  if (mbar_wait_bounded(bar, parity, abort_flag, kWaitLimitNs)) return true;
-  if ((threadIdx.x & 31) == 0 && !*abort_flag) {
-    *abort_flag = 1;
-    if (err) atomicOr(err, kErrWaitTimeout);
-  }
-  return false;
-}
-
-// acc[b] (b < NB) += row . x_b for one weight row held in shared memory
-template <typename WT, int NB>
-__device__ __forceinline__ void row_dot(const unsigned char* row, const float* xs, int xfloats,
-                                        int nchunk, float2 (&acc)[NB]) {
-  constexpr int E = Chunk<WT>::kElems;
-  const int lane = threadIdx.x & 31;
-  for (int c = lane, i = 0; c < nchunk; c += 32, ++i) {
-    const uint4 w = *reinterpret_cast<const uint4*>(row + (size_t)c * 16);
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float4* xp = reinterpret_cast<const float4*>(xs + b * xfloats) + i * (E / 4) * 32 + lane;
-      dot_chunk<WT>(w, xp, acc[b]);
-    }
-  }
-}
-
-// two rows sharing one pass over the activation
-template <typename WT, int NB>
-__device__ __forceinline__ void row_dot2(const unsigned char* ra, const unsigned char* rb,
-                                         const float* xs, int xfloats, int nchunk,
-                                         float2 (&acc_a)[NB], float2 (&acc_b)[NB]) {
-  constexpr int E = Chunk<WT>::kElems;
-  const int lane = threadIdx.x & 31;
-#pragma unroll 2
-  for (int c = lane, i = 0; c < nchunk; c += 32, ++i) {
-    const uint4 wa = *reinterpret_cast<const uint4*>(ra + (size_t)c * 16);
-    const uint4 wb = *reinterpret_cast<const uint4*>(rb + (size_t)c * 16);
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float4* xp = reinterpret_cast<const float4*>(xs + b * xfloats) + i * (E / 4) * 32 + lane;
-      dot_chunk<WT>(wa, xp, acc_a[b]);
-      dot_chunk<WT>(wb, xp, acc_b[b]);
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // RMSNorm + q_k_v_proj + g_proj + rope + cache write
@@ -267,18 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // activations: x = h * w (unscaled) and sum(h^2) per sequence
   float ss[NB];
-#pragma unroll
-  for (int b = 0; b < NB; ++b) ss[b] = 0.f;
-  for (int n = threadIdx.x; n < hidden; n += kThreads) {
-    const float w = to_f32(norm_w[n]);
-    const int pi = xperm_index<E>(n);
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float v = b < nb ? h[(int64_t)b * hidden + n] : 0.f;
-      ss[b] = fmaf(v, v, ss[b]);
-      xs[b * xfloats + pi] = v * w;
-    }
-  }
+  build_x_norm<E, WT, NB, kThreads, kMaxPer>(h, norm_w, hidden, nb, xs, xfloats, ss, threadIdx.x);
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const float v = warp_sum(ss[b]);
@@ -321,10 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane < nb) {
       const int b = lane;
       if (un.pair >= 0) {
-        float c, sn;
-        rope_cos_sin(args.pos[b], args.inv_freq[un.pair], &c, &sn);
-        const float ra = va * c - vb * sn;
-        const float rb = vb * c + va * sn;
+        const float2 cs = args.cs[b][un.pair];
+        const float ra = va * cs.x - vb * cs.y;
+        const float rb = vb * cs.x + va * cs.y;
         va = ra;
         vb = rb;
       }
@@ -392,18 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
 
   // gated attention output: a * sigmoid(g), one gate scalar per head
-  for (int n = threadIdx.x; n < q_dim; n += kThreads) {
-    const int pi = xperm_index<E>(n);
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float v = 0.f;
-      if (b < nb) {
-        const float z = g[(int64_t)b * n_q + n / kHeadDim];
-        v = a[(int64_t)b * q_dim + n] * (1.0f / (1.0f + expf(-z)));
-      }
-      xs[b * xfloats + pi] = v;
-    }
-  }
+  build_x_gated<E, NB, kThreads, kMaxPer>(a, g, q_dim, n_q, nb, xs, xfloats, threadIdx.x);
   __syncthreads();
 
   for (int k = warp; warp < nw && k < cnt; k += nw) {
@@ -464,8 +293,7 @@ cudaError_t qkv_launch(const float* h, const void* norm_w, const void* qkv_w, co
                        int rotary_dim, double theta, float eps, const int32_t* positions,
                        cudaStream_t st) {
   QkvArgs<NB> args;
-  for (int i = 0; i < kHeadDim / 2; ++i)
-    args.inv_freq[i] = i < rotary_dim / 2 ? pow(theta, -2.0 * i / (double)rotary_dim) : 0.0;
+  checks::fill_rope_table(&args.cs[0][0], kHeadDim / 2, nb, positions, rotary_dim, theta);
   for (int b = 0; b < NB; ++b) args.pos[b] = b < nb ? positions[b] : 0;
   const size_t row_bytes = (size_t)hidden * sizeof(WT);
   const size_t xb = xbytes<WT>(hidden, NB);

@@ -159,6 +159,23 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
                       const int32_t* positions, int32_t batch, float* out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step through a stack of n_layers attention blocks (mod.rs's
+ * layer loop with the MLP left out: the output of layer l is the input of
+ * layer l+1).  The same result as calling spark_attn_decode layer by layer,
+ * with h -> out, then out -> out; for bf16 weights and caches, batch <= 4,
+ * n_kv <= 4, hidden <= 4096 and full_rotary_dim a multiple of 4 it runs as
+ * one persistent kernel per 40 layers (cooperative launch, one CTA per SM)
+ * whose weight and KV streams run ahead across layer boundaries; otherwise it
+ * falls back to the per-layer path.
+ *   w, kv, layer_class  arrays of n_layers entries (host arrays of device
+ *                       pointers), positions as for spark_attn_decode.
+ *   out may equal h.  workspace as for spark_attn_decode. */
+int spark_attn_decode_stack(const spark_geom* g, const float* h, int32_t n_layers,
+                            const spark_layer_weights* w, const spark_kv_layer* kv,
+                            const int32_t* layer_class, const int32_t* positions,
+                            int32_t batch, float* out, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* ---- the block's stages, one kernel each (same conventions) ------------- */
 
 /* Input RMSNorm + q_k_v_proj + g_proj + split + per-class NeoX rope + the

@@ -367,3 +367,103 @@ def test_zero_o_proj_returns_h_exactly(B):
     B.spark_attn_decode(geom, h, B.LayerWeights(**w), B.KvLayer(kc, vc, 0), B.SPARK_FULL, wl.positions, out, ws)
     torch.cuda.synchronize()
     assert torch.equal(out, h)
+
+
+# ---------------------------------------------------------------------------
+# the whole stack in one call (one persistent kernel, or the per-layer path)
+# ---------------------------------------------------------------------------
+
+def run_stack_parity(B, wl: synth.Workload, sample=None):
+    """spark_attn_decode_stack over every layer of the workload against the
+    oracle run layer after layer (each layer's input is its own previous
+    output), and against the per-layer C entry point."""
+    seqs = list(range(wl.batch)) if sample is None else list(sample)
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, wl.batch)
+    ogeom = oracle_geom(wl)
+    h = synth.make_h(wl, "cuda")
+    layers = []
+    for li, spec in enumerate(wl.layers):
+        w = synth.make_weights(wl, li, "cuda")
+        kc, vc = synth.make_cache(wl, li, "cuda")
+        layers.append((spec, w, kc, vc, kc.clone(), vc.clone()))
+    # oracle chain, from the caches as they are before any call
+    cur = {b: synth.to_numpy(h[b]).astype(np.float64) for b in seqs}
+    h0 = {b: cur[b].copy() for b in seqs}
+    want_rows = []
+    for spec, w, kc, vc, _, _ in layers:
+        k_np = SeqCaches({b: synth.to_numpy(kc[b]) for b in seqs}, np.uint16 if wl.dtype == "bf16" else np.float32)
+        v_np = SeqCaches({b: synth.to_numpy(vc[b]) for b in seqs}, k_np.dtype)
+        h_in = np.zeros((wl.batch, wl.hidden))
+        for b in seqs:
+            h_in[b] = cur[b]
+        res = oracle.decode_step(ogeom, h_in, np_weights(w), k_np, v_np, spec.is_full, wl.positions,
+                                 spec.ring_capacity, sequences=seqs)
+        want_rows.append(res)
+        for i, b in enumerate(seqs):
+            cur[b] = res["out"][i]
+    # the stack call
+    out = torch.empty_like(h)
+    B.spark_attn_decode_stack(geom, h, [B.LayerWeights(**w) for _, w, *_ in layers],
+                              [B.KvLayer(kc, vc, spec.ring_capacity) for spec, _, kc, vc, _, _ in layers],
+                              [B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING for spec, *_ in layers],
+                              wl.positions, out, ws)
+    torch.cuda.synchronize()
+    assert B.spark_attn_error_word(ws) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    for b in seqs:
+        assert_close(got[b] - h0[b], cur[b] - h0[b], f"stack output b={b}")
+    for li, (spec, w, kc, vc, kc0, vc0) in enumerate(layers):
+        res = want_rows[li]
+        for i, b in enumerate(seqs):
+            slot = res["slot"][i]
+            assert_close(f64(synth.to_numpy(kc[b, slot])), f64(res["k_row"][i]), f"layer {li} k row b={b}")
+            assert_close(f64(synth.to_numpy(vc[b, slot])), f64(res["v_row"][i]), f"layer {li} v row b={b}")
+        for b in range(wl.batch):
+            slot = oracle.write_slot(wl.positions[b], spec.ring_capacity)
+            assert_only_slot_changed(kc0, kc, b, slot, f"layer {li} K b={b}")
+            assert_only_slot_changed(vc0, vc, b, slot, f"layer {li} V b={b}")
+    # the per-layer entry point on the same inputs (caches restored) gives the same answer
+    for spec, w, kc, vc, kc0, vc0 in layers:
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+    cur_t = h.clone()
+    for spec, w, kc, vc, _, _ in layers:
+        nxt = torch.empty_like(cur_t)
+        B.spark_attn_decode(geom, cur_t, B.LayerWeights(**w), B.KvLayer(kc, vc, spec.ring_capacity),
+                            B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING, wl.positions, nxt, ws)
+        cur_t = nxt
+    torch.cuda.synchronize()
+    ma, rel = err_stats(got - synth.to_numpy(h).astype(np.float64),
+                        cur_t.cpu().numpy().astype(np.float64) - synth.to_numpy(h).astype(np.float64))
+    assert ma < 2e-3 and rel < 1e-3, f"stack vs per-layer: max_abs {ma:.3e} rel {rel:.3e}"
+
+
+def test_stack_full_sliding_bf16_b1_pos700(B):
+    run_stack_parity(B, WORKLOADS["full+sliding_bf16_b1_pos700"])
+
+
+def test_stack36_bf16_b1_ctx8192(B):
+    run_stack_parity(B, WORKLOADS["stack36_bf16_b1_ctx8192"])
+
+
+def test_stack_batch_edges(B):
+    wl = synth.Workload("edges", "", "bf16", [0, 1, 513, 700],
+                        [synth.LayerSpec(True, 0), synth.LayerSpec(False, 512), synth.LayerSpec(False, 512)],
+                        seed=620)
+    run_stack_parity(B, wl)
+
+
+def test_stack_two_sequences_and_fallbacks(B):
+    run_stack_parity(B, synth.Workload("b2", "", "bf16", [40, 3000],
+                                       [synth.LayerSpec(False, 512), synth.LayerSpec(True, 0)], seed=621))
+    # fp32 weights and batch 8 take the per-layer path
+    run_stack_parity(B, WORKLOADS["sliding_f32_b1_pos40"])
+    run_stack_parity(B, synth.Workload("b8", "", "bf16", [5, 9, 700, 1, 40, 513, 88, 300],
+                                       [synth.LayerSpec(True, 0), synth.LayerSpec(False, 512)], seed=622))
+
+
+def test_stack_more_layers_than_one_launch(B):
+    wl = synth.Workload("stack45", "", "bf16", [600],
+                        [synth.LayerSpec(i % 4 == 3, 0 if i % 4 == 3 else 512) for i in range(45)], seed=623)
+    run_stack_parity(B, wl)
