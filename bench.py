@@ -193,6 +193,15 @@ def run_step(B, geom, wl, cp, ws, stream=None, path="stack"):
     return cur
 
 
+def projection_launches(wl) -> int:
+    """Kernels one projection (q_k_v_proj or o_proj) of one layer launches:
+    the GEMV kernel per 4 sequences up to batch 4 or with fp32 weights, else
+    a prologue and a tensor-core GEMM per 128 sequences."""
+    if wl.batch <= 4 or wl.dtype != "bf16":
+        return -(-wl.batch // 4)
+    return 2 * -(-wl.batch // 128)
+
+
 def stack_is_fused(wl) -> bool:
     """Whether spark_attn_decode_stack runs this workload as one persistent
     kernel (bf16, batch <= 4, spark2_5 geometry) rather than layer by layer."""
@@ -211,11 +220,11 @@ def stage_launcher(B, geom, wl, cp, ws, bufs, stage):
             out = cp.buf[i % 2]
             cls = B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING
             if stage == "qkv_rope":
-                B.spark_dbg_qkv_rope(geom, cur, w, kv, cls, wl.positions, bufs["q_rot"], bufs["g"])
+                B.spark_dbg_qkv_rope(geom, cur, w, kv, cls, wl.positions, bufs["q_rot"], bufs["g"], ws)
             elif stage == "attention":
                 B.spark_dbg_attention(geom, bufs["q_rot"], kv, cls, wl.positions, bufs["a"], ws, 0)
             else:
-                B.spark_dbg_gate_oproj(geom, bufs["a"], bufs["g"], cur, w, out)
+                B.spark_dbg_gate_oproj(geom, bufs["a"], bufs["g"], cur, w, out, ws)
             cur = out
     return go
 
@@ -296,8 +305,7 @@ def bench_ours(args, wl, rank, local, world):
     clocks = sampler.summary()
     ms_total = max_over_ranks(start.elapsed_time(end), world, device)
     ms_per_step = ms_total / steps
-    chunks = -(-wl.batch // 4)           # the projection kernels take up to 4 sequences each
-    kernels_per_step = -(-L // 40) if fused else L * (2 * chunks + 1)
+    kernels_per_step = -(-L // 40) if fused else L * (2 * projection_launches(wl) + 1)
 
     # per-kernel durations: each stage's launches (all layers, all copies)
     # replayed back to back in a graph between two events on this stream

@@ -19,6 +19,7 @@ import torch
 from .build_lib import LIB_PATH
 
 SPARK_OK = 0
+SPARK_PATH_AUTO, SPARK_PATH_GEMV, SPARK_PATH_MMA = 0, 1, 2
 SPARK_F32 = 0
 SPARK_BF16 = 1
 SPARK_SLIDING = 0
@@ -86,7 +87,8 @@ _SIGNATURES = {
                                                ctypes.c_int32, _P, _P, ctypes.c_size_t, _P]),
     "spark_dbg_qkv_rope": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkLayerWeights),
                                           ctypes.POINTER(SparkKvLayer), ctypes.c_int32,
-                                          ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P, _P]),
+                                          ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P,
+                                          ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "spark_dbg_attention": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                            _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
@@ -94,7 +96,8 @@ _SIGNATURES = {
                                                    ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                                    _P, _P]),
     "spark_dbg_gate_oproj": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, _P, _P,
-                                            ctypes.POINTER(SparkLayerWeights), ctypes.c_int32, _P, _P]),
+                                            ctypes.POINTER(SparkLayerWeights), ctypes.c_int32, _P,
+                                            ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "spark_attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "spark_attn_abi_version": (ctypes.c_int32, []),
 }
@@ -262,12 +265,14 @@ def spark_attn_decode_stack(geom: SparkGeom, h: torch.Tensor, weights: list, kvs
 
 def spark_dbg_qkv_rope(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, kv: KvLayer,
                        layer_class: int, positions, q_rot: torch.Tensor, g_logits: torch.Tensor,
-                       stream=None) -> None:
+                       ws: torch.Tensor, path: int = 0, stream=None) -> None:
     wc, kc, pos = weights.to_c(), kv.to_c(), _positions(positions)
     _check(load().spark_dbg_qkv_rope(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32), ctypes.byref(wc),
                                      ctypes.byref(kc), int(layer_class), pos, len(positions),
                                      _dev_ptr(q_rot, "q_rot", torch.float32),
-                                     _dev_ptr(g_logits, "g_logits", torch.float32), _stream(stream)),
+                                     _dev_ptr(g_logits, "g_logits", torch.float32), int(path),
+                                     _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                     _stream(stream)),
            "spark_dbg_qkv_rope")
 
 
@@ -293,12 +298,15 @@ def spark_dbg_attention_noalloc(geom: SparkGeom, q_rot: torch.Tensor, kv: KvLaye
 
 
 def spark_dbg_gate_oproj(geom: SparkGeom, a: torch.Tensor, g_logits: torch.Tensor, h: torch.Tensor,
-                         weights: LayerWeights, out: torch.Tensor, stream=None) -> None:
+                         weights: LayerWeights, out: torch.Tensor, ws: torch.Tensor, path: int = 0,
+                         stream=None) -> None:
     wc = weights.to_c()
     _check(load().spark_dbg_gate_oproj(ctypes.byref(geom), _dev_ptr(a, "a", torch.float32),
                                        _dev_ptr(g_logits, "g_logits", torch.float32),
                                        _dev_ptr(h, "h", torch.float32), ctypes.byref(wc), int(h.shape[0]),
-                                       _dev_ptr(out, "out", torch.float32), _stream(stream)),
+                                       _dev_ptr(out, "out", torch.float32), int(path),
+                                       _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                       _stream(stream)),
            "spark_dbg_gate_oproj")
 
 

@@ -31,12 +31,74 @@ int device_sm_count() {
   return n;
 }
 
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
 }  // namespace spark
 
 using namespace spark;
 using namespace spark::checks;
 
 namespace {
+
+// Up to this batch the GEMV kernels read each weight once for all sequences
+// (they keep every sequence's activations in registers); above it the
+// projections run as GEMMs on the tensor cores.
+constexpr int kGemvMaxBatch = 4;
+
+MmaWorkspace mma_ws(void* ws, const WsLayout& L) {
+  MmaWorkspace m;
+  m.x = ws_at<__nv_bfloat16>(ws, L.mx);
+  m.cs = ws_at<float2>(ws, L.mcs);
+  m.part = ws_at<float>(ws, L.mpart);
+  m.tickets = ws_at<uint32_t>(ws, L.mtick);
+  m.trace = ws_at<uint64_t>(ws, L.trace);
+  return m;
+}
+
+// Which kernels compute a projection: SPARK_PATH_MMA / SPARK_PATH_GEMV, or
+// a negative status if the caller forced a path these arguments cannot take.
+int pick_path(int32_t path, int wdtype, const spark_geom* g, int rotary_dim, int32_t batch) {
+  if (path != SPARK_PATH_AUTO && path != SPARK_PATH_GEMV && path != SPARK_PATH_MMA)
+    return SPARK_ERR_INVALID_ARG;
+  if (path == SPARK_PATH_GEMV || (path == SPARK_PATH_AUTO && batch <= kGemvMaxBatch))
+    return SPARK_PATH_GEMV;
+  const bool ok = mma_projections_supported(wdtype, g->hidden, g->n_q, rotary_dim);
+  if (path == SPARK_PATH_MMA) return ok ? SPARK_PATH_MMA : SPARK_ERR_UNSUPPORTED;
+  return ok ? SPARK_PATH_MMA : SPARK_PATH_GEMV;
+}
+
+cudaError_t run_qkv(int path, const spark_geom* g, const float* h, const spark_layer_weights* w,
+                    const spark_kv_layer* kv, int rotary_dim, double theta, const int32_t* positions,
+                    int32_t batch, float* q_rot, float* g_logits, uint32_t* err, void* ws,
+                    const WsLayout& L, cudaStream_t st) {
+  if (path == SPARK_PATH_MMA)
+    return launch_qkv_mma(kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot, kv->k, kv->v, g_logits,
+                          err, g->hidden, g->n_q, g->n_kv, batch, kv->capacity, kv->ring_capacity,
+                          rotary_dim, theta, g->eps, positions, mma_ws(ws, L), st);
+  return launch_qkv_rope(w->dtype, kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot, kv->k, kv->v,
+                         g_logits, err, g->hidden, g->n_q, g->n_kv, batch, kv->capacity,
+                         kv->ring_capacity, rotary_dim, theta, g->eps, positions, st);
+}
+
+cudaError_t run_oproj(int path, const spark_geom* g, const float* a, const float* g_logits,
+                      const float* h, const spark_layer_weights* w, int32_t batch, float* out,
+                      uint32_t* err, void* ws, const WsLayout& L, cudaStream_t st) {
+  if (path == SPARK_PATH_MMA)
+    return launch_oproj_mma(a, g_logits, h, w->o_w, out, err, g->hidden, g->n_q, batch, mma_ws(ws, L), st);
+  return launch_oproj(w->dtype, a, g_logits, h, w->o_w, out, err, g->hidden, g->n_q, batch, st);
+}
 
 }  // namespace
 
@@ -80,22 +142,25 @@ int spark_attn_error_word(void* workspace, size_t workspace_bytes, uint32_t* wor
 
 int spark_dbg_qkv_rope(const spark_geom* g, const float* h, const spark_layer_weights* w,
                        const spark_kv_layer* kv, int32_t layer_class, const int32_t* positions,
-                       int32_t batch, float* q_rot, float* g_logits, void* stream) {
+                       int32_t batch, float* q_rot, float* g_logits, int32_t path, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   int s;
   if ((s = check_geom(g)) != SPARK_OK) return s;
   if ((s = check_weights(w, true, false)) != SPARK_OK) return s;
   if ((s = check_batch(batch)) != SPARK_OK) return s;
   if ((s = check_kv(g, kv, layer_class, positions, batch)) != SPARK_OK) return s;
+  if ((s = check_ws(g, batch, workspace, workspace_bytes)) != SPARK_OK) return s;
   if (!h || !q_rot || !g_logits || !aligned16(h) || !aligned16(q_rot) || !aligned16(g_logits))
     return SPARK_ERR_INVALID_ARG;
   int rotary_dim;
   double theta;
   rope_for(g, layer_class, &rotary_dim, &theta);
-  // no workspace here: the kernel's own bounds check has no error word to set
-  return cuda_status(launch_qkv_rope(w->dtype, kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot,
-                                     kv->k, kv->v, g_logits, nullptr, g->hidden, g->n_q, g->n_kv,
-                                     batch, kv->capacity, kv->ring_capacity, rotary_dim, theta,
-                                     g->eps, positions, (cudaStream_t)stream));
+  const int chosen = pick_path(path, w->dtype, g, rotary_dim, batch);
+  if (chosen < 0) return chosen;
+  const WsLayout L = ws_layout(g->hidden, g->n_q, g->n_kv, batch);
+  return cuda_status(run_qkv(chosen, g, h, w, kv, rotary_dim, theta, positions, batch, q_rot,
+                             g_logits, ws_at<uint32_t>(workspace, L.err), workspace, L,
+                             (cudaStream_t)stream));
 }
 
 int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_layer* kv,
@@ -118,16 +183,20 @@ int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_
 
 int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* g_logits,
                          const float* h, const spark_layer_weights* w, int32_t batch, float* out,
-                         void* stream) {
+                         int32_t path, void* workspace, size_t workspace_bytes, void* stream) {
   int s;
   if ((s = check_geom(g)) != SPARK_OK) return s;
   if ((s = check_weights(w, false, true)) != SPARK_OK) return s;
   if ((s = check_batch(batch)) != SPARK_OK) return s;
+  if ((s = check_ws(g, batch, workspace, workspace_bytes)) != SPARK_OK) return s;
   if (!a || !g_logits || !h || !out || !aligned16(a) || !aligned16(g_logits) || !aligned16(h) ||
       !aligned16(out))
     return SPARK_ERR_INVALID_ARG;
-  return cuda_status(launch_oproj(w->dtype, a, g_logits, h, w->o_w, out, nullptr, g->hidden, g->n_q,
-                                  batch, (cudaStream_t)stream));
+  const int chosen = pick_path(path, w->dtype, g, 0, batch);
+  if (chosen < 0) return chosen;
+  const WsLayout L = ws_layout(g->hidden, g->n_q, g->n_kv, batch);
+  return cuda_status(run_oproj(chosen, g, a, g_logits, h, w, batch, out,
+                               ws_at<uint32_t>(workspace, L.err), workspace, L, (cudaStream_t)stream));
 }
 
 int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_weights* w,
@@ -150,17 +219,16 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
   int rotary_dim;
   double theta;
   rope_for(g, layer_class, &rotary_dim, &theta);
-  cudaError_t e = launch_qkv_rope(w->dtype, kv->dtype, h, w->norm_w, w->qkv_w, w->g_w, q_rot,
-                                  kv->k, kv->v, g_logits, err, g->hidden, g->n_q, g->n_kv, batch,
-                                  kv->capacity, kv->ring_capacity, rotary_dim, theta, g->eps,
-                                  positions, st);
+  cudaError_t e = run_qkv(pick_path(SPARK_PATH_AUTO, w->dtype, g, rotary_dim, batch), g, h, w, kv,
+                          rotary_dim, theta, positions, batch, q_rot, g_logits, err, workspace, L, st);
   if (e == cudaSuccess)
     e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity,
                          kv->ring_capacity, layer_class == SPARK_FULL, g->window, g->scale,
                          positions, batch, a, ws_at<float>(workspace, L.part),
                          ws_at<uint32_t>(workspace, L.counters), err, 0, nullptr, 0, st);
   if (e == cudaSuccess)
-    e = launch_oproj(w->dtype, a, g_logits, h, w->o_w, out, err, g->hidden, g->n_q, batch, st);
+    e = run_oproj(pick_path(SPARK_PATH_AUTO, w->dtype, g, 0, batch), g, a, g_logits, h, w, batch, out,
+                  err, workspace, L, st);
   return cuda_status(e);
 }
 

@@ -20,6 +20,11 @@ constexpr int kGroup = 4;            // query heads per KV head
 constexpr int kMaxAttnCtas = 1024;   // partial-result slots reserved for CTAs
 constexpr int kPartFloats = 2 * kGroup + kGroup * kHeadDim;  // m[4], l[4], o[4][256]
 
+// tensor-core projections (mma.cu): sequences per launch, CTAs a launch may use
+constexpr int kMmaMaxSeq = 128;
+constexpr int kMmaMaxCtas = 256;
+constexpr int kMmaTileRows = 128;
+
 // every bounded wait in the kernels gives up after this long
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -77,6 +82,10 @@ struct WsLayout {
   size_t a = 0;         // f32 [batch][q_dim] attention output
   size_t hbuf = 0;      // f32 [2][batch][hidden] residual stream between layers
   size_t part = 0;      // f32 [kMaxAttnCtas + batch * n_kv][kPartFloats]
+  size_t mx = 0;        // bf16 [2][bpad][max(hidden, q_dim)] projection inputs (hi, lo); bpad as below
+  size_t mcs = 0;       // f32x2 [batch][head_dim / 2] rope (cos, sin) of each sequence
+  size_t mpart = 0;     // f32 [kMmaMaxCtas][kMmaTileRows][min(batch, kMmaMaxSeq) rounded to 8]
+  size_t mtick = 0;     // uint32 [kMmaMaxCtas] split-K tickets of the projection tiles
   size_t trace = 0;     // u64 [kTraceWords] phase timestamps of the persistent kernel (opt-in)
   size_t total = 0;
 };
@@ -102,6 +111,16 @@ inline WsLayout ws_layout(int hidden, int n_q, int n_kv, int batch) {
   off = align_up(off + sizeof(float) * 2 * (size_t)batch * hidden, 256);
   L.part = off;
   off = align_up(off + sizeof(float) * (size_t)(kMaxAttnCtas + (size_t)batch * n_kv) * kPartFloats, 256);
+  const size_t kmax = (size_t)(hidden > n_q * kHeadDim ? hidden : n_q * kHeadDim);
+  const size_t bpad = (size_t)((batch < kMmaMaxSeq ? batch : kMmaMaxSeq) + 7) / 8 * 8;
+  L.mx = off;
+  off = align_up(off + 2 * 2 * bpad * kmax, 256);
+  L.mcs = off;
+  off = align_up(off + sizeof(float) * (size_t)batch * kHeadDim, 256);
+  L.mpart = off;
+  off = align_up(off + sizeof(float) * (size_t)kMmaMaxCtas * kMmaTileRows * bpad, 256);
+  L.mtick = off;
+  off = align_up(off + sizeof(uint32_t) * kMmaMaxCtas, 256);
   L.trace = off;
   off = align_up(off + sizeof(uint64_t) * kTraceWords, 256);
   L.total = off;
@@ -201,6 +220,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// 2-D tiled TMA load global -> shared, completing on `bar` (byte count).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
 

@@ -26,7 +26,36 @@ cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, con
                              int n_ctas, const void* l2_prefetch, size_t l2_prefetch_bytes,
                              cudaStream_t st);
 
+// The two projections for a batch on the tensor cores (mma.cu): same results
+// as launch_qkv_rope / launch_oproj, for bf16 weights.
+struct MmaWorkspace {
+  __nv_bfloat16* x;    // [2][bpad][max(hidden, q_dim)] activation rows (hi, lo)
+  float2* cs;          // [batch][head_dim / 2] rope (cos, sin)
+  float* part;         // split-K partial results
+  uint32_t* tickets;   // [kMmaMaxCtas] split-K tickets, zero between launches
+  uint64_t* trace;     // [kTraceWords] opt-in phase stamps
+};
+
+bool mma_projections_supported(int wdtype, int hidden, int n_q, int rotary_dim);
+
+cudaError_t launch_qkv_mma(int cdtype, const float* h, const void* norm_w, const void* qkv_w,
+                           const void* g_w, float* q_rot, void* kc, void* vc, float* g_out,
+                           uint32_t* err, int hidden, int n_q, int n_kv, int batch, int64_t capacity,
+                           int ring_capacity, int rotary_dim, double theta, float eps,
+                           const int32_t* positions, const MmaWorkspace& ws, cudaStream_t st);
+
+cudaError_t launch_oproj_mma(const float* a, const float* g, const float* h, const void* o_w,
+                             float* out, uint32_t* err, int hidden, int n_q, int batch,
+                             const MmaWorkspace& ws, cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// cuTensorMapEncodeTiled from the driver (null if the driver has none).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 }  // namespace spark

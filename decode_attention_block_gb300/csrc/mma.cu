@@ -1,0 +1,831 @@
+// mma.cu -- the block's two projections for a batch of sequences, on the
+// tensor cores (tcgen05 MMA with its accumulator in tensor memory, operands
+// staged in shared memory by TMA):
+//
+//  * qkv: input RMSNorm, q_k_v_proj and g_proj of every sequence, with the
+//    split into q / k / v, the per-class NeoX rope and the cache-row write
+//    fused into the epilogue (turbospark-runtime 0.3.0,
+//    src/families/spark/attn.rs, encode_attention_block: the fused
+//    projection, the gate's projection of the same normed x, encode_split_qkv
+//    with k and v landing in their slots, encode_rope_neox_subdim on q and k);
+//  * o: the headwise sigmoid gate, o_proj and the raw residual add (attn.rs,
+//    encode_sigmoid_head_gate_mul before the o_proj GEMV; mod.rs, the layer
+//    loop's residual add).
+//
+// With B sequences a projection is the GEMM out[r][b] = sum_c W[r][c] x_b[c].
+// The weight rows are the MMA's M side (128 rows a tile, bf16 straight from
+// HBM), the sequences its N side, so the weights -- the bytes that bound the
+// step -- are read once for the whole batch.  The MMA takes both operands in
+// one 16-bit type, so each fp32 activation is split into two bf16 numbers,
+// x = hi + lo with lo = bf16(x - hi): the B side holds [hi_0..hi_{B-1},
+// lo_0..lo_{B-1}] (N = 2 * B rounded up to 8) and the epilogue adds the two
+// halves of each sequence.  hi + lo keeps 16 significant bits of x, so the
+// result is as close to the fp32 GEMV's as rounding order allows, while the
+// HBM traffic is that of the bf16 weights alone.
+//
+// One kernel launch per projection and chunk of up to 128 sequences:
+//   k_prep_norm / k_prep_gate  build the activations' (hi, lo) rows and, for
+//                              qkv, each sequence's rope (cos, sin) table;
+//   k_proj_mma                 the GEMM.  Tiles of 128 weight rows are cut
+//                              along K into `splits` pieces (1..8) so that
+//                              every SM streams weights; each piece leaves its
+//                              fp32 partial result in the workspace and the
+//                              last CTA of a tile (an atomic ticket) adds them
+//                              in split order and runs the epilogue.
+//
+// Warp roles in k_proj_mma (192 threads): warp 0 issues the TMA loads (one
+// elected lane), warp 1 owns the tensor-memory columns and issues the MMAs
+// (one elected lane), warps 2-5 read the accumulator back (warp w reads TMEM
+// lanes 32 * (w % 4) .. +31, the quarter a warp may access) and run the
+// epilogue.  With SPARK_TRACE_MMA set in the environment each CTA stamps its
+// phases (%globaltimer) into the workspace's trace region.  Every wait is
+// bounded (kWaitLimitNs): on time-out the kernel
+// raises the error word, stops issuing, lets its copies in flight land and
+// frees its tensor memory before it returns.
+#include <math.h>
+#include <stdlib.h>
+
+#include "checks.h"
+#include "launch.h"
+
+namespace spark {
+namespace {
+
+constexpr int kMmaThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kKBlock = 64;                                   // K elements per stage = one 128 B row
+constexpr uint32_t kRowBytes = kKBlock * 2;                   // bf16
+constexpr uint32_t kABytes = kMmaTileRows * kRowBytes;        // 16 KB: a tile's rows for one stage
+constexpr int kBoxRows = 64;                                  // weight rows per TMA box
+constexpr int kMaxStages = 16;
+constexpr int kBarEpi = 1;                                    // named barrier of the epilogue warps
+constexpr size_t kMaxDynSmem = 232448;                        // 227 KB per block on sm_100 parts
+constexpr size_t kStageBudget = kMaxDynSmem - 2048;           // static smem + alignment slack
+constexpr int kPrepThreads = 256;
+constexpr int kMaxPairs = kHeadDim / 2;
+
+// ---------------------------------------------------------------------------
+// tcgen05 helpers (inline PTX)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, M x N x 16, bf16 in, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Two 8-column reads of this warp's 32 TMEM lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld_8x2(uint32_t ta, uint32_t tb, float (&a)[8], float (&b)[8]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[8 + i]);
+  }
+}
+
+// Shared-memory matrix descriptor of a K-major operand written by TMA with
+// the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+// Bits: start address >> 4 [0,14), leading byte offset >> 4 [16,30) (unused
+// by swizzled K-major layouts), stride byte offset >> 4 [32,46), descriptor
+// version 1 [46,48), swizzle mode [61,64) (2 = 128-byte).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator [4,6) = 1, A and B
+// bf16 [7,10) = [10,13) = 1, both K-major (bits 15, 16 = 0), N >> 3 at
+// [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+template <typename CT>
+__device__ __forceinline__ CT to_cache(float v);
+template <>
+__device__ __forceinline__ float to_cache<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_cache<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// x -> (hi, lo) in bf16 with x ~= hi + lo
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(x);
+  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+__device__ __forceinline__ void store_split4(__nv_bfloat16* xh, __nv_bfloat16* xl, int i, float4 v) {
+  __nv_bfloat16 h[4], l[4];
+  split_bf16(v.x, h[0], l[0]);
+  split_bf16(v.y, h[1], l[1]);
+  split_bf16(v.z, h[2], l[2]);
+  split_bf16(v.w, h[3], l[3]);
+  *reinterpret_cast<uint2*>(xh + i) = *reinterpret_cast<const uint2*>(h);
+  *reinterpret_cast<uint2*>(xl + i) = *reinterpret_cast<const uint2*>(l);
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPrepThreads / 32; ++i) t += red[i];
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// activation prologues
+// ---------------------------------------------------------------------------
+struct PrepArgs {
+  double inv_freq[kMaxPairs];  // theta^(-2i/r) for i < r/2, in double (host)
+  int32_t pos[kMmaMaxSeq];
+};
+
+// One CTA per (padded) sequence: x = RMSNorm(h_b) * w ("plain w", eps inside
+// the root) split into the rows hi[b] and lo[b] of `x` ([2][bpad][hidden]);
+// padded sequences get zero rows.  Also the rope table of sequence b:
+// cs[b][i] = (cos, sin) of pos_b * theta^(-2i/r), the angle formed and
+// reduced modulo 2 pi in double (at position 131072 an fp32 angle would be
+// off by ~1e-2 rad), then evaluated in fp32.
+__global__ void __launch_bounds__(kPrepThreads)
+k_prep_norm(const float* __restrict__ h, const __nv_bfloat16* __restrict__ norm_w,
+            __nv_bfloat16* __restrict__ x, float2* __restrict__ cs, int hidden, int nb, int bpad,
+            float eps, int rotary_dim, const __grid_constant__ PrepArgs args) {
+  __shared__ float red[kPrepThreads / 32];
+  const int b = blockIdx.x;
+  __nv_bfloat16* xh = x + (size_t)b * hidden;
+  __nv_bfloat16* xl = x + (size_t)(bpad + b) * hidden;
+  pdl_wait();
+  pdl_trigger();
+  if (b >= nb) {
+    for (int i = 4 * threadIdx.x; i < hidden; i += 4 * kPrepThreads) {
+      *reinterpret_cast<uint2*>(xh + i) = make_uint2(0u, 0u);
+      *reinterpret_cast<uint2*>(xl + i) = make_uint2(0u, 0u);
+    }
+    return;
+  }
+  if (threadIdx.x < rotary_dim / 2) {
+    const int i = threadIdx.x;
+    const double ang = (double)args.pos[b] * args.inv_freq[i];
+    const double two_pi = 6.283185307179586476925;
+    const double k = rint(ang / two_pi);
+    const float r = (float)fma(-k, two_pi, ang);
+    float s, c;
+    sincosf(r, &s, &c);
+    cs[(size_t)b * kMaxPairs + i] = make_float2(c, s);
+  }
+  const float* hb = h + (size_t)b * hidden;
+  float ss = 0.f;
+  for (int i = 4 * threadIdx.x; i < hidden; i += 4 * kPrepThreads) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(hb + i));
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
+  const float inv = 1.0f / sqrtf(block_sum(ss, red) / (float)hidden + eps);
+  for (int i = 4 * threadIdx.x; i < hidden; i += 4 * kPrepThreads) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(hb + i));
+    const uint2 wr = __ldg(reinterpret_cast<const uint2*>(norm_w + i));
+    const float2 w01 = bf16x2_to_f32x2(wr.x), w23 = bf16x2_to_f32x2(wr.y);
+    store_split4(xh, xl, i,
+                 make_float4(v.x * w01.x * inv, v.y * w01.y * inv, v.z * w23.x * inv, v.w * w23.y * inv));
+  }
+}
+
+// One CTA per (padded) sequence: the gated attention output a_b * sigmoid(g_b)
+// (one gate per query head, broadcast over head_dim) split into hi / lo rows.
+__global__ void __launch_bounds__(kPrepThreads)
+k_prep_gate(const float* __restrict__ a, const float* __restrict__ g, __nv_bfloat16* __restrict__ x,
+            int q_dim, int n_q, int nb, int bpad) {
+  const int b = blockIdx.x;
+  __nv_bfloat16* xh = x + (size_t)b * q_dim;
+  __nv_bfloat16* xl = x + (size_t)(bpad + b) * q_dim;
+  pdl_wait();
+  pdl_trigger();
+  if (b >= nb) {
+    for (int i = 4 * threadIdx.x; i < q_dim; i += 4 * kPrepThreads) {
+      *reinterpret_cast<uint2*>(xh + i) = make_uint2(0u, 0u);
+      *reinterpret_cast<uint2*>(xl + i) = make_uint2(0u, 0u);
+    }
+    return;
+  }
+  const float* ab = a + (size_t)b * q_dim;
+  for (int i = 4 * threadIdx.x; i < q_dim; i += 4 * kPrepThreads) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(ab + i));
+    const float s = 1.0f / (1.0f + expf(-__ldcg(g + (size_t)b * n_q + i / kHeadDim)));
+    store_split4(xh, xl, i, make_float4(v.x * s, v.y * s, v.z * s, v.w * s));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the GEMM
+// ---------------------------------------------------------------------------
+enum { kEpiQkv = 0, kEpiO = 1 };
+
+struct MmaParams {
+  int n_main_tiles;   // tiles over the main weight (the g tile follows them)
+  int splits;         // K pieces per tile
+  int kblocks;        // K / 64
+  int bpad;           // sequences of this chunk rounded up to 8 (N = 2 * bpad)
+  int nb;             // sequences of this chunk
+  int stages;         // pipeline depth
+  int tmem_cols;      // allocated accumulator columns (power of two >= 2 * bpad)
+  int split_halves;   // qkv: a tile pairs head dims d and d + 128 (rotary_dim 256)
+  int g_rows;         // rows of the g tile (qkv), 0 for o
+  uint32_t stage_bytes;
+  // qkv epilogue
+  float* q_rot;
+  void* kc;
+  void* vc;
+  float* g_out;
+  const float2* cs;
+  int n_q, n_kv, rotary_dim;
+  int64_t capacity;
+  // o epilogue
+  const float* h;
+  float* out;
+  int hidden;
+  // split-K and errors
+  float* part;
+  uint32_t* tickets;
+  uint32_t* err;
+  uint64_t* trace;  // [grid][kTraceEvents] %globaltimer stamps, or null (opt-in)
+};
+
+// Stamps of the opt-in timeline (SPARK_TRACE_MMA): per CTA, in this order.
+enum { kTrStart, kTrXIssued, kTrFirstFull, kTrLastFull, kTrDone, kTrTicket, kTrReduced, kTrEnd,
+       kTraceEvents };
+
+__device__ __forceinline__ void stamp(const MmaParams& p, int ev) {
+  if (p.trace) p.trace[(size_t)blockIdx.x * kTraceEvents + ev] = global_timer_ns();
+}
+
+struct MmaSeq {
+  int32_t slot[kMmaMaxSeq];  // cache row each sequence writes (qkv)
+};
+
+constexpr int kMaxSplits = 8;
+constexpr int kUnroll = 4;  // float4 elements per thread whose loads are all in flight together
+
+// Y[b][m] = sum of part[s][b][m] over the splits, added in split order.  A
+// thread owns float4 column m4 of rows b = b_first + 4k; every split of
+// kUnroll elements is loaded before anything is added, so the loads overlap
+// instead of paying the L2 latency one by one.
+__device__ __forceinline__ void reduce_parts(float* Y, const float* base, int splits, int bpad, int et) {
+  const int m4 = et & 31, b_first = et >> 5;
+  const int nel = bpad >> 2;
+  for (int k0 = 0; k0 < nel; k0 += kUnroll) {
+    float4 v[kMaxSplits][kUnroll];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (s < splits && k0 + u < nel)
+          v[s][u] = __ldcg(reinterpret_cast<const float4*>(
+                               base + ((size_t)s * bpad + b_first + 4 * (k0 + u)) * kMmaTileRows) + m4);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (k0 + u < nel) {
+        float4 acc = v[0][u];
+#pragma unroll
+        for (int s = 1; s < kMaxSplits; ++s) {
+          if (s < splits) {
+            acc.x += v[s][u].x;
+            acc.y += v[s][u].y;
+            acc.z += v[s][u].z;
+            acc.w += v[s][u].w;
+          }
+        }
+        *reinterpret_cast<float4*>(Y + (size_t)(b_first + 4 * (k0 + u)) * kMmaTileRows + 4 * m4) = acc;
+      }
+    }
+  }
+  named_bar_sync(kBarEpi, kEpiThreads);
+}
+
+// out[b][R] = h[b][R] + the sum of the splits (in split order), float4 per thread.
+__device__ __forceinline__ void epilogue_o(const MmaParams& p, int tile, const float* base, int et) {
+  const int m4 = et & 31, b_first = et >> 5;
+  const int R = kMmaTileRows * tile + 4 * m4;
+  if (R >= p.hidden) return;  // hidden % 64 == 0: a float4 is wholly inside or outside
+  const int nel = (p.nb + 3 - b_first) / 4;
+  for (int k0 = 0; k0 < nel; k0 += kUnroll) {
+    float4 v[kMaxSplits][kUnroll], hv[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int b = b_first + 4 * (k0 + u);
+      if (k0 + u < nel) {
+        hv[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)b * p.hidden + R));
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s)
+          if (s < p.splits)
+            v[s][u] = __ldcg(reinterpret_cast<const float4*>(base + ((size_t)s * p.bpad + b) * kMmaTileRows) + m4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (k0 + u < nel) {
+        const int b = b_first + 4 * (k0 + u);
+        float4 acc = v[0][u];
+#pragma unroll
+        for (int s = 1; s < kMaxSplits; ++s) {
+          if (s < p.splits) {
+            acc.x += v[s][u].x;
+            acc.y += v[s][u].y;
+            acc.z += v[s][u].z;
+            acc.w += v[s][u].w;
+          }
+        }
+        *reinterpret_cast<float4*>(p.out + (size_t)b * p.hidden + R) =
+            make_float4(hv[u].x + acc.x, hv[u].y + acc.y, hv[u].z + acc.z, hv[u].w + acc.w);
+      }
+    }
+  }
+}
+
+// q / k / v / g of one tile from Y ([bpad][128] fp32, the reduced GEMM):
+// rope on the q and k dims below the rotary dim (the pair partner is another
+// row of the same tile), q to q_rot, k and v to their cache rows, g to g_out.
+// The rope (cos, sin) of the tile's 64 pairs for every sequence are first
+// copied to CS ([bpad][64] float2) with all loads in flight together.
+template <typename CT>
+__device__ __forceinline__ void epilogue_qkv(const MmaParams& p, const MmaSeq& seq, int tile, bool g_tile,
+                                             const float* Y, float2* CS, int m, int et) {
+  if (g_tile) {
+    if (m < p.g_rows)
+      for (int b = 0; b < p.nb; ++b) p.g_out[(size_t)b * p.n_q + m] = Y[b * kMmaTileRows + m];
+    return;
+  }
+  const int unit = tile >> 1, sel = tile & 1;
+  const bool halves = p.split_halves != 0;
+  const bool has_rot = unit < p.n_q + p.n_kv && (halves || sel == 0);
+  const int p0 = halves ? kBoxRows * sel : 0;  // first rope pair of the tile
+  if (has_rot) {
+    const int c4 = et & 31, b_first = et >> 5;  // float4 = two pairs
+    const int nel = (p.nb + 3 - b_first) / 4;
+    for (int k0 = 0; k0 < nel; k0 += 2 * kUnroll) {
+      float4 v[2 * kUnroll];
+#pragma unroll
+      for (int u = 0; u < 2 * kUnroll; ++u)
+        if (k0 + u < nel)
+          v[u] = __ldcg(reinterpret_cast<const float4*>(p.cs + (size_t)(b_first + 4 * (k0 + u)) * kMaxPairs + p0) + c4);
+#pragma unroll
+      for (int u = 0; u < 2 * kUnroll; ++u)
+        if (k0 + u < nel) reinterpret_cast<float4*>(CS + (size_t)(b_first + 4 * (k0 + u)) * kBoxRows)[c4] = v[u];
+    }
+  }
+  named_bar_sync(kBarEpi, kEpiThreads);
+  int d;  // dim within the 256-row head this tile row belongs to
+  if (halves)
+    d = m < kBoxRows ? kBoxRows * sel + m : 2 * kBoxRows + kBoxRows * sel + (m - kBoxRows);
+  else
+    d = kMmaTileRows * sel + m;
+  const int R = kHeadDim * unit + d;
+  const int q_dim = p.n_q * kHeadDim;
+  int kind, head;
+  if (unit < p.n_q) {
+    kind = 0;
+    head = unit;
+  } else if (unit < p.n_q + p.n_kv) {
+    kind = 1;
+    head = unit - p.n_q;
+  } else {
+    kind = 2;
+    head = unit - p.n_q - p.n_kv;
+  }
+  const int hr = p.rotary_dim >> 1;
+  const bool rot = kind != 2 && d < p.rotary_dim;
+  int mp = m, pair = 0;
+  float sgn = 0.f;
+  if (rot) {
+    if (d < hr) {
+      pair = d;
+      sgn = -1.f;
+      mp = halves ? m + kBoxRows : m + hr;
+    } else {
+      pair = d - hr;
+      sgn = 1.f;
+      mp = halves ? m - kBoxRows : m - hr;
+    }
+  }
+  const int pl = pair - p0;  // pair within the staged table
+  CT* cache = static_cast<CT*>(kind == 1 ? p.kc : p.vc);
+  for (int b = 0; b < p.nb; ++b) {
+    float v = Y[b * kMmaTileRows + m];
+    if (rot) {
+      const float2 c = CS[b * kBoxRows + pl];
+      v = fmaf(sgn * Y[b * kMmaTileRows + mp], c.y, v * c.x);
+    }
+    if (kind == 0)
+      p.q_rot[(size_t)b * q_dim + R] = v;
+    else
+      cache[(((size_t)b * p.capacity + seq.slot[b]) * p.n_kv + head) * kHeadDim + d] = to_cache<CT>(v);
+  }
+}
+
+template <int E, typename CT>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_g,
+           const __grid_constant__ CUtensorMap tm_x, const MmaParams p,
+           const __grid_constant__ MmaSeq seq) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag, last_flag, no_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / p.splits;
+  const int split = blockIdx.x - tile * p.splits;
+  const int kb0 = split * p.kblocks / p.splits;
+  const int nk = (split + 1) * p.kblocks / p.splits - kb0;
+  const bool g_tile = E == kEpiQkv && tile >= p.n_main_tiles;
+  const uint32_t x_bytes = (uint32_t)p.bpad * 2u * kRowBytes;
+  const uint32_t a_bytes = g_tile ? (uint32_t)p.g_rows * kRowBytes : kABytes;
+  volatile int* abort_v = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&done_bar, 1);
+    abort_flag = 0;
+    last_flag = 0;
+    no_abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tm_w);
+    prefetch_tensormap(&tm_x);
+    if (g_tile) prefetch_tensormap(&tm_g);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (threadIdx.x == 0) stamp(p, kTrStart);
+
+  if (warp == 0) {
+    // ---- producer: weights first (they do not depend on earlier kernels),
+    // then the activations once the kernels before this one are done
+    if (lane == 0) {
+      int r0, r1;
+      if (E == kEpiQkv && p.split_halves) {
+        r0 = 2 * kMmaTileRows * (tile >> 1) + kBoxRows * (tile & 1);
+        r1 = r0 + 2 * kBoxRows;
+      } else {
+        r0 = kMmaTileRows * tile;
+        r1 = r0 + kBoxRows;
+      }
+      auto stage = [&](int s) { return smem + (size_t)s * p.stage_bytes; };
+      auto load_w = [&](int s, int kb) {
+        if (g_tile) {
+          tma_load_2d(stage(s), &tm_g, &full_bar[s], kb * kKBlock, 0);
+        } else {
+          tma_load_2d(stage(s), &tm_w, &full_bar[s], kb * kKBlock, r0);
+          tma_load_2d(stage(s) + kABytes / 2, &tm_w, &full_bar[s], kb * kKBlock, r1);
+        }
+      };
+      const int pre = nk < p.stages ? nk : p.stages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full_bar[i], a_bytes + x_bytes);
+        load_w(i, kb0 + i);
+      }
+      pdl_wait();
+      pdl_trigger();
+      fence_proxy_async_global();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(stage(i) + kABytes, &tm_x, &full_bar[i], (kb0 + i) * kKBlock, 0);
+      stamp(p, kTrXIssued);
+      int issued = pre;
+      for (int i = pre; i < nk; ++i) {
+        const int s = i % p.stages;
+        if (!mbar_wait_bounded(&empty_bar[s], ((i / p.stages) - 1) & 1, abort_v, kWaitLimitNs)) {
+          raise_error(p.err, kErrWaitTimeout);
+          *abort_v = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], a_bytes + x_bytes);
+        load_w(s, kb0 + i);
+        tma_load_2d(stage(s) + kABytes, &tm_x, &full_bar[s], (kb0 + i) * kKBlock, 0);
+        issued = i + 1;
+      }
+      if (*abort_v) {
+        // let the copies still in flight land before the CTA can exit
+        for (int i = issued > p.stages ? issued - p.stages : 0; i < issued; ++i)
+          mbar_wait_bounded(&full_bar[i % p.stages], (i / p.stages) & 1, &no_abort, kWaitLimitNs);
+      }
+    } else {
+      pdl_wait();
+      pdl_trigger();
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer: 4 MMAs of K = 16 per stage, then free the stage
+    pdl_wait();
+    pdl_trigger();
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kMmaTileRows, 2 * p.bpad);
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % p.stages;
+        if (!mbar_wait_bounded(&full_bar[s], (i / p.stages) & 1, abort_v, kWaitLimitNs)) {
+          raise_error(p.err, kErrWaitTimeout);
+          *abort_v = 1;
+          break;
+        }
+        tc_fence_after();
+        if (i == 0) stamp(p, kTrFirstFull);
+        if (i == nk - 1) stamp(p, kTrLastFull);
+        const uint32_t a_addr = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const uint64_t da = sw128_desc(a_addr), dx = sw128_desc(a_addr + kABytes);
+#pragma unroll
+        for (int k = 0; k < kKBlock / 16; ++k)
+          mma_bf16(tmem, da + 2u * k, dx + 2u * k, idesc, (i | k) != 0 ? 1u : 0u);
+        mma_commit(&empty_bar[s]);
+      }
+      mma_commit(&done_bar);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue warps
+    pdl_wait();
+    pdl_trigger();
+    const int quad = warp & 3;
+    const int m = quad * 32 + lane;  // tile row (TMEM lane) of this thread
+    const int et = threadIdx.x - 64;
+    bool ok = mbar_wait_bounded(&done_bar, 0, abort_v, kWaitLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) {
+      raise_error(p.err, kErrWaitTimeout);
+      *abort_v = 1;
+    }
+    tc_fence_after();
+    if (et == 0) stamp(p, kTrDone);
+    float* Y = reinterpret_cast<float*>(smem);  // [bpad][128] fp32, over the drained stages
+    float* P = p.part + (size_t)blockIdx.x * kMmaTileRows * p.bpad;
+    if (ok) {
+      const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+      for (int j = 0; j < p.bpad; j += 8) {
+        float hi[8], lo[8];
+        tmem_ld_8x2(trow + (uint32_t)j, trow + (uint32_t)(p.bpad + j), hi, lo);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) P[(j + c) * kMmaTileRows + m] = hi[c] + lo[c];
+      }
+    }
+    // the last CTA of the tile to finish (a ticket) adds the pieces
+    const float* parts = p.part + (size_t)tile * p.splits * kMmaTileRows * p.bpad;
+    __threadfence();
+    named_bar_sync(kBarEpi, kEpiThreads);
+    if (et == 0) {
+      const uint32_t t = atomicAdd(&p.tickets[tile], 1u);
+      const int last = t == (uint32_t)(p.splits - 1);
+      if (last) p.tickets[tile] = 0u;  // every piece has arrived: ready for the next launch
+      last_flag = last;
+      stamp(p, kTrTicket);
+    }
+    named_bar_sync(kBarEpi, kEpiThreads);
+    if (last_flag != 0) {
+      __threadfence();
+      if (E == kEpiQkv) {
+        reduce_parts(Y, parts, p.splits, p.bpad, et);
+        if (et == 0) stamp(p, kTrReduced);
+        epilogue_qkv<CT>(p, seq, tile, g_tile, Y, reinterpret_cast<float2*>(Y + p.bpad * kMmaTileRows), m, et);
+      } else {
+        epilogue_o(p, tile, parts, et);
+      }
+      if (p.trace) {
+        named_bar_sync(kBarEpi, kEpiThreads);
+        if (et == 0) stamp(p, kTrEnd);
+      }
+    }
+  }
+  // every tensor-memory read is done before the owner frees the columns
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+// [rows][cols] bf16 row-major matrix as a 2-D tensor map: boxes of 64
+// columns (128 bytes) x box_rows rows, 128-byte swizzle; rows past the end
+// read as zero.
+bool make_bf16_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kKBlock, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int splits, grid, stages, tmem_cols;
+  uint32_t stage_bytes;
+  size_t smem;
+};
+
+// Split K so that the tiles cover the SMs once; as many stages as fit.
+Plan plan_for(int tiles, int kblocks, int bpad) {
+  Plan P;
+  int s = device_sm_count() / tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s > kblocks) s = kblocks;
+  if (s * tiles > kMmaMaxCtas) s = kMmaMaxCtas / tiles;
+  if (s < 1) s = 1;
+  P.splits = s;
+  P.grid = tiles * s;
+  P.stage_bytes = kABytes + (uint32_t)bpad * 2u * kRowBytes;
+  const int nk_max = (kblocks + s - 1) / s;
+  int st = (int)(kStageBudget / P.stage_bytes);
+  if (st > nk_max) st = nk_max;
+  if (st > kMaxStages) st = kMaxStages;
+  if (st < 1) st = 1;
+  P.stages = st;
+  size_t body = (size_t)st * P.stage_bytes;
+  // after the pipeline drains: Y [bpad][128] fp32 and the rope table [bpad][64] float2
+  const size_t y = (sizeof(float) * kMmaTileRows + sizeof(float2) * kBoxRows) * (size_t)bpad;
+  if (y > body) body = y;
+  P.smem = body + 1024;
+  P.tmem_cols = 32;
+  while (P.tmem_cols < 2 * bpad) P.tmem_cols *= 2;
+  return P;
+}
+
+template <int E, typename CT>
+cudaError_t launch_gemm(const CUtensorMap& tw, const CUtensorMap& tg, const CUtensorMap& tx,
+                        MmaParams p, const MmaSeq& seq, int tiles, cudaStream_t st) {
+  const Plan P = plan_for(tiles, p.kblocks, p.bpad);
+  if (P.smem > kMaxDynSmem) return cudaErrorInvalidValue;
+  p.splits = P.splits;
+  p.stages = P.stages;
+  p.stage_bytes = P.stage_bytes;
+  p.tmem_cols = P.tmem_cols;
+  static const bool tracing = getenv("SPARK_TRACE_MMA") != nullptr;
+  if (!tracing || (size_t)P.grid * kTraceEvents > (size_t)kTraceWords) p.trace = nullptr;
+  auto kern = k_proj_mma<E, CT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(P.grid), dim3(kMmaThreads), P.smem, st, tw, tg, tx, p, seq);
+}
+
+}  // namespace
+
+bool mma_projections_supported(int wdtype, int hidden, int n_q, int rotary_dim) {
+  return wdtype == SPARK_BF16 && hidden % kKBlock == 0 && n_q <= kMmaTileRows &&
+         (rotary_dim <= kMmaTileRows || rotary_dim == kHeadDim) && tensor_map_encoder() != nullptr;
+}
+
+cudaError_t launch_qkv_mma(int cdtype, const float* h, const void* norm_w, const void* qkv_w,
+                           const void* g_w, float* q_rot, void* kc, void* vc, float* g_out,
+                           uint32_t* err, int hidden, int n_q, int n_kv, int batch, int64_t capacity,
+                           int ring_capacity, int rotary_dim, double theta, float eps,
+                           const int32_t* positions, const MmaWorkspace& ws, cudaStream_t st) {
+  const int q_dim = n_q * kHeadDim;
+  const int rows = (n_q + 2 * n_kv) * kHeadDim;
+  CUtensorMap tw, tg;
+  if (!make_bf16_map(&tw, qkv_w, hidden, rows, kBoxRows) || !make_bf16_map(&tg, g_w, hidden, n_q, n_q))
+    return cudaErrorInvalidValue;
+  PrepArgs pa;
+  for (int i = 0; i < kMaxPairs; ++i)
+    pa.inv_freq[i] = i < rotary_dim / 2 ? pow(theta, -2.0 * i / (double)rotary_dim) : 0.0;
+  const size_t ce = cdtype == SPARK_BF16 ? 2 : 4;
+  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
+    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
+    const int bpad = (nb + 7) / 8 * 8;
+    MmaSeq seq;
+    for (int b = 0; b < kMmaMaxSeq; ++b) {
+      pa.pos[b] = b < nb ? positions[b0 + b] : 0;
+      seq.slot[b] = b < nb ? (int32_t)write_slot_of(positions[b0 + b], ring_capacity) : 0;
+    }
+    float2* cs = ws.cs + (size_t)b0 * kMaxPairs;
+    cudaError_t e = launch_pdl(k_prep_norm, dim3(bpad), dim3(kPrepThreads), 0, st,
+                               h + (size_t)b0 * hidden, static_cast<const __nv_bfloat16*>(norm_w), ws.x,
+                               cs, hidden, nb, bpad, eps, rotary_dim, pa);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tx;
+    if (!make_bf16_map(&tx, ws.x, hidden, 2 * bpad, 2 * bpad)) return cudaErrorInvalidValue;
+    MmaParams p = {};
+    p.n_main_tiles = rows / kMmaTileRows;
+    p.kblocks = hidden / kKBlock;
+    p.bpad = bpad;
+    p.nb = nb;
+    p.split_halves = rotary_dim == kHeadDim ? 1 : 0;
+    p.g_rows = n_q;
+    p.q_rot = q_rot + (size_t)b0 * q_dim;
+    const size_t coff = (size_t)b0 * capacity * n_kv * kHeadDim * ce;
+    p.kc = static_cast<unsigned char*>(kc) + coff;
+    p.vc = static_cast<unsigned char*>(vc) + coff;
+    p.g_out = g_out + (size_t)b0 * n_q;
+    p.cs = cs;
+    p.n_q = n_q;
+    p.n_kv = n_kv;
+    p.rotary_dim = rotary_dim;
+    p.capacity = capacity;
+    p.hidden = hidden;
+    p.part = ws.part;
+    p.tickets = ws.tickets;
+    p.err = err;
+    p.trace = ws.trace;
+    const int tiles = p.n_main_tiles + 1;
+    e = cdtype == SPARK_BF16 ? launch_gemm<kEpiQkv, __nv_bfloat16>(tw, tg, tx, p, seq, tiles, st)
+                             : launch_gemm<kEpiQkv, float>(tw, tg, tx, p, seq, tiles, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_oproj_mma(const float* a, const float* g, const float* h, const void* o_w,
+                             float* out, uint32_t* err, int hidden, int n_q, int batch,
+                             const MmaWorkspace& ws, cudaStream_t st) {
+  const int q_dim = n_q * kHeadDim;
+  CUtensorMap tw;
+  if (!make_bf16_map(&tw, o_w, q_dim, hidden, kBoxRows)) return cudaErrorInvalidValue;
+  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
+    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
+    const int bpad = (nb + 7) / 8 * 8;
+    cudaError_t e = launch_pdl(k_prep_gate, dim3(bpad), dim3(kPrepThreads), 0, st, a + (size_t)b0 * q_dim,
+                               g + (size_t)b0 * n_q, ws.x, q_dim, n_q, nb, bpad);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tx;
+    if (!make_bf16_map(&tx, ws.x, q_dim, 2 * bpad, 2 * bpad)) return cudaErrorInvalidValue;
+    MmaParams p = {};
+    p.n_main_tiles = (hidden + kMmaTileRows - 1) / kMmaTileRows;
+    p.kblocks = q_dim / kKBlock;
+    p.bpad = bpad;
+    p.nb = nb;
+    p.h = h + (size_t)b0 * hidden;
+    p.out = out + (size_t)b0 * hidden;
+    p.hidden = hidden;
+    p.part = ws.part;
+    p.tickets = ws.tickets;
+    p.err = err;
+    p.trace = ws.trace;
+    MmaSeq seq = {};
+    e = launch_gemm<kEpiO, float>(tw, tw, tx, p, seq, p.n_main_tiles, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace spark

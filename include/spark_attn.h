@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define SPARK_ATTN_ABI_VERSION 1
+#define SPARK_ATTN_ABI_VERSION 2
 /* largest batch one call accepts */
 #define SPARK_MAX_BATCH 1024
 
@@ -141,6 +141,7 @@ int spark_attn_error_word(void* workspace, size_t workspace_bytes, uint32_t* wor
  * (attn.rs, encode_attention_block, plus the input RMSNorm and the raw
  * residual add of mod.rs's layer loop).
  *   h          [batch][hidden] fp32 device: residual stream in.
+ *   (the projections take SPARK_PATH_AUTO's kernels, see below)
  *   w          the layer's weights.
  *   kv         the layer's cache; row slot(positions[b]) of K and V of each
  *              sequence b is overwritten with the token's rope'd k and its v,
@@ -176,7 +177,19 @@ int spark_attn_decode_stack(const spark_geom* g, const float* h, int32_t n_layer
                             int32_t batch, float* out, void* workspace,
                             size_t workspace_bytes, void* stream);
 
-/* ---- the block's stages, one kernel each (same conventions) ------------- */
+/* ---- the block's stages (same conventions) ------------------------------ */
+
+/* Which kernels compute the two projections (the `path` argument below).
+ * AUTO picks what spark_attn_decode runs: for batch <= 4, or fp32 weights,
+ * the GEMV kernels, which read each weight once for up to 4 sequences; for
+ * larger batches with bf16 weights, a GEMM on the tensor cores (tcgen05,
+ * tensor-memory accumulator) that reads each weight once for up to 128
+ * sequences, its fp32 activations carried as two bf16 halves (x = hi + lo).
+ * GEMV and MMA force one; MMA needs bf16 weights, hidden % 64 == 0 and, for
+ * q_k_v_proj, a rotary dim <= 128 or == head_dim (else UNSUPPORTED). */
+#define SPARK_PATH_AUTO 0
+#define SPARK_PATH_GEMV 1
+#define SPARK_PATH_MMA 2
 
 /* Input RMSNorm + q_k_v_proj + g_proj + split + per-class NeoX rope + the
  * cache-row write (attn.rs, encode_attention_block: the fused projection,
@@ -184,10 +197,14 @@ int spark_attn_decode_stack(const spark_geom* g, const float* h, int32_t n_layer
  * and v landing in their slots, encode_rope_neox_subdim on q and on k).
  *   q_rot    [batch][n_q*d] fp32 device: rotated queries.
  *   g_logits [batch][n_q] fp32 device: gate logits (before the sigmoid).
- *   kv       row slot(p) of K receives rope(k), of V receives v. */
+ *   kv       row slot(p) of K receives rope(k), of V receives v.
+ *   path     SPARK_PATH_*.
+ *   workspace as for spark_attn_decode (the MMA path keeps its activation
+ *            rows, rope tables and split-K partial results there). */
 int spark_dbg_qkv_rope(const spark_geom* g, const float* h, const spark_layer_weights* w,
                        const spark_kv_layer* kv, int32_t layer_class, const int32_t* positions,
-                       int32_t batch, float* q_rot, float* g_logits, void* stream);
+                       int32_t batch, float* q_rot, float* g_logits, int32_t path,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* GQA decode attention over each sequence's window (attn.rs,
  * encode_attention_block -> kv_write.rs, encode_attention_any), split over
@@ -227,10 +244,12 @@ int spark_dbg_attention_noalloc(const spark_geom* g, const float* q_rot,
  * and the o_proj GEMV; mod.rs: encode_residual_add).
  *   a        [batch][n_q*d] fp32 device, un-gated attention output.
  *   g_logits [batch][n_q] fp32 device gate logits.
- *   h        [batch][hidden] fp32 device; out [batch][hidden], may equal h. */
+ *   h        [batch][hidden] fp32 device; out [batch][hidden], may equal h.
+ *   path, workspace as for spark_dbg_qkv_rope. */
 int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* g_logits,
                          const float* h, const spark_layer_weights* w, int32_t batch,
-                         float* out, void* stream);
+                         float* out, int32_t path, void* workspace, size_t workspace_bytes,
+                         void* stream);
 
 /* Human-readable text of a status code (static storage). */
 const char* spark_attn_status_string(int status);

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported_and_bound(B):
 
 
 def test_abi_version_and_status_strings(B):
-    assert B.spark_attn_abi_version() == 1
+    assert B.spark_attn_abi_version() == 2
     for code in range(-7, 1):
         s = B.spark_attn_status_string(code)
         assert s and s != "unknown status"
@@ -146,3 +146,41 @@ def test_rejects_unsupported_geometry(B):
     g = B.spark_geom_default()
     g.scale = float("nan")
     assert _call(B, geom=g) == -1
+
+
+def _dbg_qkv(B, path, dtype=None, batch=2):
+    lib = B.load()
+    g = B.spark_geom_default()
+    w = B.SparkLayerWeights(FAKE, FAKE, FAKE, FAKE, B.SPARK_BF16 if dtype is None else dtype)
+    k = B.SparkKvLayer(FAKE, FAKE, 1024, 0, B.SPARK_BF16)
+    pos = (ctypes.c_int32 * batch)(*([5] * batch))
+    need = B.spark_attn_workspace_bytes(g, batch)
+    return lib.spark_dbg_qkv_rope(ctypes.byref(g), FAKE, ctypes.byref(w), ctypes.byref(k), 1, pos, batch,
+                                  FAKE, FAKE, path, FAKE, need, None)
+
+
+def _dbg_oproj(B, path, dtype=None, batch=2, ws_bytes=None):
+    lib = B.load()
+    g = B.spark_geom_default()
+    w = B.SparkLayerWeights(FAKE, FAKE, FAKE, FAKE, B.SPARK_BF16 if dtype is None else dtype)
+    need = B.spark_attn_workspace_bytes(g, batch) if ws_bytes is None else ws_bytes
+    return lib.spark_dbg_gate_oproj(ctypes.byref(g), FAKE, FAKE, FAKE, ctypes.byref(w), batch, FAKE, path,
+                                    FAKE, need, None)
+
+
+def test_projection_path_argument_is_validated(B):
+    # an unknown path, and the tensor-core path forced on fp32 weights, are
+    # refused before anything is enqueued
+    assert _dbg_qkv(B, 3) == -1
+    assert _dbg_qkv(B, -1) == -1
+    assert _dbg_oproj(B, 9) == -1
+    assert _dbg_qkv(B, B.SPARK_PATH_MMA, dtype=B.SPARK_F32) == -5
+    assert _dbg_oproj(B, B.SPARK_PATH_MMA, dtype=B.SPARK_F32) == -5
+    # the stage entry points need a workspace now
+    assert _dbg_oproj(B, 0, ws_bytes=16) == -4
+
+
+def test_workspace_grows_with_the_tensor_core_batch(B):
+    g = B.spark_geom_default()
+    small, b8, b64, b128, b1024 = (B.spark_attn_workspace_bytes(g, b) for b in (1, 8, 64, 128, 1024))
+    assert small < b8 < b64 < b128 < b1024
