@@ -32,23 +32,22 @@
 namespace spark {
 namespace {
 
-constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kMinRowsPerCta = 64;            // default grid: at least this many rows per CTA
 constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from which the deep ring pays
 
-template <typename CT, int NS>
+template <typename CT, int NS, int NC>
 struct Smem {
-  static_assert(NS % kConsumers == 0, "each stage must belong to one consumer warp");
+  static_assert(NS % NC == 0, "each stage must belong to one consumer warp");
   static constexpr int kStages = NS;
   static constexpr int kSubs = kHeadDim / CacheT<CT>::kLineElems;
   static constexpr int kHalf = kv_half_bytes<CT>();  // the K (or V) half of a stage
   static constexpr int kStage = 2 * kHalf;
   static constexpr int kQ = kStages * kStage;
   static constexpr int kP = kQ + 4 * kQStride * 4;
-  static constexpr int kM = kP + kConsumers * kTile * 16;
-  static constexpr int kL = kM + kConsumers * 4 * 4;
-  static constexpr int kO = kL + kConsumers * 4 * 4;
-  static constexpr int kBars = kO + kConsumers * 4 * kHeadDim * 4;
+  static constexpr int kM = kP + NC * kTile * 16;
+  static constexpr int kL = kM + NC * 4 * 4;
+  static constexpr int kO = kL + NC * 4 * 4;
+  static constexpr int kBars = kO + NC * 4 * kHeadDim * 4;
   static constexpr int kFlags = kBars + 2 * kStages * 8;
   static constexpr int kBytes = kFlags + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 (128B swizzle)
@@ -84,15 +83,16 @@ __device__ __forceinline__ Share share_begin(const AttnArgs<MAXB>& args, int bat
   return s;
 }
 
-template <typename CT, int NS, int MAXB>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename CT, int NS, int NC, int MINB, int MAXB>
+__global__ void __launch_bounds__((NC + 1) * 32, MINB)
     k_attn_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const float* __restrict__ q_rot, float* __restrict__ a_out,
                   float* __restrict__ part, uint32_t* __restrict__ counters, uint32_t* err,
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
                   const __grid_constant__ AttnArgs<MAXB> args) {
-  using S = Smem<CT, NS>;
+  using S = Smem<CT, NS, NC>;
+  constexpr int kCT = NC * 32;  // consumer threads
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* pos = args.pos;
 
   // ------------------------------------------------------------ producer
-  if (warp == kConsumers) {
+  if (warp == NC) {
     if (lane != 0) return;
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
@@ -193,16 +193,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t r0 = sh.f - gs, r1 = min(sh.f1, gs + rows) - gs;
     const Window w = window_of(pos[b], full != 0, window, ring_capacity);
 
-    named_bar_sync(kBarConsumers, kConsumerThreads);  // the previous group's merge is done
-    attn_load_q(q_s, q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, tid);
-    named_bar_sync(kBarConsumers, kConsumerThreads);
+    named_bar_sync(kBarConsumers, kCT);  // the previous group's merge is done
+    attn_load_q<kCT>(q_s, q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, tid);
+    named_bar_sync(kBarConsumers, kCT);
     st.reset();
 
     for (int64_t r = r0; r < r1;) {
       int64_t e = min(r1, r + kTile);
       if (r < w.len_a && e > w.len_a) e = w.len_a;
       const int n = (int)(e - r);
-      if ((int)(k % kConsumers) == warp) {
+      if ((int)(k % NC) == warp) {
         const int s = (int)(k % NS);
         const uint32_t u = k / NS;
         const bool ok = !flags[0] && mbar_wait_bounded(&full_bar[s], u & 1, flags, kWaitLimitNs);
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int g = b * n_kv + j;
     const int c_first = cta_of(gs, total, G), c_last = cta_of(gs + rows - 1, total, G);
-    attn_finish_group<kConsumers>(st, msm, flags, part, counters,
+    attn_finish_group<NC>(st, msm, flags, part, counters,
                       a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, g, c, c_first,
                       c_last - c_first + 1);
     sh.f = gs + r1;
@@ -251,13 +251,13 @@ bool make_cache_map(CUtensorMap* map, const void* base, int n_kv, int64_t rows) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename CT, int NS, int MAXB>
+template <typename CT, int NS, int NC, int MINB, int MAXB>
 cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_kv,
                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
                      const int32_t* positions, int batch, float* a, float* part,
                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
                      size_t l2_pf_bytes, cudaStream_t st) {
-  using S = Smem<CT, NS>;
+  using S = Smem<CT, NS, NC>;
   AttnArgs<MAXB> args;
   args.prefix[0] = 0;
   for (int b = 0; b < MAXB; ++b) {
@@ -269,7 +269,8 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   int G = n_ctas;
   if (G <= 0) {
     const int64_t want = (total + kMinRowsPerCta - 1) / kMinRowsPerCta;
-    G = (int)(want < device_sm_count() ? want : device_sm_count());
+    const int cap = MINB * device_sm_count();
+    G = (int)(want < cap ? want : cap);
   }
   if (G < 1) G = 1;
   if (G > kMaxAttnCtas) G = kMaxAttnCtas;
@@ -278,28 +279,28 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   if (!make_cache_map<CT>(&mk, kc, n_kv, (int64_t)batch * capacity) ||
       !make_cache_map<CT>(&mv, vc, n_kv, (int64_t)batch * capacity))
     return cudaErrorInvalidValue;
-  auto kern = k_attn_decode<CT, NS, MAXB>;
+  auto kern = k_attn_decode<CT, NS, NC, MINB, MAXB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(kern, dim3(G), dim3(kThreads), S::kAlloc, st, mk, mv, q_rot, a, part, counters,
+  return launch_pdl(kern, dim3(G), dim3((NC + 1) * 32), S::kAlloc, st, mk, mv, q_rot, a, part, counters,
                     err, batch, n_kv, capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
                     static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
 }
 
-template <typename CT, int NS>
+template <typename CT, int NS, int NC, int MINB>
 cudaError_t launch_ns(const float* q_rot, const void* kc, const void* vc, int n_kv,
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
                       size_t l2_pf_bytes, cudaStream_t st) {
   if (batch <= 8)
-    return launch_t<CT, NS, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
+    return launch_t<CT, NS, NC, MINB, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
   if (batch <= 64)
-    return launch_t<CT, NS, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
+    return launch_t<CT, NS, NC, MINB, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
                                 positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
-  return launch_t<CT, NS, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
+  return launch_t<CT, NS, NC, MINB, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
                                            window, scale, positions, batch, a, part, counters, err,
                                            n_ctas, l2_pf, l2_pf_bytes, st);
 }
@@ -313,10 +314,10 @@ cudaError_t launch_ct(const float* q_rot, const void* kc, const void* vc, int n_
   int64_t rows = 0;
   for (int b = 0; b < batch; ++b) rows += window_of(positions[b], full, window, ring_capacity).rows;
   if ((int64_t)n_kv * rows >= kDeepRows)
-    return launch_ns<CT, CacheT<CT>::kDeep>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
-                                      scale, positions, batch, a, part, counters, err, n_ctas,
-                                      l2_pf, l2_pf_bytes, st);
-  return launch_ns<CT, CacheT<CT>::kShallow>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
+    return launch_ns<CT, CacheT<CT>::kDeep, kConsumers, CacheT<CT>::kDeepBlocks>(
+        q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale, positions, batch, a, part,
+        counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+  return launch_ns<CT, CacheT<CT>::kShallow, kConsumers, 1>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
                                        scale, positions, batch, a, part, counters, err, n_ctas,
                                        l2_pf, l2_pf_bytes, st);
 }

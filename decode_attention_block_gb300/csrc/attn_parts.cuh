@@ -24,15 +24,20 @@ constexpr int kBarMerge = 3;              // named barrier id of warps 0-3 while
 
 template <typename CT>
 struct CacheT;
-// Pipeline depth of the per-layer kernel (a multiple of the consumer count:
-// tile k lives in stage k % NS and belongs to warp k % 4, so each stage always
-// serves one warp and no wait can alias an older mbarrier phase).  Long
-// histories take a deep ring (the kernel runs alone for hundreds of
-// microseconds); short ones a shallow ring.
+// Pipeline shape of the per-layer kernel.  The ring depth is a multiple of
+// the consumer count (tile k lives in stage k % NS and belongs to warp k % 4,
+// so each stage always serves one warp and no wait can alias an older
+// mbarrier phase).  Long histories run two CTAs per SM with a 4-stage ring
+// each (registers capped so both fit): with one consumer warp per SMSP the
+// q.k / p.v FMA chains left the issue slots 60% idle, and a second CTA fills
+// them (measured 75% -> 90% of HBM peak at 131072 rows; one CTA with eight
+// consumer warps did not help, its single producer serialising on the ring).
+// Short histories take one CTA per SM.
 template <>
 struct CacheT<__nv_bfloat16> {
   static constexpr int kLineElems = 64;
-  static constexpr int kDeep = 8;
+  static constexpr int kDeep = 4;
+  static constexpr int kDeepBlocks = 2;  // CTAs per SM
   static constexpr int kShallow = 4;
   static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
@@ -40,6 +45,7 @@ template <>
 struct CacheT<float> {
   static constexpr int kLineElems = 32;
   static constexpr int kDeep = 4;
+  static constexpr int kDeepBlocks = 1;  // a 4-stage fp32 ring fills half the SM's shared memory
   static constexpr int kShallow = 4;
   static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 };
