@@ -26,6 +26,8 @@
 // states are merged through shared memory.
 #include <math.h>
 
+#include <type_traits>
+
 #include "attn_parts.cuh"
 #include "launch.h"
 
@@ -182,10 +184,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   }
 
   // ------------------------------------------------------------ consumers
+  // bf16 caches take the tensor-core tile, fp32 caches the CUDA-core one
+  constexpr bool kMma = std::is_same<CT, __nv_bfloat16>::value;
   const MergeSmem msm{ms, ls, os};
   uint32_t k = 0;
   Share sh = share_begin(args, batch, n_kv, f0, f1);
   AttnState st;
+  MmaQ mq;
+  MmaState mst;
   while (sh.f < sh.f1) {
     const int b = sh.b, j = sh.j;
     const int64_t rows = args.prefix[b + 1] - args.prefix[b];
@@ -194,9 +200,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     const Window w = window_of(pos[b], full != 0, window, ring_capacity);
 
     named_bar_sync(kBarConsumers, kCT);  // the previous group's merge is done
-    attn_load_q<kCT>(q_s, q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, tid);
-    named_bar_sync(kBarConsumers, kCT);
-    st.reset();
+    const float* qg = q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
+    if constexpr (kMma) {
+      mma_load_q(mq, qg);
+      mst.reset();
+    } else {
+      attn_load_q<kCT>(q_s, qg, tid);
+      named_bar_sync(kBarConsumers, kCT);
+      st.reset();
+    }
 
     for (int64_t r = r0; r < r1;) {
       int64_t e = min(r1, r + kTile);
@@ -205,15 +217,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       if ((int)(k % NC) == warp) {
         const int s = (int)(k % NS);
         const uint32_t u = k / NS;
-        const bool ok = !flags[0] && mbar_wait_bounded(&full_bar[s], u & 1, flags, kWaitLimitNs);
+        const bool ok = __all_sync(0xffffffffu, !flags[0] && mbar_wait_bounded(&full_bar[s], u & 1, flags, kWaitLimitNs));
         if (!ok) {
           if (lane == 0 && !flags[0]) {
             flags[0] = 1;
             atomicOr(err, kErrWaitTimeout);
           }
         } else {
-          const unsigned char* kst = stages + s * S::kStage;
-          attn_tile<CT>(kst, kst + S::kHalf, n, q_s, p_s + warp * kTile, scale_log2, st);
+          unsigned char* kst = stages + s * S::kStage;
+          if constexpr (kMma)
+            attn_tile_mma(kst, kst + S::kHalf, n, mq, reinterpret_cast<float*>(p_s + warp * kTile), scale_log2, mst);
+          else
+            attn_tile<CT>(kst, kst + S::kHalf, n, q_s, p_s + warp * kTile, scale_log2, st);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -224,9 +239,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
 
     const int g = b * n_kv + j;
     const int c_first = cta_of(gs, total, G), c_last = cta_of(gs + rows - 1, total, G);
-    attn_finish_group<NC>(st, msm, flags, part, counters,
-                      a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, g, c, c_first,
-                      c_last - c_first + 1);
+    float* a_head0 = a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
+    if constexpr (kMma)
+      attn_store_state_mma(mst, msm);
+    else
+      attn_store_state(st, msm);
+    attn_merge_group<NC>(msm, flags, part, counters, a_head0, g, c, c_first, c_last - c_first + 1);
     sh.f = gs + r1;
     if (++sh.j == n_kv) { sh.j = 0; ++sh.b; }
   }

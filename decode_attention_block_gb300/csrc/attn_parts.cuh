@@ -248,12 +248,9 @@ struct MergeSmem {
 // with a running max, loading eight partials per round trip.  flags[0] is the
 // block's abort flag, flags[1] a scratch word.  a_head0 points at the output
 // of the group's first query head.
-template <int NW>
-__device__ __forceinline__ void attn_finish_group(const AttnState& st, const MergeSmem& sm,
-                                                  volatile int* flags, float* part,
-                                                  uint32_t* counters, float* a_head0, int g, int c,
-                                                  int c_first, int cnt) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// Put one warp's state (the CUDA-core tile layout) into the merge scratch.
+__device__ __forceinline__ void attn_store_state(const AttnState& st, const MergeSmem& sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
     const float lw = warp_sum(st.l[h]);
@@ -265,6 +262,28 @@ __device__ __forceinline__ void attn_finish_group(const AttnState& st, const Mer
     dst[0] = make_float4(st.o[h][0].x, st.o[h][0].y, st.o[h][1].x, st.o[h][1].y);
     dst[1] = make_float4(st.o[h][2].x, st.o[h][2].y, st.o[h][3].x, st.o[h][3].y);
   }
+}
+
+template <int NW>
+__device__ __forceinline__ void attn_merge_group(const MergeSmem& sm, volatile int* flags, float* part,
+                                                 uint32_t* counters, float* a_head0, int g, int c,
+                                                 int c_first, int cnt);
+
+template <int NW>
+__device__ __forceinline__ void attn_finish_group(const AttnState& st, const MergeSmem& sm,
+                                                  volatile int* flags, float* part,
+                                                  uint32_t* counters, float* a_head0, int g, int c,
+                                                  int c_first, int cnt) {
+  attn_store_state(st, sm);
+  attn_merge_group<NW>(sm, flags, part, counters, a_head0, g, c, c_first, cnt);
+}
+
+// The merge of attn_finish_group, once every warp's state is in `sm`.
+template <int NW>
+__device__ __forceinline__ void attn_merge_group(const MergeSmem& sm, volatile int* flags, float* part,
+                                                 uint32_t* counters, float* a_head0, int g, int c,
+                                                 int c_first, int cnt) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   named_bar_sync(kBarConsumers, NW * 32);
   if (warp >= kGroup) return;
   const int h = warp;
@@ -359,6 +378,204 @@ __device__ __forceinline__ void attn_finish_group(const AttnState& st, const Mer
     reinterpret_cast<float4*>(a_dst)[0] = make_float4(O2[0] * inv, O2[1] * inv, O2[2] * inv, O2[3] * inv);
     reinterpret_cast<float4*>(a_dst)[1] = make_float4(O2[4] * inv, O2[5] * inv, O2[6] * inv, O2[7] * inv);
     if (tid == 0) counters[g] = 0;  // ready for the next call
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// The same tile on the tensor cores (bf16 caches): warp-level
+// mma.m16n8k16 (bf16 in, fp32 accumulate) for both contractions.
+//   s = K q^T:  A = the 16-row K tile (rows x dims, from shared memory by
+//               ldmatrix through the TMA swizzle), B = [q_hi | q_lo]^T, the
+//               group's 4 query heads split into two bf16 halves (8 columns,
+//               q = q_hi + q_lo keeps 16 significant bits), 16 steps of 16 dims;
+//   o^T += V^T p^T: A = V^T (ldmatrix.trans of the V tile), B = [p_hi | p_lo]^T,
+//               one MMA per 16 dims (16 of them), the accumulator o^T
+//               (256 dims x 8 columns) held in registers across tiles.
+// Lane (g = lane / 4, t = lane % 4) ends each tile holding the scores of
+// rows g and g + 8 for heads 2 (t & 1) and 2 (t & 1) + 1 (the hi and lo
+// columns added), and the running max / sum of those two heads.
+// ---------------------------------------------------------------------------
+struct MmaQ {
+  uint32_t b[kHeadDim / 16][2];  // B fragments of [q_hi | q_lo]^T, one pair per 16-dim step
+};
+
+struct MmaState {
+  float o[kHeadDim / 16][4];  // o^T fragments: dims (16 mt + g, + 8) x columns (2t, 2t + 1)
+  float m[2], l[2];           // heads 2 (t & 1) + j, base 2
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < kHeadDim / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo_elem, hi_elem);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// x, or its bf16 remainder x - bf16(x): the two halves of a hi / lo split
+__device__ __forceinline__ float split_part(float x, bool lo) {
+  return lo ? x - __bfloat162float(__float2bfloat16_rn(x)) : x;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// shared-memory address of the 16 bytes holding dims [d, d + 8) of tile row
+// `row` in a bf16 half-stage (128-byte TMA swizzle, 64-dim boxes)
+__device__ __forceinline__ uint32_t tile_chunk(uint32_t half, int row, int d) {
+  return half + (uint32_t)((d >> 6) * kSubBytes + row * kLine + ((((d & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+// B fragments of the group's queries (q: 4 heads x 256 fp32, global memory):
+// column n = g holds head g & 3, its hi half for g < 4 and its lo half after.
+__device__ __forceinline__ void mma_load_q(MmaQ& Q, const float* qg) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* qh = qg + (g & 3) * kHeadDim + 2 * t;
+  const bool lo = g >= 4;
+  float2 x[kHeadDim / 16][2];
+#pragma unroll
+  for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+    x[ks][0] = __ldcg(reinterpret_cast<const float2*>(qh + 16 * ks));
+    x[ks][1] = __ldcg(reinterpret_cast<const float2*>(qh + 16 * ks + 8));
+  }
+#pragma unroll
+  for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+    Q.b[ks][0] = pack_bf16x2(split_part(x[ks][0].x, lo), split_part(x[ks][0].y, lo));
+    Q.b[ks][1] = pack_bf16x2(split_part(x[ks][1].x, lo), split_part(x[ks][1].y, lo));
+  }
+}
+
+// One warp folds an n-row tile into its state (bf16 K and V half-stages).
+// p_w: the warp's 16 x 4 fp32 probability scratch.  Rows n..15 of the V
+// half-stage are zeroed first (their probability is 0, and 0 * a non-finite
+// stale value would not be).
+__device__ __forceinline__ void attn_tile_mma(unsigned char* kst, unsigned char* vst, int n,
+                                              const MmaQ& Q, float* p_w, float scale_log2,
+                                              MmaState& st) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
+  const int mi = lane >> 3, lr = lane & 7;
+  // s = K [q_hi | q_lo]^T
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(tile_chunk(kbase, lr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1)), a);
+    mma_16816(c, a, Q.b[ks][0], Q.b[ks][1]);
+  }
+  if (n < kTile) {
+    for (int r = n; r < kTile; ++r)
+      *reinterpret_cast<uint4*>(vst + (lane >> 3) * kSubBytes + r * kLine + (lane & 7) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills the stage
+  }
+  // hi + lo columns, scale, mask: sc[r][j] = row (g + 8 r), head 2 (t & 1) + j
+  float sc[2][2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(0xffffffffu, c[i], 2);
+  sc[0][0] = g < n ? c[0] * scale_log2 : -INFINITY;
+  sc[0][1] = g < n ? c[1] * scale_log2 : -INFINITY;
+  sc[1][0] = g + 8 < n ? c[2] * scale_log2 : -INFINITY;
+  sc[1][1] = g + 8 < n ? c[3] * scale_log2 : -INFINITY;
+  // online softmax over the tile's rows (the 8 lanes sharing t)
+  float pr[2][2], corr[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float mx = fmaxf(sc[0][j], sc[1][j]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(st.m[j], mx);
+    corr[j] = exp2f(st.m[j] - mn);
+    st.m[j] = mn;
+    pr[0][j] = exp2f(sc[0][j] - mn);
+    pr[1][j] = exp2f(sc[1][j] - mn);
+    float rs = pr[0][j] + pr[1][j];
+    rs += __shfl_xor_sync(0xffffffffu, rs, 4);
+    rs += __shfl_xor_sync(0xffffffffu, rs, 8);
+    rs += __shfl_xor_sync(0xffffffffu, rs, 16);
+    st.l[j] = fmaf(st.l[j], corr[j], rs);
+  }
+  // p to the scratch ([row][head]), then the B fragments of [p_hi | p_lo]^T:
+  // column g is head g & 3, rows 2t, 2t + 1, 2t + 8, 2t + 9
+  __syncwarp();
+  if (t < 2) {
+    p_w[g * 4 + 2 * t] = pr[0][0];
+    p_w[g * 4 + 2 * t + 1] = pr[0][1];
+    p_w[(g + 8) * 4 + 2 * t] = pr[1][0];
+    p_w[(g + 8) * 4 + 2 * t + 1] = pr[1][1];
+  }
+  __syncwarp();
+  const int hp = g & 3;
+  const bool lo = g >= 4;
+  const uint32_t pb0 = pack_bf16x2(split_part(p_w[(2 * t) * 4 + hp], lo), split_part(p_w[(2 * t + 1) * 4 + hp], lo));
+  const uint32_t pb1 =
+      pack_bf16x2(split_part(p_w[(2 * t + 8) * 4 + hp], lo), split_part(p_w[(2 * t + 9) * 4 + hp], lo));
+  // rescale o^T (columns 2t, 2t + 1 are heads 2 (t & 1), + 1 in both halves)
+  if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < kHeadDim / 16; ++mt) {
+      st.o[mt][0] *= corr[0];
+      st.o[mt][1] *= corr[1];
+      st.o[mt][2] *= corr[0];
+      st.o[mt][3] *= corr[1];
+    }
+  }
+  __syncwarp();  // zeroed V rows visible to every lane's ldmatrix
+  // o^T += V^T [p_hi | p_lo]^T
+#pragma unroll
+  for (int mt = 0; mt < kHeadDim / 16; ++mt) {
+    uint32_t a[4];
+    ldsm_x4_trans(tile_chunk(vbase, lr + 8 * (mi >> 1), 16 * mt + 8 * (mi & 1)), a);
+    mma_16816(st.o[mt], a, pb0, pb1);
+  }
+}
+
+// Put one warp's tensor-core state into the merge scratch in the layout
+// attn_merge_group reads: the hi and lo columns added, heads 2 (t & 1) + j
+// written by the lanes with t < 2.
+__device__ __forceinline__ void attn_store_state_mma(MmaState& st, const MergeSmem& sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int mt = 0; mt < kHeadDim / 16; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) st.o[mt][i] += __shfl_xor_sync(0xffffffffu, st.o[mt][i], 2);
+  if (t < 2) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = 2 * t + j;
+      float* os = sm.os + (warp * 4 + h) * kHeadDim;
+#pragma unroll
+      for (int mt = 0; mt < kHeadDim / 16; ++mt) {
+        os[16 * mt + g] = st.o[mt][j];
+        os[16 * mt + g + 8] = st.o[mt][2 + j];
+      }
+      if (g == 0) {
+        sm.ms[warp * 4 + h] = st.m[j];
+        sm.ls[warp * 4 + h] = st.l[j];
+      }
+    }
   }
 }
 
