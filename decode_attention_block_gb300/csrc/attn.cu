@@ -130,9 +130,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     }
   }
   __syncthreads();
-  pdl_trigger();
-  pdl_wait();  // q_rot and the new cache rows come from the previous kernel
 
+  // Programmatic dependent launch.  q_rot and the token's own cache row
+  // (the last row of each (sequence, KV head) group) come from the kernel
+  // before this one, so they are read after pdl_wait().  Every other row
+  // was written by kernels that completed before that one started: each
+  // kernel of the block lets its successor launch only after its own
+  // pdl_wait() has returned.  The setup below reads only this kernel's
+  // arguments, and the producer issues the tiles of older rows, before the
+  // wait.
   const int64_t total = (int64_t)n_kv * args.prefix[batch];
   const int G = gridDim.x, c = blockIdx.x;
   const int64_t f0 = total * c / G, f1 = total * (c + 1) / G;
@@ -141,11 +147,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
 
   // ------------------------------------------------------------ producer
   if (warp == NC) {
-    if (lane != 0) return;
+    if (lane != 0) {
+      pdl_wait();
+      pdl_trigger();
+      return;
+    }
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     uint32_t k = 0;
-    bool ok = true;
+    bool ok = true, waited = false;
     Share sh = share_begin(args, batch, n_kv, f0, f1);
     while (sh.f < sh.f1) {
       const int64_t rows = args.prefix[sh.b + 1] - args.prefix[sh.b];
@@ -156,6 +166,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
         int64_t e = min(r1, r + kTile);
         if (r < w.len_a && e > w.len_a) e = w.len_a;
         const int64_t slot = r < w.len_a ? w.first_slot + r : r - w.len_a;
+        if (e == rows && !waited) {  // this tile holds the row the previous kernel wrote
+          pdl_wait();
+          pdl_trigger();
+          fence_proxy_async_global();
+          waited = true;
+        }
         const int s = (int)(k % NS);
         const uint32_t u = k / NS;
         if (ok && u > 0 && !mbar_wait_bounded(&empty_bar[s], (u - 1) & 1, flags, kWaitLimitNs)) {
@@ -180,6 +196,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       sh.f = gs + r1;
       if (++sh.j == n_kv) { sh.j = 0; ++sh.b; }
     }
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+    }
     return;
   }
 
@@ -189,6 +209,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   const MergeSmem msm{ms, ls, os};
   uint32_t k = 0;
   Share sh = share_begin(args, batch, n_kv, f0, f1);
+  bool waited = false;
   AttnState st;
   MmaQ mq;
   MmaState mst;
@@ -200,13 +221,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     const Window w = window_of(pos[b], full != 0, window, ring_capacity);
 
     named_bar_sync(kBarConsumers, kCT);  // the previous group's merge is done
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
     const float* qg = q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
+    attn_load_q<kCT>(q_s, qg, tid);
+    named_bar_sync(kBarConsumers, kCT);
     if constexpr (kMma) {
-      mma_load_q(mq, qg);
+      mma_q_from_smem(mq, q_s);
       mst.reset();
     } else {
-      attn_load_q<kCT>(q_s, qg, tid);
-      named_bar_sync(kBarConsumers, kCT);
       st.reset();
     }
 

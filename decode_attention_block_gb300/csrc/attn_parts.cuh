@@ -447,22 +447,20 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t half, int row, int d) {
   return half + (uint32_t)((d >> 6) * kSubBytes + row * kLine + ((((d & 63) >> 3) ^ (row & 7)) << 4));
 }
 
-// B fragments of the group's queries (q: 4 heads x 256 fp32, global memory):
-// column n = g holds head g & 3, its hi half for g < 4 and its lo half after.
-__device__ __forceinline__ void mma_load_q(MmaQ& Q, const float* qg) {
+// B fragments of the group's queries from q_s (the layout attn_load_q
+// writes: 4 heads x 256 fp32 in 64-dim slices): column n = g holds head
+// g & 3, its hi half for g < 4 and its lo half after.
+__device__ __forceinline__ void mma_q_from_smem(MmaQ& Q, const float* q_s) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const float* qh = qg + (g & 3) * kHeadDim + 2 * t;
   const bool lo = g >= 4;
-  float2 x[kHeadDim / 16][2];
+  const float* qh = q_s + (g & 3) * 64 + 2 * t;
 #pragma unroll
   for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-    x[ks][0] = __ldcg(reinterpret_cast<const float2*>(qh + 16 * ks));
-    x[ks][1] = __ldcg(reinterpret_cast<const float2*>(qh + 16 * ks + 8));
-  }
-#pragma unroll
-  for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-    Q.b[ks][0] = pack_bf16x2(split_part(x[ks][0].x, lo), split_part(x[ks][0].y, lo));
-    Q.b[ks][1] = pack_bf16x2(split_part(x[ks][1].x, lo), split_part(x[ks][1].y, lo));
+    const float* p0 = qh + (ks >> 2) * kQStride + 16 * (ks & 3);
+    const float2 x0 = *reinterpret_cast<const float2*>(p0);
+    const float2 x1 = *reinterpret_cast<const float2*>(p0 + 8);
+    Q.b[ks][0] = pack_bf16x2(split_part(x0.x, lo), split_part(x0.y, lo));
+    Q.b[ks][1] = pack_bf16x2(split_part(x1.x, lo), split_part(x1.y, lo));
   }
 }
 
@@ -476,14 +474,19 @@ __device__ __forceinline__ void attn_tile_mma(unsigned char* kst, unsigned char*
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
   const int mi = lane >> 3, lr = lane & 7;
-  // s = K [q_hi | q_lo]^T
-  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  // s = K [q_hi | q_lo]^T, even and odd 16-dim steps in two accumulator
+  // chains (half the dependent MMA latency)
+  float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-    uint32_t a[4];
+  for (int ks = 0; ks < kHeadDim / 16; ks += 2) {
+    uint32_t a[4], a2[4];
     ldsm_x4(tile_chunk(kbase, lr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1)), a);
+    ldsm_x4(tile_chunk(kbase, lr + 8 * (mi & 1), 16 * (ks + 1) + 8 * (mi >> 1)), a2);
     mma_16816(c, a, Q.b[ks][0], Q.b[ks][1]);
+    mma_16816(c2, a2, Q.b[ks + 1][0], Q.b[ks + 1][1]);
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] += c2[i];
   if (n < kTile) {
     for (int r = n; r < kTile; ++r)
       *reinterpret_cast<uint4*>(vst + (lane >> 3) * kSubBytes + r * kLine + (lane & 7) * 16) =

@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stage now (each warp the units it will consume first).
   if (lane == 0 && warp < nw)
     for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel starts only once the one before this has completed
 
   // activations: x = h * w (unscaled) and sum(h^2) per sequence
   float ss[NB];
@@ -228,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (lane == 0 && warp < nw)
     for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // the next kernel starts only once the one before this has completed
 
   // gated attention output: a * sigmoid(g), one gate scalar per head
   build_x_gated<E, NB, kThreads, kMaxPer>(a, g, q_dim, n_q, nb, xs, xfloats, threadIdx.x);

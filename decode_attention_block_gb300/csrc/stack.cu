@@ -158,10 +158,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   return v;
 }
 
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // All CTAs' compute warps meet; epoch counts the barriers this CTA passed.
 // Arrival is one fire-and-forget release add; the wait polls the counter
 // until every CTA of this epoch has arrived (the counter only grows within a
@@ -400,8 +396,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++j == n_kv) { j = 0; ++b; }
         }
       }
-      // While attention runs HBM is nearly idle: pull the next layer's share
-      // of q_k_v_proj rows into L2, so its P1 reads them from there.
+      // P3: o_proj rows, two per stage
+      trace(ws, l, kTrProdP3Start);
+      for (int k = o0; k < o1 && ok; ++k, ++i) {
+        if (!ring_acquire(ring, i, flags)) { fail(); break; }
+        uint64_t* bar = &ring.full[i % ring.ns];
+        mbar_arrive_expect_tx(bar, (uint32_t)(2 * orow));
+        bulk_load(ring.stage(i), L.o_w + (int64_t)(2 * k) * q_dim, (uint32_t)(2 * orow), bar);
+        ring_publish(ring, i);
+      }
+      // Pull the next layer's share of q_k_v_proj rows into L2, so its P1
+      // reads them from there.  Issued after this layer's o_proj rows: ahead
+      // of them it delayed P3 (measured 1.135 -> 1.069 ms on 36 layers).
       if (l + 1 < geo.n_layers) {
         const LayerDesc& Ln = args.layer[l + 1];
         const int rotn = args.rotary[Ln.full];
@@ -418,22 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P3: o_proj rows, two per stage
-      trace(ws, l, kTrProdP3Start);
-      for (int k = o0; k < o1 && ok; ++k, ++i) {
-        if (!ring_acquire(ring, i, flags)) { fail(); break; }
-        uint64_t* bar = &ring.full[i % ring.ns];
-        mbar_arrive_expect_tx(bar, (uint32_t)(2 * orow));
-        bulk_load(ring.stage(i), L.o_w + (int64_t)(2 * k) * q_dim, (uint32_t)(2 * orow), bar);
-        ring_publish(ring, i);
-      }
     }
     return;
   }
 
   // =================================================================== compute warps
   uint32_t i = 0, epoch = 0;
-  AttnState st;
   for (int l = 0; l < geo.n_layers; ++l) {
     const LayerDesc& L = args.layer[l];
     const int rot = args.rotary[L.full];
@@ -551,17 +547,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(kBarConsumers, kComputeThreads);  // the previous group's merge is done
         attn_load_q<kComputeThreads>(q_s, ws.q_rot + ((int64_t)b * n_q + kGroup * j) * kHeadDim, tid);
         named_bar_sync(kBarConsumers, kComputeThreads);
+        MmaQ mq;
+        MmaState mst;
+        mma_q_from_smem(mq, q_s);
+        mst.reset();
         if (tid == 0 && f == sh.f0) trace(ws, l, kTrP2Q);
-        st.reset();
         for (int64_t r = r0; r < r1; ++i) {
           int64_t e = min(r1, r + kTile);
           if (r < w.len_a && e > w.len_a) e = w.len_a;
           if ((int)(i % kComputeWarps) == warp) {
-            const bool ok = !flags[0] && ring_wait(ring, i, flags);
+            const bool ok = __all_sync(0xffffffffu, !flags[0] && ring_wait(ring, i, flags));
             if (ok) {
-              const unsigned char* kst = ring.stage(i);
-              attn_tile<__nv_bfloat16>(kst, kst + kv_half_bytes<__nv_bfloat16>(), (int)(e - r), q_s,
-                                       p_s + warp * kTile, geo.scale_log2, st);
+              unsigned char* kst = ring.stage(i);
+              attn_tile_mma(kst, kst + kv_half_bytes<__nv_bfloat16>(), (int)(e - r), mq,
+                            reinterpret_cast<float*>(p_s + warp * kTile), geo.scale_log2, mst);
             } else if (lane == 0 && !flags[0]) {
               flags[0] = 1;
               atomicOr(ws.err, kErrWaitTimeout);
@@ -575,9 +574,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const int g = b * n_kv + j;
           const int c_first = cta_of(gs, sh.total, sh.G), c_last = cta_of(gs + rows - 1, sh.total, sh.G);
-          attn_finish_group<kComputeWarps>(st, msm, flags, ws.part, ws.counters,
-                                           ws.a + ((int64_t)b * n_q + kGroup * j) * kHeadDim, g,
-                                           (int)blockIdx.x, c_first, c_last - c_first + 1);
+          attn_store_state_mma(mst, msm);
+          attn_merge_group<kComputeWarps>(msm, flags, ws.part, ws.counters,
+                                          ws.a + ((int64_t)b * n_q + kGroup * j) * kHeadDim, g,
+                                          (int)blockIdx.x, c_first, c_last - c_first + 1);
           if (tid == 0 && f == sh.f0) trace(ws, l, kTrP2Merged);
         }
         f = gs + r1;
