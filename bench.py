@@ -90,6 +90,28 @@ def step_bytes(wl: synth.Workload) -> dict:
     return {"total": total, "per_kernel": per}
 
 
+# DRAM bytes (read + write) per launch of the current kernels, from ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum) of these workloads;
+# the profile summaries give each capture's command.  Attention traffic
+# follows the rows read, so other workloads scale the captured ratio.
+TRAFFIC = {
+    ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_580_928,
+    ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_021_440,
+    ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_335_296,
+    ("full_bf16_b1_ctx131072", "attention"): 541_340_160,
+}
+ATTN_TRAFFIC_RATIO = 541_340_160 / 536_875_008
+
+
+def measured_traffic(workload: str, kernel: str, bytes_per_launch: float):
+    """(traffic per launch, how it was obtained) or (None, reason)."""
+    if (workload, kernel) in TRAFFIC:
+        return TRAFFIC[(workload, kernel)], "ncu capture of this workload"
+    if kernel == "attention":
+        return int(bytes_per_launch * ATTN_TRAFFIC_RATIO), "ncu capture at 131072 rows, scaled by rows read"
+    return None, "no capture of this kernel on this workload"
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -338,6 +360,7 @@ def bench_ours(args, wl, rank, local, world):
     top = max(share, key=share.get)
     peaks = measured_peaks()
     achieved = per_launch[top] / (kavg[top] * 1e-3) / 1e9
+    traffic, traffic_src = measured_traffic(wl.name, top, per_launch[top])
 
     # end to end through the public call: h from pinned host, out read back
     h_host = [synth.make_h(wl, "cpu").pin_memory() for _ in range(2)]
@@ -391,7 +414,8 @@ def bench_ours(args, wl, rank, local, world):
         "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
         "roofline": {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "traffic_source": traffic_src,
                      "bytes_per_launch": int(per_launch[top]),
                      "avg_launch_us": round(kavg[top] * 1e3, 3)},
         "kernels": {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": launches[k],

@@ -111,6 +111,11 @@ def workloads() -> dict:
                  "8 sequences at context 131072, one full layer (rotary 64 @ 5e6) and one sliding "
                  "layer (ring 512 wrapped many times), bf16",
                  "bf16", [131072] * 8, [LayerSpec(True, 0), LayerSpec(False, RING)], seed=1004),
+        Workload("full+sliding_bf16_b64_ctx512-1023",
+                 "64 sequences, context uniform in [512, 1023], one full and one sliding layer, "
+                 "bf16: the batched projections with caches small enough to profile",
+                 "bf16", _ragged_positions(1006, 64, 512, 1023),
+                 [LayerSpec(True, 0), LayerSpec(False, RING)], seed=1006),
         Workload("full_bf16_b1_ctx131072",
                  "one full layer (rotary 64 @ 5e6), bf16, one sequence at context 131072 "
                  "(a single long-context attention)",
