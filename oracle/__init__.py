@@ -25,5 +25,6 @@ from .spark_block import (  # noqa: F401
     sigmoid,
     head_gate,
     decode_step,
+    prefill_chunk,
     cache_rows_to_f64,
 )

@@ -43,6 +43,11 @@ Parity pins (``tests/test_oracle_pins.py``) -- every function here is pinned:
 * ``head_gate`` / ``sigmoid``: g = 0 halves the attention output.
 * ``decode_step``: ``o_proj = 0`` returns ``h`` exactly, and a pure-Python
   loop implementation of the whole block at a tiny geometry.
+* ``prefill_chunk``: one token equals ``decode_step``; a dense formulation
+  (every token of the chunk projected at once, one causal / sliding mask over
+  logical positions, softmax by rows) on a full layer with and without
+  history and on a ring that wraps inside the chunk, chunks longer than the
+  ring included; the final ring contents against a brute-force ring.
 """
 
 from __future__ import annotations
@@ -342,4 +347,39 @@ def decode_step(geom: OracleGeometry, h: np.ndarray, weights: dict,
                          ("window", (seq_len, kv_start, active_ring))):
             res[key].append(val)
     res["sequences"] = seqs
+    return res
+
+
+def prefill_chunk(geom: OracleGeometry, h: np.ndarray, weights: dict,
+                  k_cache: np.ndarray, v_cache: np.ndarray, is_full: bool,
+                  p0: int, ring_capacity: int) -> dict:
+    """M consecutive tokens of one sequence through the block, at positions
+    ``p0 .. p0 + M - 1``: the per-token attention block run token after token
+    (kv_write.rs, module doc: chunked prefill reuses the per-token attention
+    block, only the K/V projections being batched), so token ``t`` sees the
+    rows tokens ``< t`` of the chunk wrote, and on a ring a later token's
+    row replaces the row of the position ``ring_capacity`` before it.
+
+    Arguments as ``decode_step`` for one sequence: ``h [M, hidden]``,
+    ``k_cache, v_cache [capacity, n_kv, head_dim]`` (not modified).
+
+    Returns ``out [M, hidden]``, ``o [M, hidden]``, the caches after the
+    chunk (``k_cache``, ``v_cache``) and per token ``slot``, ``k_row``,
+    ``v_row``, ``q``, ``a``."""
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    M = h.shape[0]
+    res = {key: [] for key in ("out", "o", "slot", "k_row", "v_row", "q", "a")}
+    for t in range(M):
+        step = decode_step(geom, h[t:t + 1], weights, kc[None], vc[None], is_full, [p0 + t],
+                           ring_capacity)
+        slot = step["slot"][0]
+        kc[slot] = step["k_row"][0]
+        vc[slot] = step["v_row"][0]
+        for key in ("out", "o", "slot", "k_row", "v_row", "q", "a"):
+            res[key].append(step[key][0])
+    res["out"] = np.stack(res["out"])
+    res["o"] = np.stack(res["o"])
+    res["k_cache"] = kc
+    res["v_cache"] = vc
     return res

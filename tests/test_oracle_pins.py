@@ -456,3 +456,123 @@ def test_decode_step_matches_python_block(is_full, ring, bf16, p):
     res = oracle.decode_step(geom, h, weights, kc, vc, is_full, [p], ring)
     want = _python_block(geom, h[0], weights, kc[0], vc[0], is_full, p, ring, bf16)
     np.testing.assert_allclose(res["out"][0], want, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# a chunk of consecutive tokens (prefill / verify)
+# ---------------------------------------------------------------------------
+
+def _dense_chunk(geom, h, weights, history_k, history_v, hist_pos, is_full, p0, bf16):
+    """The chunk in one dense pass, written independently of decode_step:
+    every token projected at once as a matrix product, the history and the
+    chunk's own rows laid out by logical position, one mask (causal, and for
+    a sliding layer the window) over positions, a row-wise softmax.
+    history_k/v: rows of the positions in hist_pos (already in the cache)."""
+    def wf(x):
+        return oracle.bf16_bits_to_f64(x) if bf16 else np.asarray(x, dtype=np.float64)
+
+    def to_cache(x):
+        return oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(x)) if bf16 else x.astype(np.float32).astype(np.float64)
+
+    M, H = h.shape
+    nq, nkv, d = geom.n_q, geom.n_kv, geom.head_dim
+    hh = h.astype(np.float64)
+    X = hh / np.sqrt(np.mean(hh * hh, axis=1, keepdims=True) + geom.eps) * wf(weights["norm_w"])[None]
+    QKV = X @ wf(weights["qkv_w"]).T
+    G = X @ wf(weights["g_w"]).T
+    Q = QKV[:, :nq * d].reshape(M, nq, d)
+    K = QKV[:, nq * d:(nq + nkv) * d].reshape(M, nkv, d)
+    V = QKV[:, (nq + nkv) * d:].reshape(M, nkv, d)
+    r, theta = (geom.full_rotary_dim, geom.full_theta) if is_full else (d, geom.sliding_theta)
+    half = r // 2
+    pos = p0 + np.arange(M)
+    ang = pos[:, None] * theta ** (-2.0 * np.arange(half) / r)[None]      # [M, half]
+    c, s = np.cos(ang)[:, None], np.sin(ang)[:, None]
+
+    def rot(u):
+        out = u.copy()
+        a, b = u[..., :half], u[..., half:r]
+        out[..., :half] = a * c - b * s
+        out[..., half:r] = b * c + a * s
+        return out
+
+    Q, K = rot(Q), rot(K)
+    Kc, Vc = to_cache(K), to_cache(V)
+    keys_pos = np.concatenate([np.asarray(hist_pos, dtype=np.int64), pos])
+    Kall = np.concatenate([history_k, Kc], axis=0)                          # [P, nkv, d]
+    Vall = np.concatenate([history_v, Vc], axis=0)
+    mask = keys_pos[None, :] <= pos[:, None]
+    if not is_full:
+        mask &= keys_pos[None, :] > pos[:, None] - geom.window
+    grp = nq // nkv
+    A = np.zeros((M, nq, d))
+    for hq in range(nq):
+        S = geom.scale * np.einsum("md,pd->mp", Q[:, hq], Kall[:, hq // grp])
+        S = np.where(mask, S, -np.inf)
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        A[:, hq] = P @ Vall[:, hq // grp]
+    A *= (1.0 / (1.0 + np.exp(-G)))[:, :, None]
+    O = A.reshape(M, nq * d) @ wf(weights["o_w"]).T
+    return hh + O
+
+
+def _chunk_geom():
+    return OracleGeometry(hidden=16, n_q=8, n_kv=2, head_dim=8, full_rotary_dim=4, window=6,
+                          full_theta=500.0, sliding_theta=10.0, scale=8 ** -0.5)
+
+
+def test_prefill_chunk_one_token_is_a_decode_step():
+    geom = _chunk_geom()
+    rng = np.random.default_rng(200)
+    h, weights, kc, vc = _tiny_inputs(rng, geom, 1, 6, True)
+    res = oracle.prefill_chunk(geom, h, weights, kc[0], vc[0], False, 9, 6)
+    step = oracle.decode_step(geom, h, weights, kc, vc, False, [9], 6)
+    np.testing.assert_array_equal(res["out"][0], step["out"][0])
+    np.testing.assert_array_equal(res["k_cache"][step["slot"][0]], step["k_row"][0])
+
+
+@pytest.mark.parametrize("p0,M,bf16", [(0, 7, True), (5, 9, False), (3, 1, True)])
+def test_prefill_chunk_full_layer_matches_dense_causal(p0, M, bf16):
+    geom = _chunk_geom()
+    rng = np.random.default_rng(210 + p0 + M)
+    cap = p0 + M + 3
+    _, weights, kc, vc = _tiny_inputs(rng, geom, 1, cap, bf16)
+    h = rng.standard_normal((M, geom.hidden)).astype(np.float32)
+    res = oracle.prefill_chunk(geom, h, weights, kc[0], vc[0], True, p0, 0)
+    hist = list(range(p0))
+    want = _dense_chunk(geom, h, weights, oracle.cache_rows_to_f64(kc[0][:p0]),
+                        oracle.cache_rows_to_f64(vc[0][:p0]), hist, True, p0, bf16)
+    np.testing.assert_allclose(res["out"], want, rtol=1e-10, atol=1e-11)
+    # rows past the chunk are untouched, the chunk's slots hold its rows
+    np.testing.assert_array_equal(res["k_cache"][p0 + M:], kc[0][p0 + M:])
+    assert res["slot"] == list(range(p0, p0 + M))
+
+
+@pytest.mark.parametrize("p0,M", [(4, 5), (9, 8), (2, 15), (13, 2)])
+def test_prefill_chunk_ring_wrapping_inside_the_chunk(p0, M):
+    """Sliding layer, ring capacity == window: tokens late in the chunk
+    overwrite ring rows that earlier tokens of the same chunk still read;
+    each token must see the row of the position it needs."""
+    geom = _chunk_geom()
+    R = geom.window
+    rng = np.random.default_rng(230 + p0 + M)
+    _, weights, kc, vc = _tiny_inputs(rng, geom, 1, R, True)
+    h = rng.standard_normal((M, geom.hidden)).astype(np.float32)
+    res = oracle.prefill_chunk(geom, h, weights, kc[0], vc[0], False, p0, R)
+    # history: the positions the ring holds before the chunk, by logical position
+    hist = list(range(max(0, p0 - R), p0))
+    hk = oracle.cache_rows_to_f64(kc[0][[x % R for x in hist]]) if hist else np.zeros((0, geom.n_kv, geom.head_dim))
+    hv = oracle.cache_rows_to_f64(vc[0][[x % R for x in hist]]) if hist else np.zeros((0, geom.n_kv, geom.head_dim))
+    want = _dense_chunk(geom, h, weights, hk, hv, hist, False, p0, True)
+    np.testing.assert_allclose(res["out"], want, rtol=1e-10, atol=1e-11)
+    # brute-force ring: replay the writes in order into a dict slot -> position
+    holder = {x % R: x for x in range(max(0, p0 - R), p0)}
+    for t in range(M):
+        holder[(p0 + t) % R] = p0 + t
+    for slot in range(R):
+        x = holder.get(slot)
+        if x is not None and x >= p0:
+            np.testing.assert_array_equal(res["k_cache"][slot], res["k_row"][x - p0])
+        else:
+            np.testing.assert_array_equal(res["k_cache"][slot], kc[0][slot])
