@@ -81,6 +81,9 @@ _SIGNATURES = {
                                          ctypes.POINTER(SparkKvLayer), ctypes.c_int32,
                                          ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, _P, _P,
                                          ctypes.c_size_t, _P]),
+    "spark_attn_prefill": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkLayerWeights),
+                                          ctypes.POINTER(SparkKvLayer), ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, _P, _P, ctypes.c_size_t, _P]),
     "spark_attn_decode_stack": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.c_int32,
                                                ctypes.POINTER(SparkLayerWeights), ctypes.POINTER(SparkKvLayer),
                                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
@@ -244,6 +247,18 @@ def spark_attn_decode(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, k
                                     batch, _dev_ptr(out, "out", torch.float32),
                                     _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
                                     _stream(stream)), "spark_attn_decode")
+
+
+def spark_attn_prefill(geom: SparkGeom, h: torch.Tensor, weights: LayerWeights, kv: KvLayer,
+                       layer_class: int, p0: int, out: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """h.shape[0] consecutive tokens of one sequence (positions p0, p0+1, ...)
+    through one layer; kv is that sequence's cache ([1, capacity, n_kv, 256])."""
+    wc, kc = weights.to_c(), kv.to_c()
+    _check(load().spark_attn_prefill(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32), ctypes.byref(wc),
+                                     ctypes.byref(kc), int(layer_class), int(p0), int(h.shape[0]),
+                                     _dev_ptr(out, "out", torch.float32), _dev_ptr(ws, "workspace"),
+                                     ws.numel() * ws.element_size(), _stream(stream)),
+           "spark_attn_prefill")
 
 
 def spark_attn_decode_stack(geom: SparkGeom, h: torch.Tensor, weights: list, kvs: list, layer_classes,

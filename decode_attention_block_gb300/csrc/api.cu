@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "checks.h"
 #include "launch.h"
@@ -229,6 +230,58 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
   if (e == cudaSuccess)
     e = run_oproj(pick_path(SPARK_PATH_AUTO, w->dtype, g, 0, batch), g, a, g_logits, h, w, batch, out,
                   err, workspace, L, st);
+  return cuda_status(e);
+}
+
+int spark_attn_prefill(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                       const spark_kv_layer* kv, int32_t layer_class, int32_t p0, int32_t m,
+                       float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  int s;
+  if ((s = check_geom(g)) != SPARK_OK) return s;
+  if ((s = check_weights(w, true, true)) != SPARK_OK) return s;
+  if ((s = check_batch(m)) != SPARK_OK) return s;
+  if (p0 < 0 || (int64_t)p0 + m - 1 >= (int64_t)INT32_MAX - 1) return SPARK_ERR_POSITION;
+  const int32_t last = p0 + m - 1;  // the chunk's positions are p0 .. last
+  if ((s = check_kv(g, kv, layer_class, &last, 1)) != SPARK_OK) return s;
+  if ((s = check_ws(g, m, workspace, workspace_bytes)) != SPARK_OK) return s;
+  if (!h || !out || !aligned16(h) || !aligned16(out)) return SPARK_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(g->hidden, g->n_q, g->n_kv, m);
+  cudaStream_t st = (cudaStream_t)stream;
+  std::vector<int32_t> positions(m);
+  for (int32_t t = 0; t < m; ++t) positions[t] = p0 + t;
+  float* g_logits = ws_at<float>(workspace, L.g);
+  float* q_rot = ws_at<float>(workspace, L.q_rot);
+  float* a = ws_at<float>(workspace, L.a);
+  uint32_t* err = ws_at<uint32_t>(workspace, L.err);
+  // the chunk's k and v rows go to a staging buffer first: on a ring a later
+  // token's row replaces a row that earlier tokens of the chunk still read
+  const size_t ce = kv->dtype == SPARK_BF16 ? 2 : 4;
+  unsigned char* ks = ws_at<unsigned char>(workspace, L.stage);
+  unsigned char* vs = ks + (size_t)m * g->n_kv * kHeadDim * ce;
+  spark_kv_layer staged = *kv;
+  staged.k = ks;
+  staged.v = vs;
+  staged.capacity = 1;       // row t of the staging buffer holds token t:
+  staged.ring_capacity = 1;  // slot = position mod 1 = 0 of "sequence" t
+  int rotary_dim;
+  double theta;
+  rope_for(g, layer_class, &rotary_dim, &theta);
+  cudaError_t e = run_qkv(pick_path(SPARK_PATH_AUTO, w->dtype, g, rotary_dim, m), g, h, w, &staged,
+                          rotary_dim, theta, positions.data(), m, q_rot, g_logits, err, workspace, L, st);
+  ChunkSrc chunk;
+  chunk.p0 = p0;
+  chunk.k = ks;
+  chunk.v = vs;
+  if (e == cudaSuccess)
+    e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity, kv->ring_capacity,
+                         layer_class == SPARK_FULL, g->window, g->scale, positions.data(), m, a,
+                         ws_at<float>(workspace, L.part), ws_at<uint32_t>(workspace, L.counters), err,
+                         0, nullptr, 0, st, chunk);
+  if (e == cudaSuccess)
+    e = launch_commit_rows(kv->dtype, ks, vs, kv->k, kv->v, g->n_kv, p0, m, kv->ring_capacity, st);
+  if (e == cudaSuccess)
+    e = run_oproj(pick_path(SPARK_PATH_AUTO, w->dtype, g, 0, m), g, a, g_logits, h, w, m, out, err,
+                  workspace, L, st);
   return cuda_status(e);
 }
 

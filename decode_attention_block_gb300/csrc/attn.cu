@@ -68,6 +68,30 @@ struct Share {
   int b, j;        // current sequence, KV head
 };
 
+// The rows one group reads, by logical position kv_start + r, r < rows.
+// Rows r < c_rows come from the cache: slot first_slot + r for r < len_a,
+// then r - len_a (a ring wraps to row 0).  Rows r >= c_rows come from the
+// staging buffer of a chunk of tokens (row kv_start + r - p0): the rows the
+// chunk itself produces, which reach the cache only after attention.
+struct Rows {
+  int64_t kv_start, rows, c_rows, first_slot, len_a;
+};
+
+__host__ __device__ inline Rows rows_of(int64_t pos, bool full, int window, int ring, int64_t chunk_p0) {
+  const Window w = window_of(pos, full, window, ring);
+  Rows r{w.kv_start, w.rows, w.rows, w.first_slot, w.len_a};
+  if (chunk_p0 >= 0) {
+    // the cache holds the positions before the chunk: slot(x) = x mod ring
+    // (x itself before the ring first fills), for every such x
+    const int64_t c = chunk_p0 - w.kv_start;
+    r.c_rows = c < 0 ? 0 : (c > w.rows ? w.rows : c);
+    r.first_slot = ring > 0 ? w.kv_start % ring : w.kv_start;
+    const int64_t to_end = ring > 0 ? ring - r.first_slot : r.c_rows;
+    r.len_a = r.c_rows < to_end ? r.c_rows : to_end;
+  }
+  return r;
+}
+
 template <int MAXB>
 __device__ __forceinline__ Share share_begin(const AttnArgs<MAXB>& args, int batch, int n_kv,
                                              int64_t f0, int64_t f1) {
@@ -88,7 +112,8 @@ __device__ __forceinline__ Share share_begin(const AttnArgs<MAXB>& args, int bat
 template <typename CT, int NS, int NC, int MINB, int MAXB>
 __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     k_attn_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const float* __restrict__ q_rot, float* __restrict__ a_out,
+                  const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
+                  int64_t chunk_p0, const float* __restrict__ q_rot, float* __restrict__ a_out,
                   float* __restrict__ part, uint32_t* __restrict__ counters, uint32_t* err,
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
@@ -154,6 +179,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     }
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    if (chunk_p0 >= 0) {
+      prefetch_tensormap(&tm_ks);
+      prefetch_tensormap(&tm_vs);
+    }
     uint32_t k = 0;
     bool ok = true, waited = false;
     Share sh = share_begin(args, batch, n_kv, f0, f1);
@@ -161,12 +190,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       const int64_t rows = args.prefix[sh.b + 1] - args.prefix[sh.b];
       const int64_t gs = (int64_t)n_kv * args.prefix[sh.b] + sh.j * rows;
       const int64_t r0 = sh.f - gs, r1 = min(sh.f1, gs + rows) - gs;
-      const Window w = window_of(pos[sh.b], full != 0, window, ring_capacity);
+      const Rows w = rows_of(pos[sh.b], full != 0, window, ring_capacity, chunk_p0);
       for (int64_t r = r0; r < r1;) {
         int64_t e = min(r1, r + kTile);
         if (r < w.len_a && e > w.len_a) e = w.len_a;
+        if (r < w.c_rows && e > w.c_rows) e = w.c_rows;
+        const bool staged = r >= w.c_rows;
         const int64_t slot = r < w.len_a ? w.first_slot + r : r - w.len_a;
-        if (e == rows && !waited) {  // this tile holds the row the previous kernel wrote
+        // tiles holding rows the previous kernel wrote: the token's own row
+        // (decode), or any row of the chunk's staging buffer
+        if ((chunk_p0 >= 0 ? staged : e == rows) && !waited) {
           pdl_wait();
           pdl_trigger();
           fence_proxy_async_global();
@@ -183,11 +216,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
           mbar_arrive_expect_tx(&full_bar[s], S::kStage);
           unsigned char* kd = stages + s * S::kStage;
           unsigned char* vd = kd + S::kHalf;
-          const int z = (int)((int64_t)sh.b * capacity + slot);
+          const CUtensorMap* mk = staged ? &tm_ks : &tm_k;
+          const CUtensorMap* mv = staged ? &tm_vs : &tm_v;
+          const int z = staged ? (int)(w.kv_start + r - chunk_p0)
+                               : (int)((int64_t)(chunk_p0 >= 0 ? 0 : sh.b) * capacity + slot);
 #pragma unroll
           for (int q = 0; q < S::kSubs; ++q) {
-            tma_load_3d(kd + q * kSubBytes, &tm_k, &full_bar[s], q * CacheT<CT>::kLineElems, sh.j, z);
-            tma_load_3d(vd + q * kSubBytes, &tm_v, &full_bar[s], q * CacheT<CT>::kLineElems, sh.j, z);
+            tma_load_3d(kd + q * kSubBytes, mk, &full_bar[s], q * CacheT<CT>::kLineElems, sh.j, z);
+            tma_load_3d(vd + q * kSubBytes, mv, &full_bar[s], q * CacheT<CT>::kLineElems, sh.j, z);
           }
         }
         ++k;
@@ -218,7 +254,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     const int64_t rows = args.prefix[b + 1] - args.prefix[b];
     const int64_t gs = (int64_t)n_kv * args.prefix[b] + j * rows;
     const int64_t r0 = sh.f - gs, r1 = min(sh.f1, gs + rows) - gs;
-    const Window w = window_of(pos[b], full != 0, window, ring_capacity);
+    const Rows w = rows_of(pos[b], full != 0, window, ring_capacity, chunk_p0);
 
     named_bar_sync(kBarConsumers, kCT);  // the previous group's merge is done
     if (!waited) {
@@ -239,6 +275,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     for (int64_t r = r0; r < r1;) {
       int64_t e = min(r1, r + kTile);
       if (r < w.len_a && e > w.len_a) e = w.len_a;
+      if (r < w.c_rows && e > w.c_rows) e = w.c_rows;
       const int n = (int)(e - r);
       if ((int)(k % NC) == warp) {
         const int s = (int)(k % NS);
@@ -300,12 +337,12 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
                      const int32_t* positions, int batch, float* a, float* part,
                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                     size_t l2_pf_bytes, cudaStream_t st) {
+                     size_t l2_pf_bytes, const ChunkSrc& chunk, cudaStream_t st) {
   using S = Smem<CT, NS, NC>;
   AttnArgs<MAXB> args;
   args.prefix[0] = 0;
   for (int b = 0; b < MAXB; ++b) {
-    const int64_t rows = b < batch ? window_of(positions[b], full, window, ring_capacity).rows : 0;
+    const int64_t rows = b < batch ? rows_of(positions[b], full, window, ring_capacity, chunk.p0).rows : 0;
     args.prefix[b + 1] = args.prefix[b] + rows;
     args.pos[b] = b < batch ? positions[b] : 0;
   }
@@ -319,15 +356,24 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   if (G < 1) G = 1;
   if (G > kMaxAttnCtas) G = kMaxAttnCtas;
 
-  CUtensorMap mk, mv;
-  if (!make_cache_map<CT>(&mk, kc, n_kv, (int64_t)batch * capacity) ||
-      !make_cache_map<CT>(&mv, vc, n_kv, (int64_t)batch * capacity))
+  // a chunk's tokens share one sequence's cache; decode rows are per sequence
+  const int64_t cache_rows = chunk.p0 >= 0 ? capacity : (int64_t)batch * capacity;
+  CUtensorMap mk, mv, mks, mvs;
+  if (!make_cache_map<CT>(&mk, kc, n_kv, cache_rows) || !make_cache_map<CT>(&mv, vc, n_kv, cache_rows))
     return cudaErrorInvalidValue;
+  if (chunk.p0 >= 0) {
+    if (!make_cache_map<CT>(&mks, chunk.k, n_kv, batch) || !make_cache_map<CT>(&mvs, chunk.v, n_kv, batch))
+      return cudaErrorInvalidValue;
+  } else {
+    mks = mk;
+    mvs = mv;
+  }
   auto kern = k_attn_decode<CT, NS, NC, MINB, MAXB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(kern, dim3(G), dim3((NC + 1) * 32), S::kAlloc, st, mk, mv, q_rot, a, part, counters,
+  return launch_pdl(kern, dim3(G), dim3((NC + 1) * 32), S::kAlloc, st, mk, mv, mks, mvs,
+                    (int64_t)chunk.p0, q_rot, a, part, counters,
                     err, batch, n_kv, capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
                     static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
 }
@@ -337,16 +383,16 @@ cudaError_t launch_ns(const float* q_rot, const void* kc, const void* vc, int n_
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                      size_t l2_pf_bytes, cudaStream_t st) {
+                      size_t l2_pf_bytes, const ChunkSrc& chunk, cudaStream_t st) {
   if (batch <= 8)
     return launch_t<CT, NS, NC, MINB, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                               positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+                               positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
   if (batch <= 64)
     return launch_t<CT, NS, NC, MINB, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
   return launch_t<CT, NS, NC, MINB, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
                                            window, scale, positions, batch, a, part, counters, err,
-                                           n_ctas, l2_pf, l2_pf_bytes, st);
+                                           n_ctas, l2_pf, l2_pf_bytes, chunk, st);
 }
 
 template <typename CT>
@@ -354,16 +400,16 @@ cudaError_t launch_ct(const float* q_rot, const void* kc, const void* vc, int n_
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                      size_t l2_pf_bytes, cudaStream_t st) {
+                      size_t l2_pf_bytes, const ChunkSrc& chunk, cudaStream_t st) {
   int64_t rows = 0;
   for (int b = 0; b < batch; ++b) rows += window_of(positions[b], full, window, ring_capacity).rows;
   if ((int64_t)n_kv * rows >= kDeepRows)
     return launch_ns<CT, CacheT<CT>::kDeep, kConsumers, CacheT<CT>::kDeepBlocks>(
         q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale, positions, batch, a, part,
-        counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+        counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
   return launch_ns<CT, CacheT<CT>::kShallow, kConsumers, 1>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
                                        scale, positions, batch, a, part, counters, err, n_ctas,
-                                       l2_pf, l2_pf_bytes, st);
+                                       l2_pf, l2_pf_bytes, chunk, st);
 }
 
 }  // namespace
@@ -372,12 +418,56 @@ cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, con
                              int n_kv, int64_t capacity, int ring_capacity, bool full,
                              int window, float scale, const int32_t* positions, int batch,
                              float* a, float* part, uint32_t* counters, uint32_t* err,
-                             int n_ctas, const void* l2_pf, size_t l2_pf_bytes, cudaStream_t st) {
+                             int n_ctas, const void* l2_pf, size_t l2_pf_bytes, cudaStream_t st,
+                             const ChunkSrc& chunk) {
   if (cdtype == SPARK_BF16)
     return launch_ct<__nv_bfloat16>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
-                                    scale, positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+                                    scale, positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
   return launch_ct<float>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                          positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, st);
+                          positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
+}
+
+namespace {
+
+// Copy the staged k / v rows of a chunk of tokens into their cache slots,
+// once attention has read them: token t of the chunk goes to the slot of
+// position p0 + t.  On a ring only the last `ring` tokens are copied (an
+// earlier token's slot is taken by a later token of the same chunk).  One
+// CTA per copied token.
+template <typename CT>
+__global__ void __launch_bounds__(256)
+    k_commit_rows(const CT* __restrict__ ks, const CT* __restrict__ vs, CT* kc, CT* vc, int row_elems,
+                  int64_t p0, int first, int ring) {
+  pdl_wait();  // attention has finished reading the slots these rows replace
+  pdl_trigger();
+  const int t = first + blockIdx.x;
+  const int64_t pos = p0 + t;
+  const int64_t slot = ring > 0 ? pos % ring : pos;
+  const int vec = (int)(row_elems * sizeof(CT) / 16);
+  const uint4* sk = reinterpret_cast<const uint4*>(ks + (int64_t)t * row_elems);
+  const uint4* sv = reinterpret_cast<const uint4*>(vs + (int64_t)t * row_elems);
+  uint4* dk = reinterpret_cast<uint4*>(kc + slot * row_elems);
+  uint4* dv = reinterpret_cast<uint4*>(vc + slot * row_elems);
+  for (int i = threadIdx.x; i < vec; i += blockDim.x) {
+    dk[i] = __ldcg(sk + i);
+    dv[i] = __ldcg(sv + i);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_commit_rows(int cdtype, const void* ks, const void* vs, void* kc, void* vc,
+                               int n_kv, int64_t p0, int m, int ring_capacity, cudaStream_t st) {
+  const int first = ring_capacity > 0 && m > ring_capacity ? m - ring_capacity : 0;
+  const int row_elems = n_kv * kHeadDim;
+  if (cdtype == SPARK_BF16)
+    return launch_pdl(k_commit_rows<__nv_bfloat16>, dim3(m - first), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(ks), static_cast<const __nv_bfloat16*>(vs),
+                      static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), row_elems, p0,
+                      first, ring_capacity);
+  return launch_pdl(k_commit_rows<float>, dim3(m - first), dim3(256), 0, st, static_cast<const float*>(ks),
+                    static_cast<const float*>(vs), static_cast<float*>(kc), static_cast<float*>(vc),
+                    row_elems, p0, first, ring_capacity);
 }
 
 }  // namespace spark

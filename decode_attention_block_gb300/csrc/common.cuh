@@ -86,6 +86,7 @@ struct WsLayout {
   size_t mcs = 0;       // f32x2 [batch][head_dim / 2] rope (cos, sin) of each sequence
   size_t mpart = 0;     // f32 [kMmaMaxCtas][kMmaTileRows][min(batch, kMmaMaxSeq) rounded to 8]
   size_t mtick = 0;     // uint32 [kMmaMaxCtas] split-K tickets of the projection tiles
+  size_t stage = 0;     // [2][batch][n_kv][head_dim] in the cache type (room for f32): a chunk's k, v rows
   size_t trace = 0;     // u64 [kTraceWords] phase timestamps of the persistent kernel (opt-in)
   size_t total = 0;
 };
@@ -121,6 +122,8 @@ inline WsLayout ws_layout(int hidden, int n_q, int n_kv, int batch) {
   off = align_up(off + sizeof(float) * (size_t)kMmaMaxCtas * kMmaTileRows * bpad, 256);
   L.mtick = off;
   off = align_up(off + sizeof(uint32_t) * kMmaMaxCtas, 256);
+  L.stage = off;
+  off = align_up(off + sizeof(float) * 2 * (size_t)batch * n_kv * kHeadDim, 256);
   L.trace = off;
   off = align_up(off + sizeof(uint64_t) * kTraceWords, 256);
   L.total = off;

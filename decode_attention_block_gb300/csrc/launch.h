@@ -18,13 +18,28 @@ cudaError_t launch_oproj(int wdtype, const float* a, const float* g, const float
                          const void* o_w, float* out, uint32_t* err, int hidden, int n_q, int batch,
                          cudaStream_t st);
 
-// Split-K GQA decode attention with the log-sum-exp merge.
+// The rows a chunk of consecutive tokens of one sequence produces, staged
+// ([tokens][n_kv][head_dim] in the cache type) until attention has run.
+// p0 < 0: a decode step (no chunk).
+struct ChunkSrc {
+  int64_t p0 = -1;
+  const void* k = nullptr;
+  const void* v = nullptr;
+};
+
+// Split-K GQA decode attention with the log-sum-exp merge.  With a chunk,
+// `positions` are the tokens' positions, the cache is one sequence's, and
+// rows at positions >= chunk.p0 come from the staged rows.
 cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, const void* vc,
                              int n_kv, int64_t capacity, int ring_capacity, bool full,
                              int window, float scale, const int32_t* positions, int batch,
                              float* a, float* part, uint32_t* counters, uint32_t* err,
                              int n_ctas, const void* l2_prefetch, size_t l2_prefetch_bytes,
-                             cudaStream_t st);
+                             cudaStream_t st, const ChunkSrc& chunk = ChunkSrc());
+
+// Copy a chunk's staged rows into their cache slots (after attention).
+cudaError_t launch_commit_rows(int cdtype, const void* ks, const void* vs, void* kc, void* vc,
+                               int n_kv, int64_t p0, int m, int ring_capacity, cudaStream_t st);
 
 // The two projections for a batch on the tensor cores (mma.cu): same results
 // as launch_qkv_rope / launch_oproj, for bf16 weights.

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define SPARK_ATTN_ABI_VERSION 2
+#define SPARK_ATTN_ABI_VERSION 3
 /* largest batch one call accepts */
 #define SPARK_MAX_BATCH 1024
 
@@ -159,6 +159,28 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
                       const spark_kv_layer* kv, int32_t layer_class,
                       const int32_t* positions, int32_t batch, float* out,
                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* A chunk of m consecutive tokens of ONE sequence through one layer, at
+ * positions p0 .. p0+m-1: prefill, or verifying drafted tokens.  The result
+ * is that of m calls of spark_attn_decode in position order (kv_write.rs,
+ * module doc: chunked prefill reuses the per-token attention block, only the
+ * K/V projections being batched): token t attends, causally, to the rows of
+ * the tokens before it in the chunk and to the history inside its window,
+ * even where a ring wraps inside the chunk (its k and v are staged in the
+ * workspace and reach the cache only after attention).  The projections of
+ * the m tokens run as one batch (tensor cores for m > 4, bf16 weights).
+ *   h     [m][hidden] fp32 device; out [m][hidden], may equal h.
+ *   kv    the sequence's cache: [1][capacity][n_kv][head_dim].  Rows
+ *         slot(p0+t) receive the tokens' k and v (on a ring with m > its
+ *         capacity, the last `capacity` tokens' rows).
+ *   p0    position of the first token (>= 0); a linear cache needs
+ *         p0 + m <= capacity.
+ *   m     1 .. SPARK_MAX_BATCH.
+ *   workspace  >= spark_attn_workspace_bytes(g, m), as for spark_attn_decode.
+ * Errors as spark_attn_decode. */
+int spark_attn_prefill(const spark_geom* g, const float* h, const spark_layer_weights* w,
+                       const spark_kv_layer* kv, int32_t layer_class, int32_t p0, int32_t m,
+                       float* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* One decode step through a stack of n_layers attention blocks (mod.rs's
  * layer loop with the MLP left out: the output of layer l is the input of

@@ -537,3 +537,79 @@ def test_stack_more_layers_than_one_launch(B):
     wl = synth.Workload("stack45", "", "bf16", [600],
                         [synth.LayerSpec(i % 4 == 3, 0 if i % 4 == 3 else 512) for i in range(45)], seed=623)
     run_stack_parity(B, wl)
+
+
+# ---------------------------------------------------------------------------
+# a chunk of consecutive tokens of one sequence (prefill / verify)
+# ---------------------------------------------------------------------------
+
+PREFILL_CASES = [
+    # id, is_full, ring, capacity, p0, m, dtype
+    ("full_p0_m1", True, 0, 64, 0, 1, "bf16"),
+    ("full_p0_m7", True, 0, 64, 0, 7, "bf16"),
+    ("full_p700_m3", True, 0, 800, 700, 3, "bf16"),
+    ("full_p700_m37", True, 0, 800, 700, 37, "bf16"),
+    ("full_p100_m130", True, 0, 300, 100, 130, "bf16"),
+    ("sliding_ring_fills_inside", False, 512, 512, 490, 45, "bf16"),
+    ("sliding_ring_wraps_inside", False, 512, 512, 1000, 100, "bf16"),
+    ("sliding_ring_outgrown", False, 512, 512, 300, 600, "bf16"),
+    ("sliding_f32", False, 512, 512, 40, 3, "f32"),
+    ("sliding_linear", False, 0, 2048, 1500, 20, "bf16"),
+]
+
+
+def _prefill_inputs(is_full, ring, cap, p0, m, dtype, seed):
+    wl = synth.Workload("t", "", dtype, [p0], [synth.LayerSpec(is_full, ring)], seed=seed)
+    w = synth.make_weights(wl, 0, "cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    kc = torch.randn((1, cap, N_KV, D), generator=_gen(seed + 1), device="cuda").to(tdt)
+    vc = torch.randn((1, cap, N_KV, D), generator=_gen(seed + 2), device="cuda").to(tdt)
+    h = torch.randn((m, 2560), generator=_gen(seed + 3), device="cuda")
+    return wl, w, kc, vc, h
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_prefill_chunk_matches_oracle(B, case):
+    _, is_full, ring, cap, p0, m, dtype = case
+    wl, w, kc, vc, h = _prefill_inputs(is_full, ring, cap, p0, m, dtype, 900 + m)
+    kc0, vc0 = kc.clone(), vc.clone()
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, m)
+    out = torch.empty_like(h)
+    B.spark_attn_prefill(geom, h, B.LayerWeights(**w), B.KvLayer(kc, vc, ring),
+                         B.SPARK_FULL if is_full else B.SPARK_SLIDING, p0, out, ws)
+    torch.cuda.synchronize()
+    assert B.spark_attn_error_word(ws) == 0
+    res = oracle.prefill_chunk(oracle_geom(wl), synth.to_numpy(h).astype(np.float64), np_weights(w),
+                               synth.to_numpy(kc0[0]), synth.to_numpy(vc0[0]), is_full, p0, ring)
+    got_o = out.cpu().numpy().astype(np.float64) - h.cpu().numpy().astype(np.float64)
+    for t in range(m):
+        assert_close(got_o[t], res["o"][t], f"token {t} (position {p0 + t}) o")
+    # the cache afterwards: exactly the oracle's rows changed, to the same values
+    want_k, want_v = res["k_cache"], res["v_cache"]
+    changed = np.any((want_k != synth.to_numpy(kc0[0])).reshape(cap, -1), axis=1) | \
+        np.any((want_v != synth.to_numpy(vc0[0])).reshape(cap, -1), axis=1)
+    got_k, got_v = synth.to_numpy(kc[0]), synth.to_numpy(vc[0])
+    for slot in range(cap):
+        if changed[slot]:
+            assert_close(f64(got_k[slot]), f64(want_k[slot]), f"k slot {slot}")
+            assert_close(f64(got_v[slot]), f64(want_v[slot]), f"v slot {slot}")
+        else:
+            assert np.array_equal(got_k[slot], want_k[slot]), f"k slot {slot} changed"
+            assert np.array_equal(got_v[slot], want_v[slot]), f"v slot {slot} changed"
+    assert int(changed.sum()) == (min(m, ring) if ring > 0 else m)
+
+
+def test_prefill_one_token_agrees_with_decode(B):
+    """A chunk of one token is a decode step."""
+    wl, w, kc, vc, h = _prefill_inputs(False, 512, 512, 700, 1, "bf16", 950)
+    kc2, vc2 = kc.clone(), vc.clone()
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, 1)
+    out1, out2 = torch.empty_like(h), torch.empty_like(h)
+    B.spark_attn_prefill(geom, h, B.LayerWeights(**w), B.KvLayer(kc, vc, 512), B.SPARK_SLIDING, 700, out1, ws)
+    B.spark_attn_decode(geom, h, B.LayerWeights(**w), B.KvLayer(kc2, vc2, 512), B.SPARK_SLIDING, [700], out2, ws)
+    torch.cuda.synchronize()
+    ma, rel = err_stats(out1.cpu().numpy() - h.cpu().numpy(), out2.cpu().numpy() - h.cpu().numpy())
+    assert ma < 1e-4 and rel < 1e-5, (ma, rel)
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported_and_bound(B):
 
 
 def test_abi_version_and_status_strings(B):
-    assert B.spark_attn_abi_version() == 2
+    assert B.spark_attn_abi_version() == 3
     for code in range(-7, 1):
         s = B.spark_attn_status_string(code)
         assert s and s != "unknown status"
@@ -184,3 +184,24 @@ def test_workspace_grows_with_the_tensor_core_batch(B):
     g = B.spark_geom_default()
     small, b8, b64, b128, b1024 = (B.spark_attn_workspace_bytes(g, b) for b in (1, 8, 64, 128, 1024))
     assert small < b8 < b64 < b128 < b1024
+
+
+def _prefill(B, p0=5, m=3, cls=1, kv=None, ws_bytes=None):
+    lib = B.load()
+    g = B.spark_geom_default()
+    w = B.SparkLayerWeights(FAKE, FAKE, FAKE, FAKE, B.SPARK_BF16)
+    k = kv or B.SparkKvLayer(FAKE, FAKE, 1024, 0, B.SPARK_BF16)
+    need = B.spark_attn_workspace_bytes(g, max(1, min(m, 1024))) if ws_bytes is None else ws_bytes
+    return lib.spark_attn_prefill(ctypes.byref(g), FAKE, ctypes.byref(w), ctypes.byref(k), cls, p0, m, FAKE,
+                                  FAKE, need or (1 << 30), None)
+
+
+def test_prefill_arguments_are_validated(B):
+    assert _prefill(B, m=0) == -1
+    assert _prefill(B, m=1025) == -1
+    assert _prefill(B, p0=-1) == -2
+    assert _prefill(B, p0=1020, m=5) == -2                # a linear cache of 1024 rows ends at 1023
+    ring = B.SparkKvLayer(FAKE, FAKE, 512, 512, B.SPARK_BF16)
+    assert _prefill(B, p0=1 << 20, m=600, cls=0, kv=ring, ws_bytes=16) == -4   # any position on a ring
+    assert _prefill(B, cls=1, kv=ring) == -3              # a full layer has no ring
+    assert _prefill(B, ws_bytes=64) == -4
