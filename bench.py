@@ -490,6 +490,86 @@ def bench_reference(args, wl, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def bench_prefill(args, wl):
+    """`--prefill M`: chunks of M consecutive tokens of the workload's one
+    sequence, starting at its decode position, through every layer of the
+    workload (spark_attn_prefill per layer, each layer's output feeding the
+    next).  Reports tokens/s, the HBM bytes a chunk must move (each layer's
+    weights and its distinct KV rows read or written, once) and the FLOPs
+    of its projections and attention."""
+    from decode_attention_block_gb300 import binding as B
+
+    if wl.batch != 1:
+        raise SystemExit("--prefill takes a one-sequence workload")
+    M, p0 = int(args.prefill), int(wl.positions[0])
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    build_lib.build()
+    B.load()
+    geom = B.spark_geom_default()
+    layers, kv_bytes, att_flops = [], 0, 0
+    for li, spec in enumerate(wl.layers):
+        w = B.LayerWeights(**synth.make_weights(wl, li, device))
+        cap = spec.ring_capacity if spec.ring_capacity > 0 else p0 + M
+        gen = torch.Generator(device=device)
+        gen.manual_seed(wl.seed * 31 + li)
+        dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        k = torch.randn((1, cap, wl.n_kv, wl.head_dim), generator=gen, device=device).to(dt)
+        v = torch.randn((1, cap, wl.n_kv, wl.head_dim), generator=gen, device=device).to(dt)
+        layers.append((spec, w, B.KvLayer(k, v, spec.ring_capacity)))
+        first = 0 if spec.is_full else max(0, p0 + 1 - wl.window)
+        row_bytes = 2 * wl.n_kv * wl.head_dim * (2 if wl.dtype == "bf16" else 4)
+        kv_bytes += (p0 + M - first) * row_bytes + M * row_bytes   # distinct rows read + rows written
+        for t in range(M):
+            lo = 0 if spec.is_full else max(0, p0 + t + 1 - wl.window)
+            att_flops += (p0 + t + 1 - lo) * wl.n_q * wl.head_dim * 4
+    nbytes = wl.weight_bytes_per_layer() * len(wl.layers) + kv_bytes
+    proj_flops = 2 * M * ((wl.n_q + 2 * wl.n_kv) * wl.head_dim * wl.hidden + wl.n_q * wl.hidden
+                          + wl.hidden * wl.n_q * wl.head_dim) * len(wl.layers)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed * 7 + 5)
+    h = torch.randn((M, wl.hidden), generator=gen, device=device)
+    bufs = [torch.empty_like(h), torch.empty_like(h)]
+    ws = B.make_workspace(geom, M, device)
+    stream = torch.cuda.current_stream(device)
+
+    def chunk():
+        cur = h
+        for i, (spec, w, kv) in enumerate(layers):
+            out = bufs[i % 2]
+            B.spark_attn_prefill(geom, cur, w, kv, B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING, p0,
+                                 out, ws, stream)
+            cur = out
+
+    for _ in range(args.warmup):
+        chunk()
+    torch.cuda.synchronize()
+    steps = args.steps or 50
+    sampler = ClockSampler(0)
+    with sampler:
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            chunk()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    assert B.spark_attn_error_word(ws) == 0
+    ms = e0.elapsed_time(e1) / steps
+    peaks = measured_peaks()
+    return {"metric": f"prefill tokens/s (chunks of {M} consecutive tokens of one sequence)",
+            "value": round(M / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": f"{wl.name}, prefill chunk of {M} from position {p0}", "chunk": M,
+                       "p0": p0, "layers": ["full" if s_.is_full else "sliding" for s_ in wl.layers]},
+            "hbm_bytes_per_step": nbytes, "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "flops_per_step": proj_flops + att_flops,
+            "tflops": round((proj_flops + att_flops) / (ms * 1e-3) / 1e12, 2),
+            "clocks": sampler.summary()}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -502,6 +582,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch steps directly instead of graph replay")
     ap.add_argument("--path", default="layers", choices=["stack", "layers"],
                     help="one call per layer (default, the faster path measured) or the whole step in one call")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="time chunks of this many consecutive tokens (spark_attn_prefill) instead of decode")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, local, world = dist_env()
@@ -511,6 +593,10 @@ def main():
         line = bench_reference(args, wl, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+
+    if args.prefill > 0:
+        print(json.dumps(bench_prefill(args, wl)), flush=True)
         return
 
     dist_init(world, "nccl")
