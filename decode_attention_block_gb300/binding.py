@@ -101,6 +101,7 @@ _SIGNATURES = {
     "spark_dbg_gate_oproj": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, _P, _P,
                                             ctypes.POINTER(SparkLayerWeights), ctypes.c_int32, _P,
                                             ctypes.c_int32, _P, ctypes.c_size_t, _P]),
+    "spark_dbg_wait_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint64, _P]),
     "spark_attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "spark_attn_abi_version": (ctypes.c_int32, []),
 }
@@ -323,6 +324,12 @@ def spark_dbg_gate_oproj(geom: SparkGeom, a: torch.Tensor, g_logits: torch.Tenso
                                        _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
                                        _stream(stream)),
            "spark_dbg_gate_oproj")
+
+
+def spark_dbg_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
+    """Run a bounded wait that nothing satisfies (see the header)."""
+    _check(load().spark_dbg_wait_timeout(_dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                         int(limit_ns), _stream(stream)), "spark_dbg_wait_timeout")
 
 
 def spark_attn_status_string(status: int) -> str:

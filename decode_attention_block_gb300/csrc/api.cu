@@ -46,6 +46,24 @@ EncodeTiledFn tensor_map_encoder() {
   return fn;
 }
 
+namespace {
+
+// One thread waits, with the same bounded wait every pipeline uses, for an
+// mbarrier phase nothing completes; when the limit passes it raises the
+// wait-timeout bit of the error word and the kernel returns.
+__global__ void k_wait_timeout(uint32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0, &abort_flag, limit_ns)) atomicOr(err, kErrWaitTimeout);
+  }
+}
+
+}  // namespace
+
 }  // namespace spark
 
 using namespace spark;
@@ -283,6 +301,14 @@ int spark_attn_prefill(const spark_geom* g, const float* h, const spark_layer_we
     e = run_oproj(pick_path(SPARK_PATH_AUTO, w->dtype, g, 0, m), g, a, g_logits, h, w, m, out, err,
                   workspace, L, st);
   return cuda_status(e);
+}
+
+int spark_dbg_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t limit_ns, void* stream) {
+  if (!workspace || workspace_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return SPARK_ERR_WORKSPACE;
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return SPARK_ERR_INVALID_ARG;
+  k_wait_timeout<<<1, 32, 0, (cudaStream_t)stream>>>(static_cast<uint32_t*>(workspace), limit_ns);
+  return cuda_status(cudaGetLastError());
 }
 
 const char* spark_attn_status_string(int status) {

@@ -273,6 +273,13 @@ int spark_dbg_gate_oproj(const spark_geom* g, const float* a, const float* g_log
                          float* out, int32_t path, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* The failure path of the kernels' bounded waits, on purpose: one thread
+ * waits for an mbarrier phase that nothing completes, gives up after
+ * limit_ns (1 .. 2e9), sets bit 1 of the workspace error word and returns,
+ * leaving the context usable.  For tests of the error reporting; the pages
+ * have no counterpart. */
+int spark_dbg_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t limit_ns, void* stream);
+
 /* Human-readable text of a status code (static storage). */
 const char* spark_attn_status_string(int status);
 

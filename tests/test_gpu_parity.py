@@ -613,3 +613,31 @@ def test_prefill_one_token_agrees_with_decode(B):
     ma, rel = err_stats(out1.cpu().numpy() - h.cpu().numpy(), out2.cpu().numpy() - h.cpu().numpy())
     assert ma < 1e-4 and rel < 1e-5, (ma, rel)
     assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+
+
+# ---------------------------------------------------------------------------
+# error reporting of the bounded waits
+# ---------------------------------------------------------------------------
+
+def test_a_wait_that_runs_out_reports_and_leaves_the_gpu_usable(B):
+    """A wait on a phase nothing completes gives up after its limit, raises
+    the wait-timeout bit of the error word, and the next call works."""
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, 1)
+    assert B.spark_attn_error_word(ws) == 0
+    B.spark_dbg_wait_timeout(ws, 2_000_000)          # 2 ms
+    torch.cuda.synchronize()
+    assert B.spark_attn_error_word(ws) == 1          # bit 1: a wait ran out; reading clears it
+    assert B.spark_attn_error_word(ws) == 0
+    # the context is intact: an attention call right after is correct
+    positions = [40]
+    wl = synth.Workload("t", "", "bf16", positions, [synth.LayerSpec(True)], seed=960)
+    kc, vc = synth.make_cache(wl, 0, "cuda")
+    q = torch.randn((1, Q_DIM), generator=_gen(961), device="cuda")
+    a = torch.empty((1, Q_DIM), device="cuda")
+    B.spark_dbg_attention(geom, q, B.KvLayer(kc, vc, 0), B.SPARK_FULL, positions, a, ws)
+    torch.cuda.synchronize()
+    assert B.spark_attn_error_word(ws) == 0
+    want = _attention_oracle(q.cpu().numpy().astype(np.float64), synth.to_numpy(kc), synth.to_numpy(vc),
+                             positions, True, 0)
+    assert_close(a.cpu().numpy(), want, "attention after a timed-out wait")

@@ -205,3 +205,11 @@ def test_prefill_arguments_are_validated(B):
     assert _prefill(B, p0=1 << 20, m=600, cls=0, kv=ring, ws_bytes=16) == -4   # any position on a ring
     assert _prefill(B, cls=1, kv=ring) == -3              # a full layer has no ring
     assert _prefill(B, ws_bytes=64) == -4
+
+
+def test_wait_timeout_arguments_are_validated(B):
+    lib = B.load()
+    assert lib.spark_dbg_wait_timeout(FAKE, 4096, 0, None) == -1
+    assert lib.spark_dbg_wait_timeout(FAKE, 4096, 3_000_000_000, None) == -1
+    assert lib.spark_dbg_wait_timeout(FAKE + 16, 4096, 1000, None) == -4
+    assert lib.spark_dbg_wait_timeout(0, 4096, 1000, None) == -4
