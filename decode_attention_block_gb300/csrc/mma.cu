@@ -143,12 +143,14 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }
 
-template <typename CT>
-__device__ __forceinline__ CT to_cache(float v);
-template <>
-__device__ __forceinline__ float to_cache<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 to_cache<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+// four consecutive cache elements in one store (8 bytes bf16, 16 bytes fp32)
+__device__ __forceinline__ void store_cache4(float* dst, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store_cache4(__nv_bfloat16* dst, const float (&v)[4]) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
 
 // x -> (hi, lo) in bf16 with x ~= hi + lo
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
@@ -296,7 +298,7 @@ struct MmaParams {
 
 // Stamps of the opt-in timeline (SPARK_TRACE_MMA): per CTA, in this order.
 enum { kTrStart, kTrXIssued, kTrFirstFull, kTrLastFull, kTrDone, kTrTicket, kTrReduced, kTrEnd,
-       kTraceEvents };
+       kTrStaged, kTrStored, kTraceEvents };
 
 __device__ __forceinline__ void stamp(const MmaParams& p, int ev) {
   if (p.trace) p.trace[(size_t)blockIdx.x * kTraceEvents + ev] = global_timer_ns();
@@ -417,52 +419,99 @@ __device__ __forceinline__ void epilogue_qkv(const MmaParams& p, const MmaSeq& s
     }
   }
   named_bar_sync(kBarEpi, kEpiThreads);
-  int d;  // dim within the 256-row head this tile row belongs to
-  if (halves)
-    d = m < kBoxRows ? kBoxRows * sel + m : 2 * kBoxRows + kBoxRows * sel + (m - kBoxRows);
-  else
-    d = kMmaTileRows * sel + m;
-  const int R = kHeadDim * unit + d;
-  const int q_dim = p.n_q * kHeadDim;
-  int kind, head;
-  if (unit < p.n_q) {
-    kind = 0;
-    head = unit;
-  } else if (unit < p.n_q + p.n_kv) {
-    kind = 1;
-    head = unit - p.n_q;
-  } else {
-    kind = 2;
-    head = unit - p.n_q - p.n_kv;
-  }
+  if (et == 0) stamp(p, kTrStaged);
+  // A thread owns rows m4 .. m4 + 3 of the tile (one 64-row box never splits
+  // them) for sequences b_first, b_first + 4, ...: it reads its four values
+  // and their rope partners from Y and writes them with one vector store.
+  const int m4 = 4 * (et & 31), b_first = et >> 5;
+  int dd[4], pp[4], mm[4];
+  float sg[4];
+  bool rr[4];
+  int kind = 0, head = 0, R0 = 0;
   const int hr = p.rotary_dim >> 1;
-  const bool rot = kind != 2 && d < p.rotary_dim;
-  int mp = m, pair = 0;
-  float sgn = 0.f;
-  if (rot) {
-    if (d < hr) {
-      pair = d;
-      sgn = -1.f;
-      mp = halves ? m + kBoxRows : m + hr;
-    } else {
-      pair = d - hr;
-      sgn = 1.f;
-      mp = halves ? m - kBoxRows : m - hr;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m_ = m4 + i;
+    const int d = halves ? (m_ < kBoxRows ? kBoxRows * sel + m_ : 2 * kBoxRows + kBoxRows * sel + (m_ - kBoxRows))
+                         : kMmaTileRows * sel + m_;
+    if (i == 0) {
+      R0 = kHeadDim * unit + d;
+      if (unit < p.n_q) {
+        kind = 0;
+        head = unit;
+      } else if (unit < p.n_q + p.n_kv) {
+        kind = 1;
+        head = unit - p.n_q;
+      } else {
+        kind = 2;
+        head = unit - p.n_q - p.n_kv;
+      }
+    }
+    dd[i] = d;
+    rr[i] = kind != 2 && d < p.rotary_dim;
+    mm[i] = m_;
+    pp[i] = 0;
+    sg[i] = 0.f;
+    if (rr[i]) {
+      if (d < hr) {
+        pp[i] = d;
+        sg[i] = -1.f;
+        mm[i] = halves ? m_ + kBoxRows : m_ + hr;
+      } else {
+        pp[i] = d - hr;
+        sg[i] = 1.f;
+        mm[i] = halves ? m_ - kBoxRows : m_ - hr;
+      }
+      pp[i] -= p0;  // pair within the staged table
     }
   }
-  const int pl = pair - p0;  // pair within the staged table
+  const int q_dim = p.n_q * kHeadDim;
   CT* cache = static_cast<CT*>(kind == 1 ? p.kc : p.vc);
-  for (int b = 0; b < p.nb; ++b) {
-    float v = Y[b * kMmaTileRows + m];
-    if (rot) {
-      const float2 c = CS[b * kBoxRows + pl];
-      v = fmaf(sgn * Y[b * kMmaTileRows + mp], c.y, v * c.x);
+  // the four rows usually rotate alike with consecutive partners and pairs:
+  // then they are read as float4 (scalar reads at stride 4 conflict 4-way)
+  bool vec = true;
+#pragma unroll
+  for (int i = 1; i < 4; ++i)
+    vec = vec && rr[i] == rr[0] && sg[i] == sg[0] && mm[i] == mm[0] + i && pp[i] == pp[0] + i;
+  vec = vec && (mm[0] & 3) == 0 && (pp[0] & 1) == 0;
+  for (int b = b_first; b < p.nb; b += 4) {
+    float val[4];
+    if (vec) {
+      const float4 y = *reinterpret_cast<const float4*>(Y + b * kMmaTileRows + m4);
+      if (rr[0]) {
+        const float4 yp = *reinterpret_cast<const float4*>(Y + b * kMmaTileRows + mm[0]);
+        const float4 c01 = *reinterpret_cast<const float4*>(CS + b * kBoxRows + pp[0]);
+        const float4 c23 = *reinterpret_cast<const float4*>(CS + b * kBoxRows + pp[0] + 2);
+        val[0] = fmaf(sg[0] * yp.x, c01.y, y.x * c01.x);
+        val[1] = fmaf(sg[0] * yp.y, c01.w, y.y * c01.z);
+        val[2] = fmaf(sg[0] * yp.z, c23.y, y.z * c23.x);
+        val[3] = fmaf(sg[0] * yp.w, c23.w, y.w * c23.z);
+      } else {
+        val[0] = y.x;
+        val[1] = y.y;
+        val[2] = y.z;
+        val[3] = y.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float v = Y[b * kMmaTileRows + m4 + i];
+        if (rr[i]) {
+          const float2 c = CS[b * kBoxRows + pp[i]];
+          val[i] = fmaf(sg[i] * Y[b * kMmaTileRows + mm[i]], c.y, v * c.x);
+        } else {
+          val[i] = v;
+        }
+      }
     }
-    if (kind == 0)
-      p.q_rot[(size_t)b * q_dim + R] = v;
-    else
-      cache[(((size_t)b * p.capacity + seq.slot[b]) * p.n_kv + head) * kHeadDim + d] = to_cache<CT>(v);
+    if (kind == 0) {
+      *reinterpret_cast<float4*>(p.q_rot + (size_t)b * q_dim + R0) = make_float4(val[0], val[1], val[2], val[3]);
+    } else {
+      CT* dst = cache + (((size_t)b * p.capacity + seq.slot[b]) * p.n_kv + head) * kHeadDim + dd[0];
+      store_cache4(dst, val);
+    }
   }
+  if (et == 0) stamp(p, kTrStored);
 }
 
 template <int E, typename CT>
