@@ -71,6 +71,12 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def job_tokens_per_s(batch: int, world: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank decodes `steps` steps of its own
+    `batch` sequences (weak scaling), timed by the slowest rank."""
+    return batch * world * steps / (ms_max * 1e-3)
+
+
 # ---------------------------------------------------------------------------
 # bytes and peaks
 # ---------------------------------------------------------------------------
@@ -381,7 +387,7 @@ def bench_ours(args, wl, rank, local, world):
         raise RuntimeError(f"device error word {err:#x}")
 
     tokens = wl.batch * world
-    value = tokens * steps / (ms_total * 1e-3)
+    value = job_tokens_per_s(wl.batch, world, steps, ms_total)
     gbs = sb["total"] / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC,
