@@ -25,6 +25,9 @@
 // lane owning 8 of the 256 output dims.  At the end of a group the four warps'
 // states are merged through shared memory.
 #include <math.h>
+#include <stdlib.h>
+
+#include <algorithm>
 
 #include <type_traits>
 
@@ -35,7 +38,9 @@ namespace spark {
 namespace {
 
 constexpr int kMinRowsPerCta = 64;            // default grid: at least this many rows per CTA
-constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from which the deep ring pays
+constexpr int64_t kDeepRows = 1 << 16;
+constexpr int kMaxCluster = 8;                // CTAs per group in cluster mode
+constexpr int kClusterRowsPerCta = 96;        // cluster mode: about this many rows per CTA        // rows (x KV heads) per call from which the deep ring pays
 
 template <typename CT, int NS, int NC>
 struct Smem {
@@ -50,7 +55,8 @@ struct Smem {
   static constexpr int kL = kM + NC * 4 * 4;
   static constexpr int kO = kL + NC * 4 * 4;
   static constexpr int kBars = kO + NC * 4 * kHeadDim * 4;
-  static constexpr int kFlags = kBars + 2 * kStages * 8;
+  static constexpr int kCst = kBars + 2 * kStages * 8;       // cluster mode: the CTA's state
+  static constexpr int kFlags = kCst + (8 + 4 * kHeadDim) * 4;
   static constexpr int kBytes = kFlags + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 (128B swizzle)
 };
@@ -113,7 +119,7 @@ template <typename CT, int NS, int NC, int MINB, int MAXB>
 __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     k_attn_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
-                  int64_t chunk_p0, const float* __restrict__ q_rot, float* __restrict__ a_out,
+                  int64_t chunk_p0, int cl, const float* __restrict__ q_rot, float* __restrict__ a_out,
                   float* __restrict__ part, uint32_t* __restrict__ counters, uint32_t* err,
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
@@ -166,17 +172,29 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   // wait.
   const int64_t total = (int64_t)n_kv * args.prefix[batch];
   const int G = gridDim.x, c = blockIdx.x;
-  const int64_t f0 = total * c / G, f1 = total * (c + 1) / G;
-  if (f0 >= f1) return;
+  int64_t f0, f1;
+  if (cl > 0) {
+    // cluster mode: the cl CTAs of a cluster split one group's rows evenly
+    // (a CTA may get none) and merge through DSMEM
+    const int g = c / cl, r = c % cl, b = g / n_kv, j = g % n_kv;
+    const int64_t rows_g = args.prefix[b + 1] - args.prefix[b];
+    const int64_t gs = (int64_t)n_kv * args.prefix[b] + j * rows_g;
+    f0 = gs + rows_g * r / cl;
+    f1 = gs + rows_g * (r + 1) / cl;
+  } else {
+    f0 = total * c / G;
+    f1 = total * (c + 1) / G;
+    if (f0 >= f1) return;
+  }
   const int32_t* pos = args.pos;
+  float* cst = reinterpret_cast<float*>(base + S::kCst);  // [4] m, [4] l, [4][256] o
 
   // ------------------------------------------------------------ producer
   if (warp == NC) {
-    if (lane != 0) {
+   if (lane != 0) {
       pdl_wait();
       pdl_trigger();
-      return;
-    }
+   } else {
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     if (chunk_p0 >= 0) {
@@ -236,9 +254,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       pdl_wait();
       pdl_trigger();
     }
-    return;
-  }
-
+   }
+    __syncwarp();
+    if (cl == 0) return;
+  } else {
   // ------------------------------------------------------------ consumers
   // bf16 caches take the tensor-core tile, fp32 caches the CUDA-core one
   constexpr bool kMma = std::is_same<CT, __nv_bfloat16>::value;
@@ -249,6 +268,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   AttnState st;
   MmaQ mq;
   MmaState mst;
+  if (f0 >= f1) {  // cluster mode, no rows: an empty state
+    pdl_wait();
+    pdl_trigger();
+    if (tid < kGroup) {
+      cst[tid] = -INFINITY;
+      cst[4 + tid] = 0.f;
+    }
+    for (int i = tid; i < kGroup * kHeadDim; i += kCT) cst[8 + i] = 0.f;
+  }
   while (sh.f < sh.f1) {
     const int b = sh.b, j = sh.j;
     const int64_t rows = args.prefix[b + 1] - args.prefix[b];
@@ -307,9 +335,24 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       attn_store_state_mma(mst, msm);
     else
       attn_store_state(st, msm);
-    attn_merge_group<NC>(msm, flags, part, counters, a_head0, g, c, c_first, c_last - c_first + 1);
+    if (cl > 0)
+      attn_cta_state<NC>(msm, cst);
+    else
+      attn_merge_group<NC>(msm, flags, part, counters, a_head0, g, c, c_first, c_last - c_first + 1);
     sh.f = gs + r1;
     if (++sh.j == n_kv) { sh.j = 0; ++sh.b; }
+  }
+  }  // consumers
+
+  if (cl > 0) {
+    // every thread of the cluster: the CTA states are complete, rank 0
+    // merges them into the output, and no CTA leaves before it has
+    cluster_sync_all();
+    if (c % cl == 0 && warp < kGroup) {
+      const int g = c / cl, b = g / n_kv, j = g % n_kv;
+      attn_cluster_merge(cst, cl, a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, flags);
+    }
+    cluster_sync_all();
   }
 }
 
@@ -347,8 +390,18 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
     args.pos[b] = b < batch ? positions[b] : 0;
   }
   const int64_t total = (int64_t)n_kv * args.prefix[batch];
-  int G = n_ctas;
-  if (G <= 0) {
+  // Short histories in small launches: one cluster of cl CTAs per group,
+  // merging through DSMEM (no partials in the workspace, no ticket).
+  int64_t max_rows = 0;
+  for (int b = 0; b < batch; ++b) max_rows = std::max(max_rows, args.prefix[b + 1] - args.prefix[b]);
+  const int groups = batch * n_kv;
+  int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
+  if (cl > kMaxCluster) cl = kMaxCluster;
+  if (n_ctas > 0 || cl < 2 || max_rows > (int64_t)kMaxCluster * 2 * kClusterRowsPerCta ||
+      (int64_t)groups * cl > device_sm_count())
+    cl = 0;
+  int G = cl > 0 ? groups * cl : n_ctas;
+  if (cl == 0 && G <= 0) {
     const int64_t want = (total + kMinRowsPerCta - 1) / kMinRowsPerCta;
     const int cap = MINB * device_sm_count();
     G = (int)(want < cap ? want : cap);
@@ -372,10 +425,23 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(kern, dim3(G), dim3((NC + 1) * 32), S::kAlloc, st, mk, mv, mks, mvs,
-                    (int64_t)chunk.p0, q_rot, a, part, counters,
-                    err, batch, n_kv, capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
-                    static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3((NC + 1) * 32);
+  cfg.dynamicSmemBytes = S::kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cl > 0 ? (unsigned)cl : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cl > 0 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, mk, mv, mks, mvs, (int64_t)chunk.p0, cl, q_rot, a, part, counters,
+                            err, batch, n_kv, capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
+                            static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
 }
 
 template <typename CT, int NS, int NC, int MINB>

@@ -582,6 +582,111 @@ __device__ __forceinline__ void attn_store_state_mma(MmaState& st, const MergeSm
   }
 }
 
+// ---------------------------------------------------------------------------
+// cluster mode: the CTAs of one cluster share one group and merge through DSMEM
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  return ra;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t ra) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t ra) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+
+// The CTA's state of its group from the NW warps' states in `sm`: warp h < 4
+// merges head h into cst ([4] m, [4] l, [4][256] unnormalised o).
+template <int NW>
+__device__ __forceinline__ void attn_cta_state(const MergeSmem& sm, float* cst) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  named_bar_sync(kBarConsumers, NW * 32);
+  if (warp >= kGroup) return;
+  const int h = warp;
+  float M = -INFINITY;
+#pragma unroll
+  for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, sm.ms[ww * 4 + h]);
+  float L = 0.f, O[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) O[i] = 0.f;
+#pragma unroll
+  for (int ww = 0; ww < NW; ++ww) {
+    const float mw = sm.ms[ww * 4 + h];
+    const float scl = mw == -INFINITY ? 0.f : exp2f(mw - M);
+    L = fmaf(sm.ls[ww * 4 + h], scl, L);
+    const float4* src = reinterpret_cast<const float4*>(sm.os + (ww * 4 + h) * kHeadDim + 8 * lane);
+    const float4 x0 = src[0], x1 = src[1];
+    O[0] = fmaf(x0.x, scl, O[0]); O[1] = fmaf(x0.y, scl, O[1]);
+    O[2] = fmaf(x0.z, scl, O[2]); O[3] = fmaf(x0.w, scl, O[3]);
+    O[4] = fmaf(x1.x, scl, O[4]); O[5] = fmaf(x1.y, scl, O[5]);
+    O[6] = fmaf(x1.z, scl, O[6]); O[7] = fmaf(x1.w, scl, O[7]);
+  }
+  if (lane == 0) {
+    cst[h] = M;
+    cst[4 + h] = L;
+  }
+  float4* dst = reinterpret_cast<float4*>(cst + 8 + h * kHeadDim + 8 * lane);
+  dst[0] = make_float4(O[0], O[1], O[2], O[3]);
+  dst[1] = make_float4(O[4], O[5], O[6], O[7]);
+}
+
+// Rank 0 of a cluster, warp h < 4: merge the cl CTA states (DSMEM, rank
+// order, every load issued first) and write head h of the group's output.
+__device__ __forceinline__ void attn_cluster_merge(const float* cst, int cl, float* a_head0,
+                                                   volatile int* flags) {
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float mq[8], lq[8];
+  float4 x0[8], x1[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (q < cl) {
+      mq[q] = ld_cluster_f32(cluster_addr(cst + h, (uint32_t)q));
+      lq[q] = ld_cluster_f32(cluster_addr(cst + 4 + h, (uint32_t)q));
+      const uint32_t ra = cluster_addr(cst + 8 + h * kHeadDim + 8 * lane, (uint32_t)q);
+      x0[q] = ld_cluster_f4(ra);
+      x1[q] = ld_cluster_f4(ra + 16);
+    } else {
+      mq[q] = -INFINITY;
+      lq[q] = 0.f;
+      x0[q] = x1[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) M = fmaxf(M, mq[q]);
+  float L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float scl = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
+    L = fmaf(lq[q], scl, L);
+    O[0] = fmaf(x0[q].x, scl, O[0]); O[1] = fmaf(x0[q].y, scl, O[1]);
+    O[2] = fmaf(x0[q].z, scl, O[2]); O[3] = fmaf(x0[q].w, scl, O[3]);
+    O[4] = fmaf(x1[q].x, scl, O[4]); O[5] = fmaf(x1[q].y, scl, O[5]);
+    O[6] = fmaf(x1[q].z, scl, O[6]); O[7] = fmaf(x1[q].w, scl, O[7]);
+  }
+  if (!flags[0]) {
+    const float inv = 1.0f / L;
+    float4* dst = reinterpret_cast<float4*>(a_head0 + h * kHeadDim + 8 * lane);
+    dst[0] = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+    dst[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
+  }
+}
+
 #endif  // __CUDACC__
 
 }  // namespace spark
