@@ -104,9 +104,9 @@ TRAFFIC = {
     ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_580_928,
     ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_021_440,
     ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_335_296,
-    ("full_bf16_b1_ctx131072", "attention"): 541_340_160,
+    ("full_bf16_b1_ctx131072", "attention"): 541_357_056,
 }
-ATTN_TRAFFIC_RATIO = 541_340_160 / 536_875_008
+ATTN_TRAFFIC_RATIO = 541_357_056 / 536_875_008
 
 
 def measured_traffic(workload: str, kernel: str, bytes_per_launch: float):

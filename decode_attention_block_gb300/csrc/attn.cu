@@ -38,9 +38,9 @@ namespace spark {
 namespace {
 
 constexpr int kMinRowsPerCta = 64;            // default grid: at least this many rows per CTA
-constexpr int64_t kDeepRows = 1 << 16;
+constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from which the deep ring pays
 constexpr int kMaxCluster = 8;                // CTAs per group in cluster mode
-constexpr int kClusterRowsPerCta = 96;        // cluster mode: about this many rows per CTA        // rows (x KV heads) per call from which the deep ring pays
+constexpr int kClusterRowsPerCta = 96;        // cluster mode: about this many rows per CTA
 
 template <typename CT, int NS, int NC>
 struct Smem {
