@@ -101,9 +101,9 @@ def step_bytes(wl: synth.Workload) -> dict:
 # the profile summaries give each capture's command.  Attention traffic
 # follows the rows read, so other workloads scale the captured ratio.
 TRAFFIC = {
-    ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_580_928,
-    ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_021_440,
-    ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_335_296,
+    ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_580_672,
+    ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_021_696,
+    ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_403_904,
     ("full_bf16_b1_ctx131072", "attention"): 541_357_056,
 }
 ATTN_TRAFFIC_RATIO = 541_357_056 / 536_875_008
