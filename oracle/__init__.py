@@ -1,4 +1,5 @@
-"""Plain float64 CPU oracle for the spark2_5 decode attention block.
+"""Plain float64 CPU oracle for the spark2_5 decode attention block and the
+rest of its decoder layer.
 
 TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test-suite (``tests/``), the
 ``smoke()`` check in ``__graft_entry__`` and the ``cpu_baseline`` / reference
@@ -6,7 +7,9 @@ leg of ``bench.py`` may import anything from this package.  The CUDA library
 and its Python binding never import, call or link it, and it imports nothing
 from them: the two sides share no code beyond the seeded input generators.
 
-Parity status of each function is stated in ``oracle.spark_block``'s header.
+Parity status of each function is stated in the headers of
+``oracle.spark_block`` (the attention block) and ``oracle.spark_layer`` (the
+MLP half of a decoder layer and the head).
 """
 
 from .spark_block import (  # noqa: F401
@@ -27,4 +30,9 @@ from .spark_block import (  # noqa: F401
     decode_step,
     prefill_chunk,
     cache_rows_to_f64,
+)
+from .spark_layer import (  # noqa: F401
+    gelu_erf,
+    mlp_block,
+    head_logits,
 )
