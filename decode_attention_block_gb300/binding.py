@@ -1,4 +1,5 @@
-"""ctypes binding of ``libspark_attn.so`` (the C ABI in ``include/spark_attn.h``).
+"""ctypes binding of ``libspark_attn.so`` (the C ABI in ``include/spark_attn.h``
+and ``include/spark_layer.h``).
 
 Argument marshalling only: every step of the block runs in the library's CUDA
 kernels.  Tensors are PyTorch CUDA tensors (PyTorch provides device memory and
@@ -70,7 +71,18 @@ class SparkKvLayer(ctypes.Structure):
     ]
 
 
-# every symbol include/spark_attn.h declares, with its ctypes signature
+class SparkMlpWeights(ctypes.Structure):
+    _fields_ = [
+        ("norm_w", ctypes.c_void_p),
+        ("gate_w", ctypes.c_void_p),
+        ("up_w", ctypes.c_void_p),
+        ("down_w", ctypes.c_void_p),
+        ("intermediate", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+# every symbol include/*.h declares, with its ctypes signature
 _P = ctypes.c_void_p
 _SIGNATURES = {
     "spark_geom_default": (None, [ctypes.POINTER(SparkGeom)]),
@@ -102,6 +114,11 @@ _SIGNATURES = {
                                             ctypes.POINTER(SparkLayerWeights), ctypes.c_int32, _P,
                                             ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "spark_dbg_wait_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint64, _P]),
+    "spark_mlp_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(SparkGeom), ctypes.c_int32, ctypes.c_int32]),
+    "spark_mlp_decode": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkMlpWeights),
+                                        ctypes.c_int32, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
+    "spark_head_logits": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, _P, _P, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "spark_attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "spark_attn_abi_version": (ctypes.c_int32, []),
 }
@@ -200,6 +217,29 @@ class KvLayer:
             raise ValueError("k and v must both be [batch, capacity, n_kv, head_dim]")
         return SparkKvLayer(_dev_ptr(self.k, "k", dt), _dev_ptr(self.v, "v", dt),
                             int(self.k.shape[1]), int(self.ring_capacity), _DTYPE_CODE[dt])
+
+
+@dataclass
+class MlpWeights:
+    """The MLP half of one layer as CUDA tensors (all float32 or all
+    bfloat16): ``norm_w [hidden]`` (post_attention_layernorm), ``gate_w`` and
+    ``up_w [intermediate, hidden]``, ``down_w [hidden, intermediate]``."""
+
+    norm_w: torch.Tensor
+    gate_w: torch.Tensor
+    up_w: torch.Tensor
+    down_w: torch.Tensor
+
+    def to_c(self) -> SparkMlpWeights:
+        dt = self.gate_w.dtype
+        if dt not in _DTYPE_CODE:
+            raise TypeError(f"weights must be float32 or bfloat16, got {dt}")
+        if self.gate_w.dim() != 2 or self.up_w.shape != self.gate_w.shape or \
+                self.down_w.shape != (self.gate_w.shape[1], self.gate_w.shape[0]):
+            raise ValueError("gate_w, up_w must be [intermediate, hidden] and down_w [hidden, intermediate]")
+        return SparkMlpWeights(_dev_ptr(self.norm_w, "norm_w", dt), _dev_ptr(self.gate_w, "gate_w", dt),
+                               _dev_ptr(self.up_w, "up_w", dt), _dev_ptr(self.down_w, "down_w", dt),
+                               int(self.gate_w.shape[0]), _DTYPE_CODE[dt])
 
 
 # ---------------------------------------------------------------------------
@@ -330,6 +370,46 @@ def spark_dbg_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None
     """Run a bounded wait that nothing satisfies (see the header)."""
     _check(load().spark_dbg_wait_timeout(_dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
                                          int(limit_ns), _stream(stream)), "spark_dbg_wait_timeout")
+
+
+def spark_mlp_workspace_bytes(geom: SparkGeom, intermediate: int, batch: int) -> int:
+    return int(load().spark_mlp_workspace_bytes(ctypes.byref(geom), int(intermediate), int(batch)))
+
+
+def make_mlp_workspace(geom: SparkGeom, intermediate: int, batch: int, device=None, stream=None) -> torch.Tensor:
+    """Allocate (through PyTorch) and initialise a workspace for
+    spark_mlp_decode at this intermediate size (0: spark_head_logits only)."""
+    nbytes = spark_mlp_workspace_bytes(geom, intermediate, batch)
+    if nbytes == 0:
+        raise ValueError("invalid geometry, intermediate size or batch for a workspace")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    spark_attn_workspace_init(ws, stream)
+    return ws
+
+
+def spark_mlp_decode(geom: SparkGeom, h: torch.Tensor, weights: MlpWeights, out: torch.Tensor,
+                     ws: torch.Tensor, path: int = 0, stream=None) -> None:
+    wc = weights.to_c()
+    _check(load().spark_mlp_decode(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32), ctypes.byref(wc),
+                                   int(h.shape[0]), _dev_ptr(out, "out", torch.float32), int(path),
+                                   _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)),
+           "spark_mlp_decode")
+
+
+def spark_head_logits(geom: SparkGeom, h: torch.Tensor, norm_w: torch.Tensor, embed: torch.Tensor,
+                      logits: torch.Tensor, ws: torch.Tensor, path: int = 0, stream=None) -> None:
+    """logits [batch, vocab] = embed [vocab, hidden] @ rms(h) * norm_w."""
+    dt = embed.dtype
+    if dt not in _DTYPE_CODE:
+        raise TypeError(f"embed must be float32 or bfloat16, got {dt}")
+    if embed.dim() != 2 or logits.dim() != 2 or logits.shape != (h.shape[0], embed.shape[0]):
+        raise ValueError("embed must be [vocab, hidden] and logits [batch, vocab]")
+    _check(load().spark_head_logits(ctypes.byref(geom), _dev_ptr(h, "h", torch.float32),
+                                    _dev_ptr(norm_w, "norm_w", dt), _dev_ptr(embed, "embed", dt),
+                                    int(embed.shape[0]), _DTYPE_CODE[dt], int(h.shape[0]),
+                                    _dev_ptr(logits, "logits", torch.float32), int(path),
+                                    _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)),
+           "spark_head_logits")
 
 
 def spark_attn_status_string(status: int) -> str:

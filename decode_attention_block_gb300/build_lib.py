@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libspark_attn.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["api.cu", "proj.cu", "attn.cu", "stack.cu", "noalloc.cu", "mma.cu"]
+SOURCES = ["api.cu", "proj.cu", "attn.cu", "stack.cu", "noalloc.cu", "mma.cu", "mlp.cu", "layer_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                  "-Xcompiler", "-Wall", "-I", INCLUDE]
@@ -36,7 +36,7 @@ def _nvcc() -> str:
 def _inputs() -> list[str]:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)
              if f.endswith((".cu", ".cuh", ".h"))]
-    files.append(os.path.join(INCLUDE, "spark_attn.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return files
 
 

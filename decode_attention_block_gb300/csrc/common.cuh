@@ -130,6 +130,41 @@ inline WsLayout ws_layout(int hidden, int n_q, int n_kv, int batch) {
   return L;
 }
 
+// Workspace of the MLP half of a layer and of the head (spark_mlp_decode,
+// spark_head_logits); the error word sits at offset 0 as in WsLayout, and the
+// tickets right after it, at an offset that does not depend on the sizes: a
+// workspace sized for one intermediate size serves the head too, and neither
+// call's partial results land on the other's tickets.
+struct MlpWsLayout {
+  size_t err = 0;    // uint32 error word
+  size_t mtick = 0;  // uint32 [kMmaMaxCtas] split-K tickets
+  size_t m = 0;      // f32 [batch][inter] GELU products (GEMV path)
+  size_t mx = 0;     // bf16 [2][bpad][hidden] normed activation rows (hi, lo)
+  size_t md = 0;     // bf16 [2][bpad][inter] GELU product rows (hi, lo)
+  size_t mpart = 0;  // f32 [kMmaMaxCtas][kMmaTileRows][bpad] split-K partials
+  size_t trace = 0;  // u64 [kTraceWords] opt-in phase stamps
+  size_t total = 0;
+};
+
+inline MlpWsLayout mlp_ws_layout(int hidden, int inter, int batch) {
+  MlpWsLayout L;
+  const size_t bpad = (size_t)((batch < kMmaMaxSeq ? batch : kMmaMaxSeq) + 7) / 8 * 8;
+  L.mtick = 256;
+  size_t off = align_up(L.mtick + sizeof(uint32_t) * kMmaMaxCtas, 256);
+  L.m = off;
+  off = align_up(off + sizeof(float) * (size_t)batch * inter, 256);
+  L.mx = off;
+  off = align_up(off + 2 * 2 * bpad * (size_t)hidden, 256);
+  L.md = off;
+  off = align_up(off + 2 * 2 * bpad * (size_t)inter, 256);
+  L.mpart = off;
+  off = align_up(off + sizeof(float) * (size_t)kMmaMaxCtas * kMmaTileRows * bpad, 256);
+  L.trace = off;
+  off = align_up(off + sizeof(uint64_t) * kTraceWords, 256);
+  L.total = off;
+  return L;
+}
+
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while its predecessor in the stream finishes; it calls pdl_wait() before
 // touching anything the predecessor writes.

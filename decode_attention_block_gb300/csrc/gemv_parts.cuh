@@ -239,6 +239,35 @@ __device__ __forceinline__ void row_dot2(const unsigned char* ra, const unsigned
   }
 }
 
+// ---------------------------------------------------------------------------
+// host: launch shape of a weight-streaming kernel
+// ---------------------------------------------------------------------------
+
+// Stages of a CTA-wide pool of `budget` bytes of shared memory: one per unit
+// of the CTA's share when they all fit next to the activations and the
+// barriers, so no stage is reused.  Otherwise a multiple of the consuming
+// warps: unit k lives in stage k % stages and belongs to warp k % nw, so the
+// warp that frees a stage is the one that consumes its next unit and never
+// waits on a barrier phase other than the next one (mbarrier parity tells
+// only the last two phases apart).  With fewer stages than warps only that
+// many warps consume; 0: not even one unit fits.
+inline int gemv_stages(size_t budget, int warps, size_t unit_bytes, size_t x_bytes, int max_units) {
+  if (x_bytes >= budget) return 0;
+  const size_t room = budget - x_bytes;
+  int s = (int)(room / (unit_bytes + 8));
+  if (s >= max_units) return max_units;
+  if (s >= warps) s -= s % warps;
+  return s < 1 ? 0 : s;
+}
+
+// Shared-memory bytes of nb permuted activation vectors of `cols` elements.
+template <typename WT>
+inline size_t gemv_xbytes(int cols, int nb) {
+  constexpr int E = Chunk<WT>::kElems;
+  const int nchunk = cols / E;
+  return sizeof(float) * (size_t)nb * ((nchunk + 31) / 32) * 32 * E;
+}
+
 #endif  // __CUDACC__
 
 }  // namespace spark

@@ -63,6 +63,25 @@ cudaError_t launch_oproj_mma(const float* a, const float* g, const float* h, con
                              float* out, uint32_t* err, int hidden, int n_q, int batch,
                              const MmaWorkspace& ws, cudaStream_t st);
 
+// The MLP half of a decoder layer and the head (mlp.cu: GEMV kernels for
+// small batches, any weight type; mma.cu: tensor-core GEMMs, bf16 weights).
+//   mlp:  out[b] = h[b] + W_down (gelu(W_gate x_b) * (W_up x_b)), x_b = rms(h_b) * norm_w
+//   head: logits[b] = E rms(h_b) * norm_w
+// m ([batch][inter] fp32) holds the GELU products of the GEMV path; xd
+// ([2][bpad][inter] bf16) the (hi, lo) rows of the tensor-core path.
+cudaError_t launch_mlp_gemv(int wdtype, const float* h, const void* norm_w, const void* gate_w,
+                            const void* up_w, const void* down_w, float* m, float* out, uint32_t* err,
+                            int hidden, int inter, int batch, float eps, cudaStream_t st);
+cudaError_t launch_head_gemv(int wdtype, const float* h, const void* norm_w, const void* embed,
+                             float* logits, uint32_t* err, int hidden, int vocab, int batch, float eps,
+                             cudaStream_t st);
+bool mma_mlp_supported(int wdtype, int hidden, int inter);
+cudaError_t launch_mlp_mma(const float* h, const void* norm_w, const void* gate_w, const void* up_w,
+                           const void* down_w, float* out, uint32_t* err, int hidden, int inter, int batch,
+                           float eps, const MmaWorkspace& ws, __nv_bfloat16* xd, cudaStream_t st);
+cudaError_t launch_head_mma(const float* h, const void* norm_w, const void* embed, float* logits, uint32_t* err,
+                            int hidden, int vocab, int batch, float eps, const MmaWorkspace& ws, cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

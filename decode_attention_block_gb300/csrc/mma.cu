@@ -10,7 +10,14 @@
 //    with k and v landing in their slots, encode_rope_neox_subdim on q and k);
 //  * o: the headwise sigmoid gate, o_proj and the raw residual add (attn.rs,
 //    encode_sigmoid_head_gate_mul before the o_proj GEMV; mod.rs, the layer
-//    loop's residual add).
+//    loop's residual add);
+//  * the rest of the decoder layer and the head (mod.rs, the module doc's
+//    transcription of one layer and its last two lines): up -- the
+//    post-attention RMSNorm, gate_proj and up_proj with the exact GELU product
+//    in the epilogue, which writes the product straight into the (hi, lo)
+//    rows down_proj reads; down -- down_proj and the residual add (the o
+//    epilogue); head -- the final RMSNorm and the tied embedding (the o
+//    epilogue without a residual).
 //
 // With B sequences a projection is the GEMM out[r][b] = sum_c W[r][c] x_b[c].
 // The weight rows are the MMA's M side (128 rows a tile, bf16 straight from
@@ -71,6 +78,8 @@ constexpr size_t kMaxDynSmem = 232448;                        // 227 KB per bloc
 constexpr size_t kStageBudget = kMaxDynSmem - 2048;           // static smem + alignment slack
 constexpr int kPrepThreads = 256;
 constexpr int kMaxPairs = kHeadDim / 2;
+constexpr size_t kSmemPerSm = 233472;                         // 228 KB of shared memory per SM
+constexpr uint32_t kTmemCols = 512;                           // tensor-memory columns per SM
 
 // ---------------------------------------------------------------------------
 // tcgen05 helpers (inline PTX)
@@ -295,7 +304,7 @@ k_prep_gate(const float* __restrict__ a, const float* __restrict__ g, __nv_bfloa
 // ---------------------------------------------------------------------------
 // the GEMM
 // ---------------------------------------------------------------------------
-enum { kEpiQkv = 0, kEpiO = 1 };
+enum { kEpiQkv = 0, kEpiO = 1, kEpiUp = 2 };
 
 struct MmaParams {
   int n_main_tiles;   // tiles over the main weight (the g tile follows them)
@@ -317,10 +326,13 @@ struct MmaParams {
   const float2* cs;
   int n_q, n_kv, rotary_dim;
   int64_t capacity;
-  // o epilogue
+  // o epilogue (also down_proj and the head: h null means no residual)
   const float* h;
   float* out;
-  int hidden;
+  int hidden;  // output rows (hidden, or vocab for the head)
+  // up epilogue
+  __nv_bfloat16* xd;  // [2][bpad][inter] (hi, lo) rows of the GELU product
+  int inter;
   // split-K and errors
   float* part;
   uint32_t* tickets;
@@ -380,7 +392,7 @@ __device__ __forceinline__ void reduce_parts(float* Y, const float* base, int sp
 }
 
 // out[b][R] = h[b][R] + the sum of the splits (in split order), float4 per
-// thread, for sequences [bb0, bb1).  Y non-null: the sum is already in Y
+// thread, for sequences [bb0, bb1); without h (the head) out[b][R] = the sum.  Y non-null: the sum is already in Y
 // ([bpad][128], the cluster reduction); else the splits' partials are read
 // from `base`.
 __device__ __forceinline__ void epilogue_o(const MmaParams& p, int tile, const float* base, const float* Y,
@@ -388,9 +400,10 @@ __device__ __forceinline__ void epilogue_o(const MmaParams& p, int tile, const f
   const int m4 = et & 31, b_first = bb0 + (et >> 5);
   const int R = kMmaTileRows * tile + 4 * m4;
   if (R >= p.hidden) return;  // hidden % 64 == 0: a float4 is wholly inside or outside
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   if (Y) {
     for (int b = b_first; b < bb1; b += 4) {
-      const float4 hv = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)b * p.hidden + R));
+      const float4 hv = p.h ? __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)b * p.hidden + R)) : zero;
       const float4 y = *reinterpret_cast<const float4*>(Y + (size_t)b * kMmaTileRows + 4 * m4);
       *reinterpret_cast<float4*>(p.out + (size_t)b * p.hidden + R) =
           make_float4(hv.x + y.x, hv.y + y.y, hv.z + y.z, hv.w + y.w);
@@ -404,7 +417,7 @@ __device__ __forceinline__ void epilogue_o(const MmaParams& p, int tile, const f
     for (int u = 0; u < kUnroll; ++u) {
       const int b = b_first + 4 * (k0 + u);
       if (k0 + u < nel) {
-        hv[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)b * p.hidden + R));
+        hv[u] = p.h ? __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)b * p.hidden + R)) : zero;
 #pragma unroll
         for (int s = 0; s < kMaxSplits; ++s)
           if (s < p.splits)
@@ -429,6 +442,25 @@ __device__ __forceinline__ void epilogue_o(const MmaParams& p, int tile, const f
             make_float4(hv[u].x + acc.x, hv[u].y + acc.y, hv[u].z + acc.z, hv[u].w + acc.w);
       }
     }
+  }
+}
+
+__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+
+// The up tile's rows 0..63 are gate_proj rows j0..j0+63 and rows 64..127 the
+// up_proj rows of the same j: m[b][j] = gelu(gate) * up, written as the
+// (hi, lo) rows b and bpad + b of down_proj's input, float4 per thread, for
+// sequences [bb0, bb1) (padded sequences included: their Y is zero).
+__device__ __forceinline__ void epilogue_up(const MmaParams& p, int tile, const float* Y, int bb0, int bb1,
+                                            int et) {
+  const int c4 = et & 15;
+  const int j = kBoxRows * tile + 4 * c4;
+  if (j >= p.inter) return;  // inter % 8 == 0: a float4 is wholly inside or outside
+  for (int b = bb0 + (et >> 4); b < bb1; b += kEpiThreads / 16) {
+    const float4 g = *reinterpret_cast<const float4*>(Y + (size_t)b * kMmaTileRows + 4 * c4);
+    const float4 u = *reinterpret_cast<const float4*>(Y + (size_t)b * kMmaTileRows + kBoxRows + 4 * c4);
+    const float4 m = make_float4(gelu_erf(g.x) * u.x, gelu_erf(g.y) * u.y, gelu_erf(g.z) * u.z, gelu_erf(g.w) * u.w);
+    store_split4(p.xd + (size_t)b * p.inter, p.xd + (size_t)(p.bpad + b) * p.inter, j, m);
   }
 }
 
@@ -559,6 +591,31 @@ __device__ __forceinline__ void epilogue_qkv(const MmaParams& p, const MmaSeq& s
   if (et == 0) stamp(p, kTrStored);
 }
 
+// The epilogue of one tile for sequences [bb0, bb1), run by the 128 epilogue
+// threads: from Y ([bpad][128] fp32, the finished sum), or -- parts non-null
+// -- from the splits' partial results in the workspace.
+template <int E, typename CT>
+__device__ __forceinline__ void epilogue(const MmaParams& p, const MmaSeq& seq, int tile, bool g_tile, float* Y,
+                                         const float* parts, int bb0, int bb1, int m, int et) {
+  if (E == kEpiO) {
+    epilogue_o(p, tile, parts, parts ? nullptr : Y, bb0, bb1, et);
+  } else {
+    if (parts) {
+      reduce_parts(Y, parts, p.splits, p.bpad, et);
+      if (et == 0) stamp(p, kTrReduced);
+    }
+    if (E == kEpiQkv)
+      epilogue_qkv<CT>(p, seq, tile, g_tile, Y, reinterpret_cast<float2*>(Y + p.bpad * kMmaTileRows), m, et, bb0,
+                       bb1);
+    else
+      epilogue_up(p, tile, Y, bb0, bb1, et);
+  }
+  if (p.trace) {
+    named_bar_sync(kBarEpi, kEpiThreads);
+    if (et == 0) stamp(p, kTrEnd);
+  }
+}
+
 template <int E, typename CT>
 __global__ void __launch_bounds__(kMmaThreads, 1)
 k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_g,
@@ -581,6 +638,9 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   const bool g_tile = E == kEpiQkv && tile >= p.n_main_tiles;
   const uint32_t x_bytes = (uint32_t)p.bpad * 2u * kRowBytes;
   const uint32_t a_bytes = g_tile ? (uint32_t)p.g_rows * kRowBytes : kABytes;
+  // sequences the epilogue covers: the up epilogue also zeroes the padded ones
+  const int nrows = E == kEpiUp ? p.bpad : p.nb;
+  float* const Y0 = reinterpret_cast<float*>(smem);
   volatile int* abort_v = &abort_flag;
 
   if (threadIdx.x == 0) {
@@ -595,7 +655,7 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     fence_mbar_init();
     prefetch_tensormap(&tm_w);
     prefetch_tensormap(&tm_x);
-    if (g_tile) prefetch_tensormap(&tm_g);
+    if (g_tile || E == kEpiUp) prefetch_tensormap(&tm_g);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, (uint32_t)p.tmem_cols);
@@ -623,6 +683,9 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
       auto load_w = [&](int s, int kb) {
         if (g_tile) {
           tma_load_2d(stage(s), &tm_g, &full_bar[s], kb * kKBlock, 0);
+        } else if (E == kEpiUp) {  // gate rows, then the up rows of the same j
+          tma_load_2d(stage(s), &tm_w, &full_bar[s], kb * kKBlock, kBoxRows * tile);
+          tma_load_2d(stage(s) + kABytes / 2, &tm_g, &full_bar[s], kb * kKBlock, kBoxRows * tile);
         } else {
           tma_load_2d(stage(s), &tm_w, &full_bar[s], kb * kKBlock, r0);
           tma_load_2d(stage(s) + kABytes / 2, &tm_w, &full_bar[s], kb * kKBlock, r1);
@@ -704,8 +767,9 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     tc_fence_after();
     if (et == 0) stamp(p, kTrDone);
     float* Y = reinterpret_cast<float*>(smem);  // [bpad][128] fp32, over the drained stages
-    // this split's partial: to shared memory (cluster reduction) or to the workspace
-    float* P = p.cluster ? Y : p.part + (size_t)blockIdx.x * kMmaTileRows * p.bpad;
+    // this split's partial: to shared memory (cluster reduction, or the whole
+    // sum when K is not split) or to the workspace
+    float* P = (p.cluster || p.splits == 1) ? Y : p.part + (size_t)blockIdx.x * kMmaTileRows * p.bpad;
     if (ok) {
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
       for (int j = 0; j < p.bpad; j += 8) {
@@ -721,7 +785,7 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     // are in shared memory, CTA r adds up the sequences [r nb / S, (r+1) nb / S)
     // over the cluster (DSMEM, in split order) and runs their epilogue.
     const int S = p.splits, r = (int)cluster_rank();
-    const int bb0 = r * p.nb / S, bb1 = (r + 1) * p.nb / S;
+    const int bb0 = r * nrows / S, bb1 = (r + 1) * nrows / S;
     float* Y = reinterpret_cast<float*>(smem);
     cluster_sync_all();  // every partial written
     if (warp >= 2) {
@@ -758,15 +822,14 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
       const int et = threadIdx.x - 64;
       const int m = (warp & 3) * 32 + lane;
       if (et == 0) stamp(p, kTrReduced);
-      if (E == kEpiQkv)
-        epilogue_qkv<CT>(p, seq, tile, g_tile, Y, reinterpret_cast<float2*>(Y + p.bpad * kMmaTileRows), m, et,
-                         bb0, bb1);
-      else
-        epilogue_o(p, tile, nullptr, Y, bb0, bb1, et);
-      if (p.trace) {
-        named_bar_sync(kBarEpi, kEpiThreads);
-        if (et == 0) stamp(p, kTrEnd);
-      }
+      epilogue<E, CT>(p, seq, tile, g_tile, Y, nullptr, bb0, bb1, m, et);
+    }
+  } else if (p.splits == 1) {
+    if (warp >= 2) {
+      const int et = threadIdx.x - 64;
+      const int m = (warp & 3) * 32 + lane;
+      named_bar_sync(kBarEpi, kEpiThreads);  // every row of Y written
+      epilogue<E, CT>(p, seq, tile, g_tile, Y0, nullptr, 0, nrows, m, et);
     }
   } else if (warp >= 2) {
     const int et = threadIdx.x - 64;
@@ -786,18 +849,7 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     named_bar_sync(kBarEpi, kEpiThreads);
     if (last_flag != 0) {
       __threadfence();
-      if (E == kEpiQkv) {
-        reduce_parts(Y, parts, p.splits, p.bpad, et);
-        if (et == 0) stamp(p, kTrReduced);
-        epilogue_qkv<CT>(p, seq, tile, g_tile, Y, reinterpret_cast<float2*>(Y + p.bpad * kMmaTileRows), m, et,
-                         0, p.nb);
-      } else {
-        epilogue_o(p, tile, parts, nullptr, 0, p.nb, et);
-      }
-      if (p.trace) {
-        named_bar_sync(kBarEpi, kEpiThreads);
-        if (et == 0) stamp(p, kTrEnd);
-      }
+      epilogue<E, CT>(p, seq, tile, g_tile, Y, parts, 0, nrows, m, et);
     }
   }
   // every tensor-memory read is done before the owner frees the columns
@@ -855,6 +907,11 @@ Plan plan_with(int tiles, int kblocks, int bpad, int s) {
   P.smem = body + 1024;
   P.tmem_cols = 32;
   while (P.tmem_cols < 2 * bpad) P.tmem_cols *= 2;
+  // No more CTAs on an SM than its tensor memory holds: a CTA whose
+  // allocation had to wait for another's columns could wait on a cluster
+  // peer that cannot start.  Enough shared memory keeps the extra CTA out.
+  const size_t min_smem = kSmemPerSm / (kTmemCols / (uint32_t)P.tmem_cols + 1) + 1;
+  if (P.smem < min_smem) P.smem = min_smem;
   return P;
 }
 
@@ -950,6 +1007,10 @@ cudaError_t launch_gemm(const CUtensorMap& tw, const CUtensorMap& tg, const CUte
 
 }  // namespace
 
+bool mma_mlp_supported(int wdtype, int hidden, int inter) {
+  return wdtype == SPARK_BF16 && hidden % kKBlock == 0 && inter % 8 == 0 && tensor_map_encoder() != nullptr;
+}
+
 bool mma_projections_supported(int wdtype, int hidden, int n_q, int rotary_dim) {
   return wdtype == SPARK_BF16 && hidden % kKBlock == 0 && n_q <= kMmaTileRows &&
          (rotary_dim <= kMmaTileRows || rotary_dim == kHeadDim) && tensor_map_encoder() != nullptr;
@@ -1042,6 +1103,92 @@ cudaError_t launch_oproj_mma(const float* a, const float* g, const float* h, con
     p.trace = ws.trace;
     MmaSeq seq = {};
     e = launch_gemm<kEpiO, float>(tw, tw, tx, p, seq, p.n_main_tiles, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_mlp_mma(const float* h, const void* norm_w, const void* gate_w, const void* up_w,
+                           const void* down_w, float* out, uint32_t* err, int hidden, int inter, int batch,
+                           float eps, const MmaWorkspace& ws, __nv_bfloat16* xd, cudaStream_t st) {
+  CUtensorMap tg, tu, td;
+  if (!make_bf16_map(&tg, gate_w, hidden, inter, kBoxRows) || !make_bf16_map(&tu, up_w, hidden, inter, kBoxRows) ||
+      !make_bf16_map(&td, down_w, inter, hidden, kBoxRows))
+    return cudaErrorInvalidValue;
+  PrepArgs pa = {};  // no rope table
+  const int up_tiles = (inter + kBoxRows - 1) / kBoxRows;
+  const int down_tiles = (hidden + kMmaTileRows - 1) / kMmaTileRows;
+  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
+    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
+    const int bpad = (nb + 7) / 8 * 8;
+    cudaError_t e = launch_pdl(k_prep_norm, dim3(bpad), dim3(kPrepThreads), 0, st, h + (size_t)b0 * hidden,
+                               static_cast<const __nv_bfloat16*>(norm_w), ws.x, (float2*)nullptr, hidden, nb,
+                               bpad, eps, 0, pa);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tx, txd;
+    if (!make_bf16_map(&tx, ws.x, hidden, 2 * bpad, 2 * bpad) || !make_bf16_map(&txd, xd, inter, 2 * bpad, 2 * bpad))
+      return cudaErrorInvalidValue;
+    MmaSeq seq = {};
+    MmaParams p = {};
+    p.n_main_tiles = up_tiles;
+    p.kblocks = hidden / kKBlock;
+    p.bpad = bpad;
+    p.nb = nb;
+    p.xd = xd;
+    p.inter = inter;
+    p.part = ws.part;
+    p.tickets = ws.tickets;
+    p.err = err;
+    p.trace = ws.trace;
+    e = launch_gemm<kEpiUp, float>(tg, tu, tx, p, seq, up_tiles, st);
+    if (e != cudaSuccess) return e;
+    MmaParams q = {};
+    q.n_main_tiles = down_tiles;
+    q.kblocks = (inter + kKBlock - 1) / kKBlock;  // the last block's columns past inter read as zero
+    q.bpad = bpad;
+    q.nb = nb;
+    q.h = h + (size_t)b0 * hidden;
+    q.out = out + (size_t)b0 * hidden;
+    q.hidden = hidden;
+    q.part = ws.part;
+    q.tickets = ws.tickets;
+    q.err = err;
+    q.trace = ws.trace;
+    e = launch_gemm<kEpiO, float>(td, td, txd, q, seq, down_tiles, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_head_mma(const float* h, const void* norm_w, const void* embed, float* logits, uint32_t* err,
+                            int hidden, int vocab, int batch, float eps, const MmaWorkspace& ws, cudaStream_t st) {
+  CUtensorMap te;
+  if (!make_bf16_map(&te, embed, hidden, vocab, kBoxRows)) return cudaErrorInvalidValue;
+  PrepArgs pa = {};
+  const int tiles = (vocab + kMmaTileRows - 1) / kMmaTileRows;
+  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
+    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
+    const int bpad = (nb + 7) / 8 * 8;
+    cudaError_t e = launch_pdl(k_prep_norm, dim3(bpad), dim3(kPrepThreads), 0, st, h + (size_t)b0 * hidden,
+                               static_cast<const __nv_bfloat16*>(norm_w), ws.x, (float2*)nullptr, hidden, nb,
+                               bpad, eps, 0, pa);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tx;
+    if (!make_bf16_map(&tx, ws.x, hidden, 2 * bpad, 2 * bpad)) return cudaErrorInvalidValue;
+    MmaSeq seq = {};
+    MmaParams p = {};
+    p.n_main_tiles = tiles;
+    p.kblocks = hidden / kKBlock;
+    p.bpad = bpad;
+    p.nb = nb;
+    p.h = nullptr;  // no residual
+    p.out = logits + (size_t)b0 * vocab;
+    p.hidden = vocab;
+    p.part = ws.part;
+    p.tickets = ws.tickets;
+    p.err = err;
+    p.trace = ws.trace;
+    e = launch_gemm<kEpiO, float>(te, te, tx, p, seq, tiles, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -263,27 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-// Stages of the CTA-wide pool: one per unit of the CTA's share when they all
-// fit next to the activations and the barriers, so no stage is reused.
-// Otherwise a multiple of the consuming warps: unit k lives in stage
-// k % stages and belongs to warp k % nw, so the warp that frees a stage is the
-// one that consumes its next unit and never waits on a barrier phase other
-// than the next one (mbarrier parity tells only the last two phases apart).
-// With fewer stages than warps only that many warps consume; 0: not even one
-// unit fits.
 int stages_for(size_t unit_bytes, size_t x_bytes, int max_units) {
-  const size_t room = kSmemBudget - x_bytes;
-  int s = (int)(room / (unit_bytes + 8));
-  if (s >= max_units) return max_units;
-  if (s >= kWarps) s -= s % kWarps;
-  return s < 1 ? 0 : s;
+  return gemv_stages(kSmemBudget, kWarps, unit_bytes, x_bytes, max_units);
 }
 
 template <typename WT>
 size_t xbytes(int cols, int nb) {
-  constexpr int E = Chunk<WT>::kElems;
-  const int nchunk = cols / E;
-  return sizeof(float) * (size_t)nb * ((nchunk + 31) / 32) * 32 * E;
+  return gemv_xbytes<WT>(cols, nb);
 }
 
 template <typename WT, typename CT, int NB>

@@ -4,7 +4,13 @@ The one module both the CUDA path's callers and the CPU oracle's callers use:
 it draws random numbers and casts them, and holds none of the block's
 arithmetic.  Value distributions: h ~ N(0, 1); input_layernorm = 1 + 0.1 N(0, 1);
 q_k_v_proj and g_proj ~ N(0, 1/hidden); o_proj ~ N(0, 1/(n_q*d)); every
-cache row ~ N(0, 1).  Values are drawn in fp32 and rounded to bf16 with
+cache row ~ N(0, 1).  The rest of the decoder layer and the head:
+post_attention_layernorm and model.norm = 1 + 0.1 N(0, 1); gate_proj and
+up_proj ~ N(0, 1/hidden); down_proj ~ N(0, 1/intermediate); the tied
+embedding ~ N(0, 1/hidden) (logits of order 1).  The pages print neither the
+intermediate size nor the vocabulary: INTERMEDIATE and VOCAB are stand-ins
+(a 4x MLP and 2^17 tokens, which with 36 layers put the model near the 4B
+parameters its name states).  Values are drawn in fp32 and rounded to bf16 with
 round-to-nearest-even where the workload is bf16.  No trained checkpoint and
 no dataset is involved: the workloads are defined by their shapes, lengths and
 distributions alone.
@@ -23,6 +29,8 @@ N_KV = 4
 HEAD_DIM = 256
 WINDOW = 512
 RING = 512
+INTERMEDIATE = 4 * HIDDEN
+VOCAB = 1 << 17
 
 
 @dataclass(frozen=True)
@@ -184,3 +192,35 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
     return t.numpy()
+
+
+def make_mlp_weights(seed: int, hidden: int, inter: int, dtype=torch.bfloat16, device="cpu",
+                     gen_device=None) -> dict:
+    """The MLP half of one layer: norm_w [H] (post_attention_layernorm),
+    gate_w, up_w [I, H], down_w [H, I]."""
+    gd = gen_device or device
+    g = _gen(seed * 1000033 + 11, gd)
+    out = {
+        "norm_w": _randn((hidden,), g, gd, 0.1, 1.0, dtype),
+        "gate_w": _randn((inter, hidden), g, gd, hidden ** -0.5, 0.0, dtype),
+        "up_w": _randn((inter, hidden), g, gd, hidden ** -0.5, 0.0, dtype),
+        "down_w": _randn((hidden, inter), g, gd, inter ** -0.5, 0.0, dtype),
+    }
+    return {k: v.to(device) for k, v in out.items()}
+
+
+def make_head(seed: int, hidden: int, vocab: int, dtype=torch.bfloat16, device="cpu", gen_device=None) -> dict:
+    """The head: norm_w [H] (model.norm) and the tied embedding [V, H]."""
+    gd = gen_device or device
+    g = _gen(seed * 1000037 + 13, gd)
+    out = {
+        "norm_w": _randn((hidden,), g, gd, 0.1, 1.0, dtype),
+        "embed": _randn((vocab, hidden), g, gd, hidden ** -0.5, 0.0, dtype),
+    }
+    return {k: v.to(device) for k, v in out.items()}
+
+
+def make_hidden(seed: int, batch: int, hidden: int, device="cpu", gen_device=None) -> torch.Tensor:
+    """A residual stream [batch, hidden] ~ N(0, 1) (fp32)."""
+    gd = gen_device or device
+    return _randn((batch, hidden), _gen(seed * 7919 + 5, gd), gd).to(device)

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define SPARK_ATTN_ABI_VERSION 3
+#define SPARK_ATTN_ABI_VERSION 4
 /* largest batch one call accepts */
 #define SPARK_MAX_BATCH 1024
 

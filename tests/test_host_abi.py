@@ -25,10 +25,14 @@ def B():
 
 
 def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "spark_attn.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(spark_[a-z0-9_]+)\s*\(",
-                       text, flags=re.M)
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(spark_[a-z0-9_]+)\s*\(",
+                            text, flags=re.M)
     return sorted(set(names))
 
 
@@ -37,12 +41,12 @@ def test_every_declared_symbol_is_exported_and_bound(B):
     assert len(declared) >= 10
     lib = ctypes.CDLL(build_lib.LIB_PATH)
     for name in declared:
-        assert hasattr(lib, name), f"{name} declared in spark_attn.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
     assert sorted(B.declared_symbols()) == declared
 
 
 def test_abi_version_and_status_strings(B):
-    assert B.spark_attn_abi_version() == 3
+    assert B.spark_attn_abi_version() == 4
     for code in range(-7, 1):
         s = B.spark_attn_status_string(code)
         assert s and s != "unknown status"
@@ -213,3 +217,72 @@ def test_wait_timeout_arguments_are_validated(B):
     assert lib.spark_dbg_wait_timeout(FAKE, 4096, 3_000_000_000, None) == -1
     assert lib.spark_dbg_wait_timeout(FAKE + 16, 4096, 1000, None) == -4
     assert lib.spark_dbg_wait_timeout(0, 4096, 1000, None) == -4
+
+
+# -- the rest of the decoder layer and the head ------------------------------
+
+def _mlp(B, inter=10240, batch=1, dtype=None, path=0, ptrs=None, h=FAKE, out=FAKE, ws=FAKE, ws_bytes=None,
+         geom=None):
+    lib = B.load()
+    g = geom or B.spark_geom_default()
+    dt = B.SPARK_BF16 if dtype is None else dtype
+    p = ptrs or (FAKE, FAKE, FAKE, FAKE)
+    w = B.SparkMlpWeights(p[0], p[1], p[2], p[3], inter, dt)
+    if ws_bytes is None:
+        ws_bytes = B.spark_mlp_workspace_bytes(g, inter, max(1, min(batch, 1024))) or (1 << 30)
+    return lib.spark_mlp_decode(ctypes.byref(g), h, ctypes.byref(w), batch, out, path, ws, ws_bytes, None)
+
+
+def _head(B, vocab=131072, batch=1, dtype=None, path=0, norm=FAKE, embed=FAKE, ws=FAKE, ws_bytes=None):
+    lib = B.load()
+    g = B.spark_geom_default()
+    dt = B.SPARK_BF16 if dtype is None else dtype
+    if ws_bytes is None:
+        ws_bytes = B.spark_mlp_workspace_bytes(g, 0, max(1, min(batch, 1024))) or (1 << 30)
+    return lib.spark_head_logits(ctypes.byref(g), FAKE, norm, embed, vocab, dt, batch, FAKE, path, ws, ws_bytes,
+                                 None)
+
+
+def test_mlp_workspace_bytes(B):
+    g = B.spark_geom_default()
+    sizes = [B.spark_mlp_workspace_bytes(g, 10240, b) for b in (1, 8, 64, 1024)]
+    assert all(s > 0 and s % 256 == 0 for s in sizes) and sizes == sorted(sizes)
+    assert B.spark_mlp_workspace_bytes(g, 0, 1) < B.spark_mlp_workspace_bytes(g, 8, 1)
+    for inter in (-8, 4, 12, 16392):
+        assert B.spark_mlp_workspace_bytes(g, inter, 1) == 0
+    assert B.spark_mlp_workspace_bytes(g, 10240, 0) == 0
+
+
+def test_mlp_arguments_are_validated(B):
+    assert _mlp(B, h=0) == -1
+    assert _mlp(B, out=FAKE + 4) == -1
+    assert _mlp(B, ptrs=(FAKE, FAKE, 0, FAKE)) == -1
+    assert _mlp(B, ptrs=(FAKE, FAKE + 8, FAKE, FAKE)) == -1
+    assert _mlp(B, dtype=3) == -1
+    assert _mlp(B, batch=0) == -1
+    assert _mlp(B, batch=1025) == -1
+    assert _mlp(B, inter=-8) == -1
+    assert _mlp(B, inter=12, ws_bytes=1 << 30) == -5      # not a multiple of 8
+    assert _mlp(B, inter=16392, ws_bytes=1 << 30) == -5
+    assert _mlp(B, path=5) == -1
+    assert _mlp(B, batch=8, path=B.SPARK_PATH_MMA, dtype=B.SPARK_F32) == -5
+    need = B.spark_mlp_workspace_bytes(B.spark_geom_default(), 10240, 1)
+    assert _mlp(B, ws_bytes=need - 1) == -4
+    assert _mlp(B, ws=FAKE + 16) == -4
+    bad = B.spark_geom_default()
+    bad.hidden = 2564
+    assert _mlp(B, geom=bad, ws_bytes=1 << 30) == -5
+
+
+def test_head_arguments_are_validated(B):
+    assert _head(B, norm=0) == -1
+    assert _head(B, embed=FAKE + 8) == -1
+    assert _head(B, vocab=0) == -1
+    assert _head(B, vocab=1001) == -5
+    assert _head(B, vocab=(1 << 22) + 8) == -5
+    assert _head(B, dtype=2) == -1
+    assert _head(B, batch=0) == -1
+    assert _head(B, path=7) == -1
+    assert _head(B, batch=8, path=B.SPARK_PATH_MMA, dtype=B.SPARK_F32) == -5
+    assert _head(B, ws_bytes=64) == -4
+    assert _head(B, ws=0) == -4
