@@ -576,6 +576,151 @@ def bench_prefill(args, wl):
             "clocks": sampler.summary()}
 
 
+def bench_decoder(args, wl):
+    """`--decoder`: whole decode steps of a model with the workload's layers --
+    per layer the attention block (spark_attn_decode) and the MLP half
+    (spark_mlp_decode, intermediate synth.INTERMEDIATE), then the final norm and
+    the tied head (spark_head_logits, vocabulary synth.VOCAB) -- replayed from
+    a CUDA graph.  Reports tokens/s, the step's HBM bytes (every weight once,
+    the KV rows read) and each stage's time per launch against its bytes."""
+    from decode_attention_block_gb300 import binding as B
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    build_lib.build()
+    B.load()
+    geom = B.spark_geom_default()
+    stream = torch.cuda.current_stream(device)
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    eb = 2 if wl.dtype == "bf16" else 4
+    I, V, H, L = synth.INTERMEDIATE, synth.VOCAB, wl.hidden, len(wl.layers)
+    sb = step_bytes(wl)
+    mlp_bytes = (3 * I * H + H) * eb
+    head_bytes = (V * H + H) * eb
+    total = sb["total"] + L * mlp_bytes + head_bytes
+    l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
+    copies = args.copies or max(1, math.ceil(4 * l2 / total))
+    cps = []
+    for c in range(copies):
+        cp = Copy(wl, B, device)
+        cp.mlp = [B.MlpWeights(**synth.make_mlp_weights(wl.seed * 100 + li, H, I, dt, device)) for li in range(L)]
+        hd = synth.make_head(wl.seed, H, V, dt, device)
+        cp.head = (hd["norm_w"], hd["embed"])
+        cp.logits = torch.empty((wl.batch, V), device=device)
+        cps.append(cp)
+    ws = B.make_workspace(geom, wl.batch, device)
+    wsm = B.make_mlp_workspace(geom, I, wl.batch, device)
+
+    # launches go to the current stream (the capturing one inside capture())
+    def attn(cp, li, cur, out):
+        spec, w, kv = cp.layers[li]
+        B.spark_attn_decode(geom, cur, w, kv, B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING, wl.positions,
+                            out, ws)
+
+    def mlp(cp, li, buf):
+        B.spark_mlp_decode(geom, buf, cp.mlp[li], buf, wsm, 0)
+
+    def head(cp, cur):
+        B.spark_head_logits(geom, cur, cp.head[0], cp.head[1], cp.logits, wsm, 0)
+
+    def step_of(cp):
+        cur = cp.h
+        for li in range(L):
+            out = cp.buf[li % 2]
+            attn(cp, li, cur, out)
+            mlp(cp, li, out)
+            cur = out
+        head(cp, cur)
+        return cp.logits
+
+    graphs = [capture(lambda cp=cp: step_of(cp)) for cp in cps]
+    for i in range(args.warmup):
+        graphs[i % copies].replay()
+    torch.cuda.synchronize()
+    steps = args.steps or 200
+    sampler = ClockSampler(0)
+    with sampler:
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % copies].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+
+    # each stage's launches (all layers, all copies) replayed back to back
+    stages = {
+        "attention_block": (lambda cp: [attn(cp, li, cp.buf[li % 2], cp.buf[(li + 1) % 2]) for li in range(L)],
+                            L, sb["total"] / L),
+        "mlp": (lambda cp: [mlp(cp, li, cp.buf[li % 2]) for li in range(L)], L, mlp_bytes),
+        "head": (lambda cp: head(cp, cp.buf[0]), 1, head_bytes),
+    }
+    kern = {}
+    for name, (fn, n, nbytes) in stages.items():
+        g = capture(lambda: [fn(cp) for cp in cps])
+        reps = max(3, min(100, int(400 / (n * copies))))
+        g.replay()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        us = a0.elapsed_time(a1) / (reps * n * copies) * 1e3
+        kern[name] = {"avg_us": round(us, 3), "launches_per_step": n, "bytes_per_launch": int(nbytes),
+                      "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    tot = sum(k["avg_us"] * k["launches_per_step"] for k in kern.values())
+    for k in kern.values():
+        k["share"] = round(k["avg_us"] * k["launches_per_step"] / tot, 4)
+    top = max(kern, key=lambda k: kern[k]["share"])
+
+    # end to end: h from pinned host memory, the logits read back
+    h_host = synth.make_h(wl, "cpu").pin_memory()
+    lg_host = torch.empty((wl.batch, V), dtype=torch.float32).pin_memory()
+    n_e2e = max(10, min(steps, 200))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        cp = cps[i % copies]
+        cp.h.copy_(h_host, non_blocking=True)
+        lg_host.copy_(step_of(cp), non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    for w_ in (ws, wsm):
+        if B.spark_attn_error_word(w_) != 0:
+            raise RuntimeError("device error word set")
+    peaks = measured_peaks()
+    ach = kern[top]["gbs"]
+    # tensor cores: a prologue and two GEMMs per 128 sequences; GEMV: up per 4, down per 2
+    mlp_launches = (3 * -(-wl.batch // 128)) if (wl.batch > 4 and wl.dtype == "bf16") else \
+        (-(-wl.batch // 4) + -(-wl.batch // 2))
+    head_launches = (2 * -(-wl.batch // 128)) if (wl.batch > 4 and wl.dtype == "bf16") else -(-wl.batch // 4)
+    launches = L * (2 * projection_launches(wl) + 1 + mlp_launches) + head_launches
+    return {"metric": "decoder step tokens/s (per layer the attention block and the MLP half, then the "
+                      "final norm and the tied head)",
+            "value": round(wl.batch / (ms * 1e-3), 3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; no checkpoint)",
+            "config": {"workload": f"{wl.name} + MLP (intermediate {I}) per layer + head (vocab {V})",
+                       "batch": wl.batch, "n_layers": L, "intermediate": I, "vocab": V,
+                       "launch": "CUDA graph per step",
+                       "l2": f"{copies} rotating copies ({copies * total / 1e6:.0f} MB) vs {l2 / 1e6:.0f} MB L2"},
+            "hbm_bytes_per_step": total, "hbm_gbs": round(total / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(total / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "roofline": {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                         "peak_source": peaks["source"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                         "traffic": None, "traffic_source": "no capture of this stage on this workload",
+                         "bytes_per_launch": kern[top]["bytes_per_launch"], "avg_launch_us": kern[top]["avg_us"]},
+            "kernels": kern,
+            "e2e": {"value": round(wl.batch * n_e2e / e2e_s, 3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * V * 4,
+                    "launch": "direct calls, synchronised every step"},
+            "gpu_launches": launches * steps,
+            "clocks": sampler.summary()}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -588,6 +733,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch steps directly instead of graph replay")
     ap.add_argument("--path", default="layers", choices=["stack", "layers"],
                     help="one call per layer (default, the faster path measured) or the whole step in one call")
+    ap.add_argument("--decoder", action="store_true",
+                    help="time whole decoder steps: attention block + MLP per layer, then the head")
     ap.add_argument("--prefill", type=int, default=0,
                     help="time chunks of this many consecutive tokens (spark_attn_prefill) instead of decode")
     args = ap.parse_args()
@@ -603,6 +750,9 @@ def main():
 
     if args.prefill > 0:
         print(json.dumps(bench_prefill(args, wl)), flush=True)
+        return
+    if args.decoder:
+        print(json.dumps(bench_decoder(args, wl)), flush=True)
         return
 
     dist_init(world, "nccl")
