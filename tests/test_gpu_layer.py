@@ -78,6 +78,10 @@ MLP_SMALL = [
     (256, 1000, 64, torch.bfloat16, "mma"),
     (256, 352, 130, torch.bfloat16, "mma"),
     (256, 352, 9, torch.float32, "auto"),      # fp32 weights: the GEMV path at any batch
+    # more up tiles than SMs (two CTAs per SM, or a second wave), ragged last tile
+    (256, 12296, 8, torch.bfloat16, "mma"),
+    (512, 10248, 64, torch.bfloat16, "mma"),
+    (256, 16384, 130, torch.bfloat16, "mma"),
 ]
 
 
@@ -152,6 +156,9 @@ HEAD_SMALL = [
     (256, 1000, 64, torch.bfloat16, "mma"),
     (256, 4104, 130, torch.bfloat16, "mma"),
     (256, 8, 16, torch.bfloat16, "mma"),
+    # more tiles than SMs (several waves), ragged last tile
+    (256, 40008, 16, torch.bfloat16, "mma"),
+    (512, 20488, 77, torch.bfloat16, "mma"),
 ]
 
 
@@ -181,3 +188,26 @@ def test_head_full_size_on_sampled_rows(B, batch, path):
     assert np.all(np.isfinite(logits.cpu().numpy())), "a logit was never written"
     for b in range(batch):
         assert_close(got[b], want[b], f"head full b={b} {path}")
+
+
+def test_many_tile_results_repeat_bit_for_bit(B):
+    # launches with more tiles than SMs give the same bits call after call on
+    # one workspace (split-K tickets reset, partials added in split order)
+    hidden, inter, batch = 256, 12296, 8
+    w = synth.make_mlp_weights(9, hidden, inter, torch.bfloat16, "cuda")
+    h = synth.make_hidden(9, batch, hidden, "cuda")
+    g = _geom(B, hidden)
+    ws = B.make_mlp_workspace(g, inter, batch)
+    outs = []
+    for _ in range(3):
+        o = torch.empty_like(h)
+        B.spark_mlp_decode(g, h, B.MlpWeights(**w), o, ws, PATHS["mma"])
+        outs.append(o)
+    p = synth.make_head(9, hidden, 40008, torch.bfloat16, "cuda")
+    lg = [torch.empty((batch, 40008), device="cuda") for _ in range(2)]
+    for t in lg:
+        B.spark_head_logits(g, h, p["norm_w"], p["embed"], t, ws, PATHS["mma"])
+    torch.cuda.synchronize()
+    assert B.spark_attn_error_word(ws) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert torch.equal(lg[0], lg[1])
