@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libspark_attn.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["api.cu", "proj.cu", "attn.cu", "stack.cu", "noalloc.cu", "mma.cu", "mlp.cu", "layer_api.cu"]
+SOURCES = ["api.cu", "proj.cu", "attn.cu", "stack.cu", "noalloc.cu", "mma.cu", "mlp.cu", "layer_api.cu", "attn_chunk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                  "-Xcompiler", "-Wall", "-I", INCLUDE]

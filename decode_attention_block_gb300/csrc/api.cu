@@ -290,11 +290,17 @@ int spark_attn_prefill(const spark_geom* g, const float* h, const spark_layer_we
   chunk.p0 = p0;
   chunk.k = ks;
   chunk.v = vs;
-  if (e == cudaSuccess)
-    e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity, kv->ring_capacity,
-                         layer_class == SPARK_FULL, g->window, g->scale, positions.data(), m, a,
-                         ws_at<float>(workspace, L.part), ws_at<uint32_t>(workspace, L.counters), err,
-                         0, nullptr, 0, st, chunk);
+  if (e == cudaSuccess) {
+    if (attention_chunk_grouped_applies(kv->dtype, m, g->n_kv))
+      e = launch_attention_chunk_grouped(q_rot, kv->k, kv->v, g->n_kv, kv->capacity, kv->ring_capacity,
+                                         layer_class == SPARK_FULL, g->window, g->scale, p0, m, ks, vs, a, err,
+                                         st);
+    else
+      e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity, kv->ring_capacity,
+                           layer_class == SPARK_FULL, g->window, g->scale, positions.data(), m, a,
+                           ws_at<float>(workspace, L.part), ws_at<uint32_t>(workspace, L.counters), err,
+                           0, nullptr, 0, st, chunk);
+  }
   if (e == cudaSuccess)
     e = launch_commit_rows(kv->dtype, ks, vs, kv->k, kv->v, g->n_kv, p0, m, kv->ring_capacity, st);
   if (e == cudaSuccess)

@@ -464,13 +464,15 @@ __device__ __forceinline__ void mma_q_from_smem(MmaQ& Q, const float* q_s) {
   }
 }
 
-// One warp folds an n-row tile into its state (bf16 K and V half-stages).
-// p_w: the warp's 16 x 4 fp32 probability scratch.  Rows n..15 of the V
-// half-stage are zeroed first (their probability is 0, and 0 * a non-finite
-// stale value would not be).
-__device__ __forceinline__ void attn_tile_mma(unsigned char* kst, unsigned char* vst, int n,
-                                              const MmaQ& Q, float* p_w, float scale_log2,
-                                              MmaState& st) {
+// One warp folds rows [row_lo, n) of a tile into its state (bf16 K and V
+// half-stages); rows outside take probability 0.  p_w: the warp's 16 x 4 fp32
+// probability scratch.  kZeroTail: rows n..15 of the V half-stage are zeroed
+// first (their probability is 0, and 0 * a non-finite stale value would not
+// be); without it the caller has zeroed them, or they hold finite rows.
+template <bool kZeroTail>
+__device__ __forceinline__ void attn_tile_mma_rows(unsigned char* kst, unsigned char* vst, int row_lo, int n,
+                                                   const MmaQ& Q, float* p_w, float scale_log2,
+                                                   MmaState& st) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
   const int mi = lane >> 3, lr = lane & 7;
@@ -487,7 +489,7 @@ __device__ __forceinline__ void attn_tile_mma(unsigned char* kst, unsigned char*
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) c[i] += c2[i];
-  if (n < kTile) {
+  if (kZeroTail && n < kTile) {
     for (int r = n; r < kTile; ++r)
       *reinterpret_cast<uint4*>(vst + (lane >> 3) * kSubBytes + r * kLine + (lane & 7) * 16) =
           make_uint4(0u, 0u, 0u, 0u);
@@ -497,10 +499,11 @@ __device__ __forceinline__ void attn_tile_mma(unsigned char* kst, unsigned char*
   float sc[2][2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(0xffffffffu, c[i], 2);
-  sc[0][0] = g < n ? c[0] * scale_log2 : -INFINITY;
-  sc[0][1] = g < n ? c[1] * scale_log2 : -INFINITY;
-  sc[1][0] = g + 8 < n ? c[2] * scale_log2 : -INFINITY;
-  sc[1][1] = g + 8 < n ? c[3] * scale_log2 : -INFINITY;
+  const bool in0 = g >= row_lo && g < n, in1 = g + 8 >= row_lo && g + 8 < n;
+  sc[0][0] = in0 ? c[0] * scale_log2 : -INFINITY;
+  sc[0][1] = in0 ? c[1] * scale_log2 : -INFINITY;
+  sc[1][0] = in1 ? c[2] * scale_log2 : -INFINITY;
+  sc[1][1] = in1 ? c[3] * scale_log2 : -INFINITY;
   // online softmax over the tile's rows (the 8 lanes sharing t)
   float pr[2][2], corr[2];
 #pragma unroll
@@ -553,6 +556,13 @@ __device__ __forceinline__ void attn_tile_mma(unsigned char* kst, unsigned char*
     ldsm_x4_trans(tile_chunk(vbase, lr + 8 * (mi >> 1), 16 * mt + 8 * (mi & 1)), a);
     mma_16816(st.o[mt], a, pb0, pb1);
   }
+}
+
+// The decode kernels' tile: rows [0, n), the stale tail zeroed here.
+__device__ __forceinline__ void attn_tile_mma(unsigned char* kst, unsigned char* vst, int n,
+                                              const MmaQ& Q, float* p_w, float scale_log2,
+                                              MmaState& st) {
+  attn_tile_mma_rows<true>(kst, vst, 0, n, Q, p_w, scale_log2, st);
 }
 
 // Put one warp's tensor-core state into the merge scratch in the layout

@@ -37,6 +37,15 @@ cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, con
                              int n_ctas, const void* l2_prefetch, size_t l2_prefetch_bytes,
                              cudaStream_t st, const ChunkSrc& chunk = ChunkSrc());
 
+// The same attention for a chunk, grouped by query (attn_chunk.cu): one CTA
+// per (group of consecutive tokens, KV head) reads the union of the tokens'
+// windows once.  Applies to bf16 caches when the groups cover the GPU.
+bool attention_chunk_grouped_applies(int cdtype, int m, int n_kv);
+cudaError_t launch_attention_chunk_grouped(const float* q_rot, const void* kc, const void* vc, int n_kv,
+                                           int64_t capacity, int ring_capacity, bool full, int window,
+                                           float scale, int64_t p0, int m, const void* ks, const void* vs,
+                                           float* a, uint32_t* err, cudaStream_t st);
+
 // Copy a chunk's staged rows into their cache slots (after attention).
 cudaError_t launch_commit_rows(int cdtype, const void* ks, const void* vs, void* kc, void* vc,
                                int n_kv, int64_t p0, int m, int ring_capacity, cudaStream_t st);

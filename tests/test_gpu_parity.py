@@ -555,6 +555,12 @@ PREFILL_CASES = [
     ("sliding_ring_outgrown", False, 512, 512, 300, 600, "bf16"),
     ("sliding_f32", False, 512, 512, 40, 3, "f32"),
     ("sliding_linear", False, 0, 2048, 1500, 20, "bf16"),
+    # chunks long enough for the query-grouped kernel (one CTA per 4 tokens and KV head)
+    ("grouped_full_p700_m300", True, 0, 1024, 700, 300, "bf16"),
+    ("grouped_full_p0_m161", True, 0, 200, 0, 161, "bf16"),
+    ("grouped_sliding_ring_wraps", False, 512, 512, 1000, 257, "bf16"),
+    ("grouped_sliding_ring_fills", False, 512, 512, 300, 400, "bf16"),
+    ("grouped_sliding_linear", False, 0, 2048, 1500, 170, "bf16"),
 ]
 
 
@@ -598,6 +604,27 @@ def test_prefill_chunk_matches_oracle(B, case):
             assert np.array_equal(got_k[slot], want_k[slot]), f"k slot {slot} changed"
             assert np.array_equal(got_v[slot], want_v[slot]), f"v slot {slot} changed"
     assert int(changed.sum()) == (min(m, ring) if ring > 0 else m)
+
+
+def test_prefill_grouped_ignores_non_finite_unused_rows(B):
+    # cache rows the chunk does not read (positions >= p0 of a linear cache)
+    # hold NaN: the short tiles' stale rows must not reach any token
+    is_full, ring, cap, p0, m = True, 0, 1024, 700, 200
+    wl, w, kc, vc, h = _prefill_inputs(is_full, ring, cap, p0, m, "bf16", 4242)
+    kc[0, p0:] = float("nan")
+    vc[0, p0:] = float("nan")
+    kc0, vc0 = kc.clone(), vc.clone()
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, m)
+    out = torch.empty_like(h)
+    B.spark_attn_prefill(geom, h, B.LayerWeights(**w), B.KvLayer(kc, vc, ring), B.SPARK_FULL, p0, out, ws)
+    torch.cuda.synchronize()
+    assert B.spark_attn_error_word(ws) == 0
+    res = oracle.prefill_chunk(oracle_geom(wl), synth.to_numpy(h).astype(np.float64), np_weights(w),
+                               synth.to_numpy(kc0[0]), synth.to_numpy(vc0[0]), is_full, p0, ring)
+    got_o = out.cpu().numpy().astype(np.float64) - h.cpu().numpy().astype(np.float64)
+    for t in range(m):
+        assert_close(got_o[t], res["o"][t], f"token {t} o")
 
 
 def test_prefill_one_token_agrees_with_decode(B):
