@@ -24,8 +24,12 @@
 namespace spark {
 namespace {
 
+// Measured at 256-1024 tokens (p0 700, full + sliding): 4 tokens per CTA,
+// two CTAs per SM, a 4-stage ring.  8 tokens per CTA (one CTA per SM, 4 or 8
+// stages) was 2-4% slower, a 6-stage ring 15% slower (one CTA per SM).
 constexpr int kChunkStages = 4;
 constexpr int kChunkGroup = 4;  // consecutive tokens per CTA (one consumer warp each)
+constexpr int kChunkMinBlocks = 2;
 
 template <int NC>
 struct ChunkSmem {
@@ -272,7 +276,7 @@ cudaError_t launch_attention_chunk_grouped(const float* q_rot, const void* kc, c
       !chunk_cache_map(&mks, ks, n_kv, m) || !chunk_cache_map(&mvs, vs, n_kv, m))
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * 1.4426950408889634f;
-  return launch_nc<kChunkGroup, 2>(mk, mv, mks, mvs, p0, m, q_rot, a, err, n_kv, ring_capacity, full, window,
+  return launch_nc<kChunkGroup, kChunkMinBlocks>(mk, mv, mks, mvs, p0, m, q_rot, a, err, n_kv, ring_capacity, full, window,
                                    scale_log2, st);
 }
 
