@@ -82,7 +82,7 @@ struct WsLayout {
   size_t a = 0;         // f32 [batch][q_dim] attention output
   size_t hbuf = 0;      // f32 [2][batch][hidden] residual stream between layers
   size_t part = 0;      // f32 [kMaxAttnCtas + batch * n_kv][kPartFloats]
-  size_t mx = 0;        // bf16 [2][bpad][max(hidden, q_dim)] projection inputs (hi, lo); bpad as below
+  size_t mx = 0;        // bf16 [chunk][2][bpad][max(hidden, q_dim)] projection inputs (hi, lo)
   size_t mcs = 0;       // f32x2 [batch][head_dim / 2] rope (cos, sin) of each sequence
   size_t mpart = 0;     // f32 [kMmaMaxCtas][kMmaTileRows][min(batch, kMmaMaxSeq) rounded to 8]
   size_t mtick = 0;     // uint32 [kMmaMaxCtas] split-K tickets of the projection tiles
@@ -94,6 +94,13 @@ struct WsLayout {
 constexpr int kTraceWords = 4096;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Padded sequences of the tensor-core projections' activation rows: chunks
+// of kMmaMaxSeq, or one chunk rounded up to 8.
+inline size_t mma_padded_rows(int batch) {
+  return batch > kMmaMaxSeq ? (size_t)(batch + kMmaMaxSeq - 1) / kMmaMaxSeq * kMmaMaxSeq
+                            : (size_t)(batch + 7) / 8 * 8;
+}
 
 inline WsLayout ws_layout(int hidden, int n_q, int n_kv, int batch) {
   WsLayout L;
@@ -115,7 +122,7 @@ inline WsLayout ws_layout(int hidden, int n_q, int n_kv, int batch) {
   const size_t kmax = (size_t)(hidden > n_q * kHeadDim ? hidden : n_q * kHeadDim);
   const size_t bpad = (size_t)((batch < kMmaMaxSeq ? batch : kMmaMaxSeq) + 7) / 8 * 8;
   L.mx = off;
-  off = align_up(off + 2 * 2 * bpad * kmax, 256);
+  off = align_up(off + 2 * 2 * mma_padded_rows(batch) * kmax, 256);
   L.mcs = off;
   off = align_up(off + sizeof(float) * (size_t)batch * kHeadDim, 256);
   L.mpart = off;
@@ -139,8 +146,8 @@ struct MlpWsLayout {
   size_t err = 0;    // uint32 error word
   size_t mtick = 0;  // uint32 [kMmaMaxCtas] split-K tickets
   size_t m = 0;      // f32 [batch][inter] GELU products (GEMV path)
-  size_t mx = 0;     // bf16 [2][bpad][hidden] normed activation rows (hi, lo)
-  size_t md = 0;     // bf16 [2][bpad][inter] GELU product rows (hi, lo)
+  size_t mx = 0;     // bf16 [chunk][2][bpad][hidden] normed activation rows (hi, lo)
+  size_t md = 0;     // bf16 [chunk][2][bpad][inter] GELU product rows (hi, lo)
   size_t mpart = 0;  // f32 [kMmaMaxCtas][kMmaTileRows][bpad] split-K partials
   size_t trace = 0;  // u64 [kTraceWords] opt-in phase stamps
   size_t total = 0;
@@ -154,9 +161,9 @@ inline MlpWsLayout mlp_ws_layout(int hidden, int inter, int batch) {
   L.m = off;
   off = align_up(off + sizeof(float) * (size_t)batch * inter, 256);
   L.mx = off;
-  off = align_up(off + 2 * 2 * bpad * (size_t)hidden, 256);
+  off = align_up(off + 2 * 2 * mma_padded_rows(batch) * (size_t)hidden, 256);
   L.md = off;
-  off = align_up(off + 2 * 2 * bpad * (size_t)inter, 256);
+  off = align_up(off + 2 * 2 * mma_padded_rows(batch) * (size_t)inter, 256);
   L.mpart = off;
   off = align_up(off + sizeof(float) * (size_t)kMmaMaxCtas * kMmaTileRows * bpad, 256);
   L.trace = off;

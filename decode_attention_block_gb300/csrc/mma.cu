@@ -224,12 +224,21 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // ---------------------------------------------------------------------------
 struct PrepArgs {
   double inv_freq[kMaxPairs];  // theta^(-2i/r) for i < r/2, in double (host)
-  int32_t pos[kMmaMaxSeq];
+  int32_t pos[SPARK_MAX_BATCH];
 };
 
-// One CTA per (padded) sequence: x = RMSNorm(h_b) * w ("plain w", eps inside
-// the root) split into the rows hi[b] and lo[b] of `x` ([2][bpad][hidden]);
-// padded sequences get zero rows.  Also the rope table of sequence b:
+// Row pointers of padded sequence bb (of a launch's chunks of bpad) in the
+// activation rows [chunk][2][bpad][k]: hi, then lo.
+__device__ __forceinline__ void chunk_rows(__nv_bfloat16* x, int bb, int bpad, int k, __nv_bfloat16*& xh,
+                                           __nv_bfloat16*& xl) {
+  const int c = bb / bpad, b = bb - c * bpad;
+  xh = x + ((size_t)c * 2 * bpad + b) * k;
+  xl = x + ((size_t)c * 2 * bpad + bpad + b) * k;
+}
+
+// One CTA per (padded) sequence b: x = RMSNorm(h_b) * w ("plain w", eps
+// inside the root) split into its hi and lo rows (chunk_rows); padded
+// sequences get zero rows.  Also the rope table of sequence b:
 // cs[b][i] = (cos, sin) of pos_b * theta^(-2i/r), the angle formed and
 // reduced modulo 2 pi in double (at position 131072 an fp32 angle would be
 // off by ~1e-2 rad), then evaluated in fp32.
@@ -239,8 +248,8 @@ k_prep_norm(const float* __restrict__ h, const __nv_bfloat16* __restrict__ norm_
             float eps, int rotary_dim, const __grid_constant__ PrepArgs args) {
   __shared__ float red[kPrepThreads / 32];
   const int b = blockIdx.x;
-  __nv_bfloat16* xh = x + (size_t)b * hidden;
-  __nv_bfloat16* xl = x + (size_t)(bpad + b) * hidden;
+  __nv_bfloat16 *xh, *xl;
+  chunk_rows(x, b, bpad, hidden, xh, xl);
   pdl_wait();
   pdl_trigger();
   if (b >= nb) {
@@ -282,8 +291,8 @@ __global__ void __launch_bounds__(kPrepThreads)
 k_prep_gate(const float* __restrict__ a, const float* __restrict__ g, __nv_bfloat16* __restrict__ x,
             int q_dim, int n_q, int nb, int bpad) {
   const int b = blockIdx.x;
-  __nv_bfloat16* xh = x + (size_t)b * q_dim;
-  __nv_bfloat16* xl = x + (size_t)(bpad + b) * q_dim;
+  __nv_bfloat16 *xh, *xl;
+  chunk_rows(x, b, bpad, q_dim, xh, xl);
   pdl_wait();
   pdl_trigger();
   if (b >= nb) {
@@ -310,8 +319,10 @@ struct MmaParams {
   int n_main_tiles;   // tiles over the main weight (the g tile follows them)
   int splits;         // K pieces per tile
   int kblocks;        // K / 64
-  int bpad;           // sequences of this chunk rounded up to 8 (N = 2 * bpad)
-  int nb;             // sequences of this chunk
+  int bpad;           // sequences of a chunk rounded up to 8 (N = 2 * bpad)
+  int nb;             // sequences of the launch (all chunks)
+  int chunks;         // chunks of bpad sequences in the launch (1 up to 128 sequences)
+  int seq0;           // first sequence of this CTA's chunk (set in the kernel)
   int stages;         // pipeline depth
   int tmem_cols;      // allocated accumulator columns (power of two >= 2 * bpad)
   int split_halves;   // qkv: a tile pairs head dims d and d + 128 (rotary_dim 256)
@@ -349,7 +360,7 @@ __device__ __forceinline__ void stamp(const MmaParams& p, int ev) {
 }
 
 struct MmaSeq {
-  int32_t slot[kMmaMaxSeq];  // cache row each sequence writes (qkv)
+  int32_t slot[SPARK_MAX_BATCH];  // cache row each sequence writes (qkv)
 };
 
 constexpr int kMaxSplits = 8;
@@ -584,7 +595,7 @@ __device__ __forceinline__ void epilogue_qkv(const MmaParams& p, const MmaSeq& s
     if (kind == 0) {
       *reinterpret_cast<float4*>(p.q_rot + (size_t)b * q_dim + R0) = make_float4(val[0], val[1], val[2], val[3]);
     } else {
-      CT* dst = cache + (((size_t)b * p.capacity + seq.slot[b]) * p.n_kv + head) * kHeadDim + dd[0];
+      CT* dst = cache + (((size_t)b * p.capacity + seq.slot[p.seq0 + b]) * p.n_kv + head) * kHeadDim + dd[0];
       store_cache4(dst, val);
     }
   }
@@ -619,7 +630,7 @@ __device__ __forceinline__ void epilogue(const MmaParams& p, const MmaSeq& seq, 
 template <int E, typename CT>
 __global__ void __launch_bounds__(kMmaThreads, 1)
 k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_g,
-           const __grid_constant__ CUtensorMap tm_x, const MmaParams p,
+           const __grid_constant__ CUtensorMap tm_x, const MmaParams pk,
            const __grid_constant__ MmaSeq seq) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -631,8 +642,27 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   __shared__ int abort_flag, last_flag, no_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / p.splits;
-  const int split = blockIdx.x - tile * p.splits;
+  // CTA = (tile, chunk, split), split fastest (a cluster's CTAs are
+  // consecutive), then chunk: the chunks of one weight tile run side by side
+  // and all but the first find its rows in L2
+  const int cta = blockIdx.x / pk.splits;
+  const int split = blockIdx.x - cta * pk.splits;
+  const int chunk = cta % pk.chunks, tile = cta / pk.chunks;
+  MmaParams p = pk;  // this chunk's view: its sequences and their outputs
+  p.seq0 = chunk * pk.bpad;
+  p.nb = pk.nb - p.seq0 < pk.bpad ? pk.nb - p.seq0 : pk.bpad;
+  if (chunk > 0) {
+    const size_t s0 = (size_t)p.seq0;
+    if (p.q_rot) p.q_rot += s0 * p.n_q * kHeadDim;
+    if (p.g_out) p.g_out += s0 * p.n_q;
+    if (p.cs) p.cs += s0 * kMaxPairs;
+    if (p.kc) p.kc = static_cast<CT*>(p.kc) + s0 * p.capacity * p.n_kv * kHeadDim;
+    if (p.vc) p.vc = static_cast<CT*>(p.vc) + s0 * p.capacity * p.n_kv * kHeadDim;
+    if (p.h) p.h += s0 * p.hidden;
+    if (p.out) p.out += s0 * p.hidden;
+    if (p.xd) p.xd += (size_t)chunk * 2 * p.bpad * p.inter;
+  }
+  const int x_row = chunk * 2 * pk.bpad;  // this chunk's activation rows in the tensor map
   const int kb0 = split * p.kblocks / p.splits;
   const int nk = (split + 1) * p.kblocks / p.splits - kb0;
   const bool g_tile = E == kEpiQkv && tile >= p.n_main_tiles;
@@ -700,7 +730,7 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
       pdl_trigger();
       fence_proxy_async_global();
       for (int i = 0; i < pre; ++i)
-        tma_load_2d(stage(i) + kABytes, &tm_x, &full_bar[i], (kb0 + i) * kKBlock, 0);
+        tma_load_2d(stage(i) + kABytes, &tm_x, &full_bar[i], (kb0 + i) * kKBlock, x_row);
       stamp(p, kTrXIssued);
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -712,7 +742,7 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         }
         mbar_arrive_expect_tx(&full_bar[s], a_bytes + x_bytes);
         load_w(s, kb0 + i);
-        tma_load_2d(stage(s) + kABytes, &tm_x, &full_bar[s], (kb0 + i) * kKBlock, 0);
+        tma_load_2d(stage(s) + kABytes, &tm_x, &full_bar[s], (kb0 + i) * kKBlock, x_row);
         issued = i + 1;
       }
       if (*abort_v) {
@@ -836,13 +866,13 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     const int m = (warp & 3) * 32 + lane;
     float* Y = reinterpret_cast<float*>(smem);
     // the last CTA of the tile to finish (a ticket) adds the pieces
-    const float* parts = p.part + (size_t)tile * p.splits * kMmaTileRows * p.bpad;
+    const float* parts = p.part + (size_t)cta * p.splits * kMmaTileRows * p.bpad;
     __threadfence();
     named_bar_sync(kBarEpi, kEpiThreads);
     if (et == 0) {
-      const uint32_t t = atomicAdd(&p.tickets[tile], 1u);
+      const uint32_t t = atomicAdd(&p.tickets[cta], 1u);
       const int last = t == (uint32_t)(p.splits - 1);
-      if (last) p.tickets[tile] = 0u;  // every piece has arrived: ready for the next launch
+      if (last) p.tickets[cta] = 0u;  // every piece has arrived: ready for the next launch
       last_flag = last;
       stamp(p, kTrTicket);
     }
@@ -915,9 +945,11 @@ Plan plan_with(int tiles, int kblocks, int bpad, int s) {
   return P;
 }
 
-// Split K so that the tiles cover the SMs once.
-int default_splits(int tiles, int kblocks) {
-  int s = device_sm_count() / tiles;
+// Split K so that the tiles cover the SMs once (a launch of several chunks:
+// the nearest multiple, e.g. 80 (tile, chunk) pairs on 152 SMs -> 2).
+int default_splits(int tiles, int kblocks, bool chunked) {
+  const int sms = device_sm_count();
+  int s = chunked ? (sms + tiles / 2) / tiles : sms / tiles;
   if (s > kMaxSplits) s = kMaxSplits;
   if (s > kblocks) s = kblocks;
   if (s * tiles > kMmaMaxCtas) s = kMmaMaxCtas / tiles;
@@ -947,8 +979,8 @@ cudaLaunchConfig_t launch_config(const Plan& P, cudaStream_t st, cudaLaunchAttri
 // prefill of 512 tokens 0.832 -> 0.740 ms); otherwise, or if no cluster
 // shape fits in one wave, the workspace-ticket reduction.
 template <typename K>
-Plan choose_plan_uncached(K kern, int tiles, int kblocks, int bpad, cudaStream_t st) {
-  const int s0 = default_splits(tiles, kblocks);
+Plan choose_plan_uncached(K kern, int tiles, int kblocks, int bpad, bool chunked, cudaStream_t st) {
+  const int s0 = default_splits(tiles, kblocks, chunked);
   // Below kClusterMinBpad sequences the epilogue is short and the smaller
   // cluster grid streams weights more slowly (batch 8: qkv 15.4 -> 16.4 us).
   for (int s = s0; s >= 2 && bpad >= kClusterMinBpad; --s) {
@@ -966,20 +998,21 @@ Plan choose_plan_uncached(K kern, int tiles, int kblocks, int bpad, cudaStream_t
   return plan_with(tiles, kblocks, bpad, s0);
 }
 
-// choose_plan_uncached, remembered per kernel, device and shape
+// choose_plan_uncached, remembered per kernel, device and shape; `tiles`
+// counts (tile, chunk) pairs
 template <typename K>
-Plan choose_plan(K kern, int tiles, int kblocks, int bpad, cudaStream_t st) {
+Plan choose_plan(K kern, int tiles, int kblocks, int bpad, bool chunked, cudaStream_t st) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int>, Plan> memo;
+  static std::map<std::tuple<int, int, int, int, int>, Plan> memo;
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto key = std::make_tuple(dev, tiles, kblocks, bpad);
+  const auto key = std::make_tuple(dev, tiles, kblocks, bpad, chunked ? 1 : 0);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = memo.find(key);
     if (it != memo.end()) return it->second;
   }
-  const Plan P = choose_plan_uncached(kern, tiles, kblocks, bpad, st);
+  const Plan P = choose_plan_uncached(kern, tiles, kblocks, bpad, chunked, st);
   std::lock_guard<std::mutex> lock(mu);
   memo[key] = P;
   return P;
@@ -989,7 +1022,7 @@ template <int E, typename CT>
 cudaError_t launch_gemm(const CUtensorMap& tw, const CUtensorMap& tg, const CUtensorMap& tx,
                         MmaParams p, const MmaSeq& seq, int tiles, cudaStream_t st) {
   auto kern = k_proj_mma<E, CT>;
-  Plan P = choose_plan(kern, tiles, p.kblocks, p.bpad, st);
+  Plan P = choose_plan(kern, tiles * p.chunks, p.kblocks, p.bpad, p.chunks > 1, st);
   if (P.smem > kMaxDynSmem) return cudaErrorInvalidValue;
   // A grid of one to two CTAs per SM (the up GEMM's 160 tiles): a shallower
   // pipeline that lets two CTAs share an SM runs them all at once instead of
@@ -1031,182 +1064,173 @@ bool mma_projections_supported(int wdtype, int hidden, int n_q, int rotary_dim) 
          (rotary_dim <= kMmaTileRows || rotary_dim == kHeadDim) && tensor_map_encoder() != nullptr;
 }
 
+// The sequences of a launch: chunks of kMmaMaxSeq (the 256 hi/lo columns of
+// one MMA), padded to 8 when there is a single chunk.
+struct Chunking {
+  int chunks, bpad;
+};
+Chunking chunking(int batch) {
+  Chunking c;
+  c.chunks = (batch + kMmaMaxSeq - 1) / kMmaMaxSeq;
+  c.bpad = c.chunks > 1 ? kMmaMaxSeq : (batch + 7) / 8 * 8;
+  return c;
+}
+
 cudaError_t launch_qkv_mma(int cdtype, const float* h, const void* norm_w, const void* qkv_w,
                            const void* g_w, float* q_rot, void* kc, void* vc, float* g_out,
                            uint32_t* err, int hidden, int n_q, int n_kv, int batch, int64_t capacity,
                            int ring_capacity, int rotary_dim, double theta, float eps,
                            const int32_t* positions, const MmaWorkspace& ws, cudaStream_t st) {
-  const int q_dim = n_q * kHeadDim;
   const int rows = (n_q + 2 * n_kv) * kHeadDim;
-  CUtensorMap tw, tg;
-  if (!make_bf16_map(&tw, qkv_w, hidden, rows, kBoxRows) || !make_bf16_map(&tg, g_w, hidden, n_q, n_q))
+  CUtensorMap tw, tg, tx;
+  const Chunking ch = chunking(batch);
+  if (!make_bf16_map(&tw, qkv_w, hidden, rows, kBoxRows) || !make_bf16_map(&tg, g_w, hidden, n_q, n_q) ||
+      !make_bf16_map(&tx, ws.x, hidden, (int64_t)ch.chunks * 2 * ch.bpad, 2 * ch.bpad))
     return cudaErrorInvalidValue;
   PrepArgs pa;
   for (int i = 0; i < kMaxPairs; ++i)
     pa.inv_freq[i] = i < rotary_dim / 2 ? pow(theta, -2.0 * i / (double)rotary_dim) : 0.0;
-  const size_t ce = cdtype == SPARK_BF16 ? 2 : 4;
-  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
-    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
-    const int bpad = (nb + 7) / 8 * 8;
-    MmaSeq seq;
-    for (int b = 0; b < kMmaMaxSeq; ++b) {
-      pa.pos[b] = b < nb ? positions[b0 + b] : 0;
-      seq.slot[b] = b < nb ? (int32_t)write_slot_of(positions[b0 + b], ring_capacity) : 0;
-    }
-    float2* cs = ws.cs + (size_t)b0 * kMaxPairs;
-    cudaError_t e = launch_pdl(k_prep_norm, dim3(bpad), dim3(kPrepThreads), 0, st,
-                               h + (size_t)b0 * hidden, static_cast<const __nv_bfloat16*>(norm_w), ws.x,
-                               cs, hidden, nb, bpad, eps, rotary_dim, pa);
-    if (e != cudaSuccess) return e;
-    CUtensorMap tx;
-    if (!make_bf16_map(&tx, ws.x, hidden, 2 * bpad, 2 * bpad)) return cudaErrorInvalidValue;
-    MmaParams p = {};
-    p.n_main_tiles = rows / kMmaTileRows;
-    p.kblocks = hidden / kKBlock;
-    p.bpad = bpad;
-    p.nb = nb;
-    p.split_halves = rotary_dim == kHeadDim ? 1 : 0;
-    p.g_rows = n_q;
-    p.q_rot = q_rot + (size_t)b0 * q_dim;
-    const size_t coff = (size_t)b0 * capacity * n_kv * kHeadDim * ce;
-    p.kc = static_cast<unsigned char*>(kc) + coff;
-    p.vc = static_cast<unsigned char*>(vc) + coff;
-    p.g_out = g_out + (size_t)b0 * n_q;
-    p.cs = cs;
-    p.n_q = n_q;
-    p.n_kv = n_kv;
-    p.rotary_dim = rotary_dim;
-    p.capacity = capacity;
-    p.hidden = hidden;
-    p.part = ws.part;
-    p.tickets = ws.tickets;
-    p.err = err;
-    p.trace = ws.trace;
-    const int tiles = p.n_main_tiles + 1;
-    e = cdtype == SPARK_BF16 ? launch_gemm<kEpiQkv, __nv_bfloat16>(tw, tg, tx, p, seq, tiles, st)
-                             : launch_gemm<kEpiQkv, float>(tw, tg, tx, p, seq, tiles, st);
-    if (e != cudaSuccess) return e;
+  MmaSeq seq;
+  for (int b = 0; b < SPARK_MAX_BATCH; ++b) {
+    pa.pos[b] = b < batch ? positions[b] : 0;
+    seq.slot[b] = b < batch ? (int32_t)write_slot_of(positions[b], ring_capacity) : 0;
   }
-  return cudaSuccess;
+  cudaError_t e = launch_pdl(k_prep_norm, dim3(ch.chunks * ch.bpad), dim3(kPrepThreads), 0, st, h,
+                             static_cast<const __nv_bfloat16*>(norm_w), ws.x, ws.cs, hidden, batch, ch.bpad, eps,
+                             rotary_dim, pa);
+  if (e != cudaSuccess) return e;
+  MmaParams p = {};
+  p.n_main_tiles = rows / kMmaTileRows;
+  p.kblocks = hidden / kKBlock;
+  p.bpad = ch.bpad;
+  p.nb = batch;
+  p.chunks = ch.chunks;
+  p.split_halves = rotary_dim == kHeadDim ? 1 : 0;
+  p.g_rows = n_q;
+  p.q_rot = q_rot;
+  p.kc = kc;
+  p.vc = vc;
+  p.g_out = g_out;
+  p.cs = ws.cs;
+  p.n_q = n_q;
+  p.n_kv = n_kv;
+  p.rotary_dim = rotary_dim;
+  p.capacity = capacity;
+  p.hidden = hidden;
+  p.part = ws.part;
+  p.tickets = ws.tickets;
+  p.err = err;
+  p.trace = ws.trace;
+  const int tiles = p.n_main_tiles + 1;
+  return cdtype == SPARK_BF16 ? launch_gemm<kEpiQkv, __nv_bfloat16>(tw, tg, tx, p, seq, tiles, st)
+                              : launch_gemm<kEpiQkv, float>(tw, tg, tx, p, seq, tiles, st);
 }
 
 cudaError_t launch_oproj_mma(const float* a, const float* g, const float* h, const void* o_w,
                              float* out, uint32_t* err, int hidden, int n_q, int batch,
                              const MmaWorkspace& ws, cudaStream_t st) {
   const int q_dim = n_q * kHeadDim;
-  CUtensorMap tw;
-  if (!make_bf16_map(&tw, o_w, q_dim, hidden, kBoxRows)) return cudaErrorInvalidValue;
-  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
-    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
-    const int bpad = (nb + 7) / 8 * 8;
-    cudaError_t e = launch_pdl(k_prep_gate, dim3(bpad), dim3(kPrepThreads), 0, st, a + (size_t)b0 * q_dim,
-                               g + (size_t)b0 * n_q, ws.x, q_dim, n_q, nb, bpad);
-    if (e != cudaSuccess) return e;
-    CUtensorMap tx;
-    if (!make_bf16_map(&tx, ws.x, q_dim, 2 * bpad, 2 * bpad)) return cudaErrorInvalidValue;
-    MmaParams p = {};
-    p.n_main_tiles = (hidden + kMmaTileRows - 1) / kMmaTileRows;
-    p.kblocks = q_dim / kKBlock;
-    p.bpad = bpad;
-    p.nb = nb;
-    p.h = h + (size_t)b0 * hidden;
-    p.out = out + (size_t)b0 * hidden;
-    p.hidden = hidden;
-    p.part = ws.part;
-    p.tickets = ws.tickets;
-    p.err = err;
-    p.trace = ws.trace;
-    MmaSeq seq = {};
-    e = launch_gemm<kEpiO, float>(tw, tw, tx, p, seq, p.n_main_tiles, st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  const Chunking ch = chunking(batch);
+  CUtensorMap tw, tx;
+  if (!make_bf16_map(&tw, o_w, q_dim, hidden, kBoxRows) ||
+      !make_bf16_map(&tx, ws.x, q_dim, (int64_t)ch.chunks * 2 * ch.bpad, 2 * ch.bpad))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(k_prep_gate, dim3(ch.chunks * ch.bpad), dim3(kPrepThreads), 0, st, a, g, ws.x, q_dim,
+                             n_q, batch, ch.bpad);
+  if (e != cudaSuccess) return e;
+  MmaParams p = {};
+  p.n_main_tiles = (hidden + kMmaTileRows - 1) / kMmaTileRows;
+  p.kblocks = q_dim / kKBlock;
+  p.bpad = ch.bpad;
+  p.nb = batch;
+  p.chunks = ch.chunks;
+  p.h = h;
+  p.out = out;
+  p.hidden = hidden;
+  p.part = ws.part;
+  p.tickets = ws.tickets;
+  p.err = err;
+  p.trace = ws.trace;
+  MmaSeq seq = {};
+  return launch_gemm<kEpiO, float>(tw, tw, tx, p, seq, p.n_main_tiles, st);
 }
 
 cudaError_t launch_mlp_mma(const float* h, const void* norm_w, const void* gate_w, const void* up_w,
                            const void* down_w, float* out, uint32_t* err, int hidden, int inter, int batch,
                            float eps, const MmaWorkspace& ws, __nv_bfloat16* xd, cudaStream_t st) {
-  CUtensorMap tg, tu, td;
+  const Chunking ch = chunking(batch);
+  CUtensorMap tg, tu, td, tx, txd;
   if (!make_bf16_map(&tg, gate_w, hidden, inter, kBoxRows) || !make_bf16_map(&tu, up_w, hidden, inter, kBoxRows) ||
-      !make_bf16_map(&td, down_w, inter, hidden, kBoxRows))
+      !make_bf16_map(&td, down_w, inter, hidden, kBoxRows) ||
+      !make_bf16_map(&tx, ws.x, hidden, (int64_t)ch.chunks * 2 * ch.bpad, 2 * ch.bpad) ||
+      !make_bf16_map(&txd, xd, inter, (int64_t)ch.chunks * 2 * ch.bpad, 2 * ch.bpad))
     return cudaErrorInvalidValue;
   PrepArgs pa = {};  // no rope table
   const int up_tiles = (inter + kBoxRows - 1) / kBoxRows;
   const int down_tiles = (hidden + kMmaTileRows - 1) / kMmaTileRows;
-  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
-    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
-    const int bpad = (nb + 7) / 8 * 8;
-    cudaError_t e = launch_pdl(k_prep_norm, dim3(bpad), dim3(kPrepThreads), 0, st, h + (size_t)b0 * hidden,
-                               static_cast<const __nv_bfloat16*>(norm_w), ws.x, (float2*)nullptr, hidden, nb,
-                               bpad, eps, 0, pa);
-    if (e != cudaSuccess) return e;
-    CUtensorMap tx, txd;
-    if (!make_bf16_map(&tx, ws.x, hidden, 2 * bpad, 2 * bpad) || !make_bf16_map(&txd, xd, inter, 2 * bpad, 2 * bpad))
-      return cudaErrorInvalidValue;
-    MmaSeq seq = {};
-    MmaParams p = {};
-    p.n_main_tiles = up_tiles;
-    p.kblocks = hidden / kKBlock;
-    p.bpad = bpad;
-    p.nb = nb;
-    p.xd = xd;
-    p.inter = inter;
-    p.part = ws.part;
-    p.tickets = ws.tickets;
-    p.err = err;
-    p.trace = ws.trace;
-    e = launch_gemm<kEpiUp, float>(tg, tu, tx, p, seq, up_tiles, st);
-    if (e != cudaSuccess) return e;
-    MmaParams q = {};
-    q.n_main_tiles = down_tiles;
-    q.kblocks = (inter + kKBlock - 1) / kKBlock;  // the last block's columns past inter read as zero
-    q.bpad = bpad;
-    q.nb = nb;
-    q.h = h + (size_t)b0 * hidden;
-    q.out = out + (size_t)b0 * hidden;
-    q.hidden = hidden;
-    q.part = ws.part;
-    q.tickets = ws.tickets;
-    q.err = err;
-    q.trace = ws.trace;
-    e = launch_gemm<kEpiO, float>(td, td, txd, q, seq, down_tiles, st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  cudaError_t e = launch_pdl(k_prep_norm, dim3(ch.chunks * ch.bpad), dim3(kPrepThreads), 0, st, h,
+                             static_cast<const __nv_bfloat16*>(norm_w), ws.x, (float2*)nullptr, hidden, batch,
+                             ch.bpad, eps, 0, pa);
+  if (e != cudaSuccess) return e;
+  MmaSeq seq = {};
+  MmaParams p = {};
+  p.n_main_tiles = up_tiles;
+  p.kblocks = hidden / kKBlock;
+  p.bpad = ch.bpad;
+  p.nb = batch;
+  p.chunks = ch.chunks;
+  p.xd = xd;
+  p.inter = inter;
+  p.part = ws.part;
+  p.tickets = ws.tickets;
+  p.err = err;
+  p.trace = ws.trace;
+  e = launch_gemm<kEpiUp, float>(tg, tu, tx, p, seq, up_tiles, st);
+  if (e != cudaSuccess) return e;
+  MmaParams q = {};
+  q.n_main_tiles = down_tiles;
+  q.kblocks = (inter + kKBlock - 1) / kKBlock;  // the last block's columns past inter read as zero
+  q.bpad = ch.bpad;
+  q.nb = batch;
+  q.chunks = ch.chunks;
+  q.h = h;
+  q.out = out;
+  q.hidden = hidden;
+  q.part = ws.part;
+  q.tickets = ws.tickets;
+  q.err = err;
+  q.trace = ws.trace;
+  return launch_gemm<kEpiO, float>(td, td, txd, q, seq, down_tiles, st);
 }
 
 cudaError_t launch_head_mma(const float* h, const void* norm_w, const void* embed, float* logits, uint32_t* err,
                             int hidden, int vocab, int batch, float eps, const MmaWorkspace& ws, cudaStream_t st) {
-  CUtensorMap te;
-  if (!make_bf16_map(&te, embed, hidden, vocab, kBoxRows)) return cudaErrorInvalidValue;
+  const Chunking ch = chunking(batch);
+  CUtensorMap te, tx;
+  if (!make_bf16_map(&te, embed, hidden, vocab, kBoxRows) ||
+      !make_bf16_map(&tx, ws.x, hidden, (int64_t)ch.chunks * 2 * ch.bpad, 2 * ch.bpad))
+    return cudaErrorInvalidValue;
   PrepArgs pa = {};
   const int tiles = (vocab + kMmaTileRows - 1) / kMmaTileRows;
-  for (int b0 = 0; b0 < batch; b0 += kMmaMaxSeq) {
-    const int nb = batch - b0 < kMmaMaxSeq ? batch - b0 : kMmaMaxSeq;
-    const int bpad = (nb + 7) / 8 * 8;
-    cudaError_t e = launch_pdl(k_prep_norm, dim3(bpad), dim3(kPrepThreads), 0, st, h + (size_t)b0 * hidden,
-                               static_cast<const __nv_bfloat16*>(norm_w), ws.x, (float2*)nullptr, hidden, nb,
-                               bpad, eps, 0, pa);
-    if (e != cudaSuccess) return e;
-    CUtensorMap tx;
-    if (!make_bf16_map(&tx, ws.x, hidden, 2 * bpad, 2 * bpad)) return cudaErrorInvalidValue;
-    MmaSeq seq = {};
-    MmaParams p = {};
-    p.n_main_tiles = tiles;
-    p.kblocks = hidden / kKBlock;
-    p.bpad = bpad;
-    p.nb = nb;
-    p.h = nullptr;  // no residual
-    p.out = logits + (size_t)b0 * vocab;
-    p.hidden = vocab;
-    p.part = ws.part;
-    p.tickets = ws.tickets;
-    p.err = err;
-    p.trace = ws.trace;
-    e = launch_gemm<kEpiO, float>(te, te, tx, p, seq, tiles, st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  cudaError_t e = launch_pdl(k_prep_norm, dim3(ch.chunks * ch.bpad), dim3(kPrepThreads), 0, st, h,
+                             static_cast<const __nv_bfloat16*>(norm_w), ws.x, (float2*)nullptr, hidden, batch,
+                             ch.bpad, eps, 0, pa);
+  if (e != cudaSuccess) return e;
+  MmaSeq seq = {};
+  MmaParams p = {};
+  p.n_main_tiles = tiles;
+  p.kblocks = hidden / kKBlock;
+  p.bpad = ch.bpad;
+  p.nb = batch;
+  p.chunks = ch.chunks;
+  p.h = nullptr;  // no residual
+  p.out = logits;
+  p.hidden = vocab;
+  p.part = ws.part;
+  p.tickets = ws.tickets;
+  p.err = err;
+  p.trace = ws.trace;
+  return launch_gemm<kEpiO, float>(te, te, tx, p, seq, tiles, st);
 }
 
 }  // namespace spark

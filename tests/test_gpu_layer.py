@@ -82,6 +82,8 @@ MLP_SMALL = [
     (256, 12296, 8, torch.bfloat16, "mma"),
     (512, 10248, 64, torch.bfloat16, "mma"),
     (256, 16384, 130, torch.bfloat16, "mma"),
+    # five chunks of 128 sequences in one launch, the last one partial
+    (256, 352, 520, torch.bfloat16, "mma"),
 ]
 
 
@@ -159,6 +161,7 @@ HEAD_SMALL = [
     # more tiles than SMs (several waves), ragged last tile
     (256, 40008, 16, torch.bfloat16, "mma"),
     (512, 20488, 77, torch.bfloat16, "mma"),
+    (256, 1000, 300, torch.bfloat16, "mma"),
 ]
 
 

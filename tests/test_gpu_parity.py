@@ -148,10 +148,10 @@ def _ragged_positions(n, seed, hi=140000):
 
 
 @pytest.mark.parametrize("is_full", [True, False])
-@pytest.mark.parametrize("batch", [5, 8, 64, 130])
+@pytest.mark.parametrize("batch", [5, 8, 64, 130, 300])
 def test_qkv_rope_tensor_core_batches(B, is_full, batch):
     """The batched path: padding to 8 sequences, split-K tiles, and more than
-    128 sequences (two launches)."""
+    128 sequences (chunks of 128 in one launch, the last one partial)."""
     positions = _ragged_positions(batch, 700 + batch)
     if is_full:
         positions = [p % 2048 for p in positions]   # a linear cache holds every position
