@@ -338,7 +338,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     if (cl > 0)
       attn_cta_state<NC>(msm, cst);
     else
-      attn_merge_group<NC>(msm, flags, part, counters, a_head0, g, c, c_first, c_last - c_first + 1);
+      attn_merge_group<NC, 16>(msm, flags, part, counters, a_head0, g, c, c_first, c_last - c_first + 1);
     sh.f = gs + r1;
     if (++sh.j == n_kv) { sh.j = 0; ++sh.b; }
   }
