@@ -13,7 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import torch
 
@@ -174,13 +174,30 @@ def _check(status: int, where: str) -> None:
         raise SparkError(status, where)
 
 
+class _CachedC:
+    """Mixin of the weight and cache descriptors: the C struct is built and
+    checked once and reused while no field is reassigned (the tensors' device
+    addresses do not change in place), which keeps the per-call marshalling
+    of a decode step short."""
+
+    def __setattr__(self, name, value):
+        if name != "_c":
+            object.__setattr__(self, "_c", None)
+        object.__setattr__(self, name, value)
+
+    def to_c(self):
+        if self._c is None:
+            object.__setattr__(self, "_c", self._build_c())
+        return self._c
+
+
 def _positions(positions) -> ctypes.Array:
     vals = [int(p) for p in positions]
     return (ctypes.c_int32 * max(1, len(vals)))(*vals)
 
 
 @dataclass
-class LayerWeights:
+class LayerWeights(_CachedC):
     """One layer's weights as CUDA tensors (all float32 or all bfloat16):
     ``norm_w [hidden]``, ``qkv_w [n_q*d + 2*n_kv*d, hidden]``,
     ``g_w [n_q, hidden]``, ``o_w [hidden, n_q*d]``."""
@@ -189,8 +206,9 @@ class LayerWeights:
     qkv_w: torch.Tensor
     g_w: torch.Tensor
     o_w: torch.Tensor
+    _c: object = field(default=None, init=False, repr=False, compare=False)
 
-    def to_c(self) -> SparkLayerWeights:
+    def _build_c(self) -> SparkLayerWeights:
         dt = self.qkv_w.dtype
         if dt not in _DTYPE_CODE:
             raise TypeError(f"weights must be float32 or bfloat16, got {dt}")
@@ -200,7 +218,7 @@ class LayerWeights:
 
 
 @dataclass
-class KvLayer:
+class KvLayer(_CachedC):
     """One layer's cache as CUDA tensors ``k``, ``v`` of shape
     ``[batch, capacity, n_kv, head_dim]`` (float32 or bfloat16) and the ring
     capacity (0 = linear addressing)."""
@@ -208,8 +226,9 @@ class KvLayer:
     k: torch.Tensor
     v: torch.Tensor
     ring_capacity: int = 0
+    _c: object = field(default=None, init=False, repr=False, compare=False)
 
-    def to_c(self) -> SparkKvLayer:
+    def _build_c(self) -> SparkKvLayer:
         dt = self.k.dtype
         if dt not in _DTYPE_CODE:
             raise TypeError(f"cache must be float32 or bfloat16, got {dt}")
@@ -220,7 +239,7 @@ class KvLayer:
 
 
 @dataclass
-class MlpWeights:
+class MlpWeights(_CachedC):
     """The MLP half of one layer as CUDA tensors (all float32 or all
     bfloat16): ``norm_w [hidden]`` (post_attention_layernorm), ``gate_w`` and
     ``up_w [intermediate, hidden]``, ``down_w [hidden, intermediate]``."""
@@ -229,8 +248,9 @@ class MlpWeights:
     gate_w: torch.Tensor
     up_w: torch.Tensor
     down_w: torch.Tensor
+    _c: object = field(default=None, init=False, repr=False, compare=False)
 
-    def to_c(self) -> SparkMlpWeights:
+    def _build_c(self) -> SparkMlpWeights:
         dt = self.gate_w.dtype
         if dt not in _DTYPE_CODE:
             raise TypeError(f"weights must be float32 or bfloat16, got {dt}")
