@@ -39,6 +39,7 @@ from decode_attention_block_gb300 import build_lib, synth  # noqa: E402
 DEFAULT_WORKLOAD = "full+sliding_bf16_b1_pos700"
 METRIC = "decode attn-block steps/s & tokens/s; achieved HBM GB/s vs ~8 TB/s peak"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------------------
@@ -123,8 +124,9 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)),
+                "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
 
 
 # ---------------------------------------------------------------------------
@@ -474,6 +476,74 @@ def time_oracle(wl: synth.Workload, budget_s: float) -> dict:
                       f"({elapsed:.1f} s, numpy float64, BLAS threads up to {cores} cores)"}
 
 
+def time_oracle_prefill(wl: synth.Workload, m: int, budget_s: float) -> dict:
+    """The float64 oracle on the first tokens of a chunk (prefill_chunk on a
+    prefix of the chunk, each layer on its own inputs), until `budget_s` is
+    spent; the rate is tokens/s through every layer."""
+    import oracle
+
+    geom = oracle.OracleGeometry(hidden=wl.hidden, n_q=wl.n_q, n_kv=wl.n_kv, head_dim=wl.head_dim,
+                                 window=wl.window)
+    p0 = int(wl.positions[0])
+    t_tok = 0.0
+    n_tok = 0
+    for mm in (1, 2, 4, 8, 16):
+        per_layer = []
+        for li, spec in enumerate(wl.layers):
+            w = {k: synth.to_numpy(v) for k, v in synth.make_weights(wl, li, "cpu").items()}
+            cap = spec.ring_capacity if spec.ring_capacity > 0 else p0 + mm
+            g = torch.Generator().manual_seed(wl.seed * 31 + li)
+            dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+            k = synth.to_numpy(torch.randn((cap, wl.n_kv, wl.head_dim), generator=g).to(dt))
+            v = synth.to_numpy(torch.randn((cap, wl.n_kv, wl.head_dim), generator=g).to(dt))
+            h = np.random.default_rng(li).standard_normal((mm, wl.hidden))
+            t0 = time.perf_counter()
+            oracle.prefill_chunk(geom, h, w, k, v, spec.is_full, p0, spec.ring_capacity)
+            per_layer.append(time.perf_counter() - t0)
+        t_tok, n_tok = t_tok + sum(per_layer), n_tok + mm
+        if t_tok >= budget_s or mm >= m:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(n_tok / t_tok, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_tok} tokens in chunks of 1..{mm} from position {p0} through every layer "
+                      f"({t_tok:.1f} s, numpy float64, BLAS threads up to {cores} cores)"}
+
+
+def time_oracle_decoder(wl: synth.Workload, inter: int, vocab: int) -> dict:
+    """The float64 oracle on one sequence of one decoder step: the attention
+    block and MLP half of the first layers (at most 4, the time scaled to
+    every layer), then the head."""
+    import oracle
+
+    geom = oracle.OracleGeometry(hidden=wl.hidden, n_q=wl.n_q, n_kv=wl.n_kv, head_dim=wl.head_dim,
+                                 window=wl.window)
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    h = synth.to_numpy(synth.make_h(wl, "cpu")).astype(np.float64)[:1]
+    pos = [wl.positions[0]]
+    elapsed = 0.0
+    n_l = min(len(wl.layers), 4)
+    for li, spec in enumerate(wl.layers[:n_l]):
+        w = {k: synth.to_numpy(v) for k, v in synth.make_weights(wl, li, "cpu").items()}
+        k, v = synth.make_cache(wl, li, "cpu", sequences=[0])
+        mw = {k_: synth.to_numpy(v_) for k_, v_ in
+              synth.make_mlp_weights(wl.seed * 100 + li, wl.hidden, inter, dt, "cpu").items()}
+        t0 = time.perf_counter()
+        r = oracle.decode_step(geom, h, w, synth.to_numpy(k)[:1], synth.to_numpy(v)[:1], spec.is_full, pos,
+                               spec.ring_capacity)
+        h = oracle.mlp_block(geom, r["out"], mw)["out"]
+        elapsed += time.perf_counter() - t0
+    elapsed *= len(wl.layers) / n_l
+    hd = {k_: synth.to_numpy(v_) for k_, v_ in synth.make_head(wl.seed, wl.hidden, vocab, dt, "cpu").items()}
+    t0 = time.perf_counter()
+    oracle.head_logits(geom, h, hd["norm_w"], hd["embed"])
+    elapsed += time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(1.0 / elapsed, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one sequence through {n_l} of {len(wl.layers)} layers (attention block + MLP half, "
+                      f"time scaled to every layer) and the head "
+                      f"({elapsed:.1f} s, numpy float64, BLAS threads up to {cores} cores)"}
+
+
 def bench_reference(args, wl, rank, world):
     """The reference arm: the float64 CPU oracle as it stands, on the host
     cores, each step a bounded sample of the workload; rank 0 only."""
@@ -573,6 +643,14 @@ def bench_prefill(args, wl):
             "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "flops_per_step": proj_flops + att_flops,
             "tflops": round((proj_flops + att_flops) / (ms * 1e-3) / 1e12, 2),
+            # the chunk's algorithmic FLOPs (projections and attention, without
+            # the hi/lo operand split) against the dense bf16 tensor peak
+            "roofline": {"kernel": "whole chunk (projection GEMMs + grouped attention)", "bound": "tensor",
+                         "achieved": round((proj_flops + att_flops) / (ms * 1e-3) / 1e12, 2),
+                         "peak": peaks["bf16_tflops"], "peak_source": peaks["source"], "unit": "TFLOP/s",
+                         "frac": round((proj_flops + att_flops) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                         "traffic": None},
+            "cpu_baseline": None if args.no_cpu_baseline else time_oracle_prefill(wl, M, 10.0),
             "clocks": sampler.summary()}
 
 
@@ -718,6 +796,7 @@ def bench_decoder(args, wl):
                     "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * V * 4,
                     "launch": "direct calls, synchronised every step"},
             "gpu_launches": launches * steps,
+            "cpu_baseline": None if args.no_cpu_baseline else time_oracle_decoder(wl, I, V),
             "clocks": sampler.summary()}
 
 
