@@ -322,6 +322,7 @@ struct MmaParams {
   int bpad;           // sequences of a chunk rounded up to 8 (N = 2 * bpad)
   int nb;             // sequences of the launch (all chunks)
   int chunks;         // chunks of bpad sequences in the launch (1 up to 128 sequences)
+  int mt;             // 128-row weight tiles per CTA (2: o epilogue, unsplit, two accumulators)
   int seq0;           // first sequence of this CTA's chunk (set in the kernel)
   int stages;         // pipeline depth
   int tmem_cols;      // allocated accumulator columns (power of two >= 2 * bpad)
@@ -667,7 +668,8 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   const int nk = (split + 1) * p.kblocks / p.splits - kb0;
   const bool g_tile = E == kEpiQkv && tile >= p.n_main_tiles;
   const uint32_t x_bytes = (uint32_t)p.bpad * 2u * kRowBytes;
-  const uint32_t a_bytes = g_tile ? (uint32_t)p.g_rows * kRowBytes : kABytes;
+  const int mt = E == kEpiO ? p.mt : 1;  // weight tiles of this CTA, sharing each activation stage
+  const uint32_t a_bytes = g_tile ? (uint32_t)p.g_rows * kRowBytes : kABytes * (uint32_t)mt;
   // sequences the epilogue covers: the up epilogue also zeroes the padded ones
   const int nrows = E == kEpiUp ? p.bpad : p.nb;
   float* const Y0 = reinterpret_cast<float*>(smem);
@@ -716,6 +718,12 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         } else if (E == kEpiUp) {  // gate rows, then the up rows of the same j
           tma_load_2d(stage(s), &tm_w, &full_bar[s], kb * kKBlock, kBoxRows * tile);
           tma_load_2d(stage(s) + kABytes / 2, &tm_g, &full_bar[s], kb * kKBlock, kBoxRows * tile);
+        } else if (mt > 1) {  // tiles mt * tile .. + mt - 1, each as two 64-row boxes
+          for (int h = 0; h < mt; ++h) {
+            const int rr = kMmaTileRows * (mt * tile + h);
+            tma_load_2d(stage(s) + h * kABytes, &tm_w, &full_bar[s], kb * kKBlock, rr);
+            tma_load_2d(stage(s) + h * kABytes + kABytes / 2, &tm_w, &full_bar[s], kb * kKBlock, rr + kBoxRows);
+          }
         } else {
           tma_load_2d(stage(s), &tm_w, &full_bar[s], kb * kKBlock, r0);
           tma_load_2d(stage(s) + kABytes / 2, &tm_w, &full_bar[s], kb * kKBlock, r1);
@@ -730,7 +738,7 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
       pdl_trigger();
       fence_proxy_async_global();
       for (int i = 0; i < pre; ++i)
-        tma_load_2d(stage(i) + kABytes, &tm_x, &full_bar[i], (kb0 + i) * kKBlock, x_row);
+        tma_load_2d(stage(i) + kABytes * mt, &tm_x, &full_bar[i], (kb0 + i) * kKBlock, x_row);
       stamp(p, kTrXIssued);
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
@@ -742,7 +750,7 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         }
         mbar_arrive_expect_tx(&full_bar[s], a_bytes + x_bytes);
         load_w(s, kb0 + i);
-        tma_load_2d(stage(s) + kABytes, &tm_x, &full_bar[s], (kb0 + i) * kKBlock, x_row);
+        tma_load_2d(stage(s) + kABytes * mt, &tm_x, &full_bar[s], (kb0 + i) * kKBlock, x_row);
         issued = i + 1;
       }
       if (*abort_v) {
@@ -772,10 +780,14 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         if (i == 0) stamp(p, kTrFirstFull);
         if (i == nk - 1) stamp(p, kTrLastFull);
         const uint32_t a_addr = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const uint64_t da = sw128_desc(a_addr), dx = sw128_desc(a_addr + kABytes);
+        const uint64_t dx = sw128_desc(a_addr + kABytes * mt);
+        for (int h = 0; h < mt; ++h) {  // accumulator h at columns h * tmem_cols / mt
+          const uint64_t da = sw128_desc(a_addr + h * kABytes);
+          const uint32_t dt = tmem + (uint32_t)(h * (p.tmem_cols / mt));
 #pragma unroll
-        for (int k = 0; k < kKBlock / 16; ++k)
-          mma_bf16(tmem, da + 2u * k, dx + 2u * k, idesc, (i | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < kKBlock / 16; ++k)
+            mma_bf16(dt, da + 2u * k, dx + 2u * k, idesc, (i | k) != 0 ? 1u : 0u);
+        }
         mma_commit(&empty_bar[s]);
       }
       mma_commit(&done_bar);
@@ -859,7 +871,22 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
       const int et = threadIdx.x - 64;
       const int m = (warp & 3) * 32 + lane;
       named_bar_sync(kBarEpi, kEpiThreads);  // every row of Y written
-      epilogue<E, CT>(p, seq, tile, g_tile, Y0, nullptr, 0, nrows, m, et);
+      epilogue<E, CT>(p, seq, mt * tile, g_tile, Y0, nullptr, 0, nrows, m, et);
+      // the CTA's further weight tiles: accumulator h into Y, then its epilogue
+      for (int h = 1; h < mt; ++h) {
+        named_bar_sync(kBarEpi, kEpiThreads);  // Y is free again
+        if (!*abort_v) {
+          const uint32_t trow = tmem + (uint32_t)(h * (p.tmem_cols / mt)) + ((uint32_t)((warp & 3) * 32) << 16);
+          for (int j = 0; j < p.bpad; j += 8) {
+            float hi[8], lo[8];
+            tmem_ld_8x2(trow + (uint32_t)j, trow + (uint32_t)(p.bpad + j), hi, lo);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) Y0[(j + c) * kMmaTileRows + m] = hi[c] + lo[c];
+          }
+        }
+        named_bar_sync(kBarEpi, kEpiThreads);
+        epilogue<E, CT>(p, seq, mt * tile + h, g_tile, Y0, nullptr, 0, nrows, m, et);
+      }
     }
   } else if (warp >= 2) {
     const int et = threadIdx.x - 64;
@@ -1037,6 +1064,33 @@ cudaError_t launch_gemm(const CUtensorMap& tw, const CUtensorMap& tg, const CUte
       if (st2 < P.stages) P.stages = st2;
       const size_t body = (size_t)P.stages * P.stage_bytes;
       P.smem = (body > y ? body : y) + 1024;
+    }
+  }
+  // Grids of more than two waves of unsplit o tiles (the head's 1024): two
+  // weight tiles per CTA share each activation stage, two accumulators, half
+  // the CTAs, so the start-up of a CTA is paid once per 256 weight rows
+  // (head at batch 8: 153 -> 145 us; at batch 64 in the decoder step 158 ->
+  // 144 us).  Only with at least 4 stages: at 128 sequences (3) it was slower.
+  p.mt = 1;
+  if (E == kEpiO && P.splits == 1 && !P.cluster && P.grid > 2 * sms) {
+    Plan Q = P;
+    Q.stage_bytes = 2 * kABytes + (uint32_t)p.bpad * 2u * kRowBytes;
+    int st2 = (int)(kStageBudget / Q.stage_bytes);
+    if (st2 > kMaxStages) st2 = kMaxStages;
+    if (st2 > p.kblocks) st2 = p.kblocks;
+    const size_t y = (sizeof(float) * kMmaTileRows + sizeof(float2) * kBoxRows) * (size_t)p.bpad;
+    if (st2 >= 4 && 2 * P.tmem_cols <= (int)kTmemCols) {
+      Q.stages = st2;
+      const size_t body = (size_t)st2 * Q.stage_bytes;
+      Q.smem = (body > y ? body : y) + 1024;
+      Q.tmem_cols = 2 * P.tmem_cols;
+      const size_t min_smem = kSmemPerSm / (kTmemCols / (uint32_t)Q.tmem_cols + 1) + 1;  // TMEM per SM
+      if (Q.smem < min_smem) Q.smem = min_smem;
+      Q.grid = (tiles + 1) / 2 * p.chunks;
+      if (Q.smem <= kMaxDynSmem) {
+        P = Q;
+        p.mt = 2;
+      }
     }
   }
   p.splits = P.splits;
