@@ -659,38 +659,46 @@ __device__ __forceinline__ void attn_cta_state(const MergeSmem& sm, float* cst) 
 }
 
 // Rank 0 of a cluster, warp h < 4: merge the cl CTA states (DSMEM, rank
-// order, every load issued first) and write head h of the group's output.
+// order, eight ranks' loads issued together per round, a running max across
+// rounds) and write head h of the group's output.
 __device__ __forceinline__ void attn_cluster_merge(const float* cst, int cl, float* a_head0,
                                                    volatile int* flags) {
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float mq[8], lq[8];
-  float4 x0[8], x1[8];
+  float M = -INFINITY, L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int q0 = 0; q0 < cl; q0 += 8) {
+    float mq[8], lq[8];
+    float4 x0[8], x1[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    if (q < cl) {
-      mq[q] = ld_cluster_f32(cluster_addr(cst + h, (uint32_t)q));
-      lq[q] = ld_cluster_f32(cluster_addr(cst + 4 + h, (uint32_t)q));
-      const uint32_t ra = cluster_addr(cst + 8 + h * kHeadDim + 8 * lane, (uint32_t)q);
-      x0[q] = ld_cluster_f4(ra);
-      x1[q] = ld_cluster_f4(ra + 16);
-    } else {
-      mq[q] = -INFINITY;
-      lq[q] = 0.f;
-      x0[q] = x1[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < 8; ++q) {
+      if (q0 + q < cl) {
+        mq[q] = ld_cluster_f32(cluster_addr(cst + h, (uint32_t)(q0 + q)));
+        lq[q] = ld_cluster_f32(cluster_addr(cst + 4 + h, (uint32_t)(q0 + q)));
+        const uint32_t ra = cluster_addr(cst + 8 + h * kHeadDim + 8 * lane, (uint32_t)(q0 + q));
+        x0[q] = ld_cluster_f4(ra);
+        x1[q] = ld_cluster_f4(ra + 16);
+      } else {
+        mq[q] = -INFINITY;
+        lq[q] = 0.f;
+        x0[q] = x1[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-  }
-  float M = -INFINITY;
+    float mb = M;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) M = fmaxf(M, mq[q]);
-  float L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int q = 0; q < 8; ++q) mb = fmaxf(mb, mq[q]);
+    const float rs = M == -INFINITY ? 0.f : exp2f(M - mb);  // rescale the earlier rounds
+    L *= rs;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float scl = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
-    L = fmaf(lq[q], scl, L);
-    O[0] = fmaf(x0[q].x, scl, O[0]); O[1] = fmaf(x0[q].y, scl, O[1]);
-    O[2] = fmaf(x0[q].z, scl, O[2]); O[3] = fmaf(x0[q].w, scl, O[3]);
-    O[4] = fmaf(x1[q].x, scl, O[4]); O[5] = fmaf(x1[q].y, scl, O[5]);
-    O[6] = fmaf(x1[q].z, scl, O[6]); O[7] = fmaf(x1[q].w, scl, O[7]);
+    for (int i = 0; i < 8; ++i) O[i] *= rs;
+    M = mb;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float scl = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
+      L = fmaf(lq[q], scl, L);
+      O[0] = fmaf(x0[q].x, scl, O[0]); O[1] = fmaf(x0[q].y, scl, O[1]);
+      O[2] = fmaf(x0[q].z, scl, O[2]); O[3] = fmaf(x0[q].w, scl, O[3]);
+      O[4] = fmaf(x1[q].x, scl, O[4]); O[5] = fmaf(x1[q].y, scl, O[5]);
+      O[6] = fmaf(x1[q].z, scl, O[6]); O[7] = fmaf(x1[q].w, scl, O[7]);
+    }
   }
   if (!flags[0]) {
     const float inv = 1.0f / L;
