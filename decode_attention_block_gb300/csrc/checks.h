@@ -6,6 +6,11 @@
 
 #include <math.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 
 namespace spark {
@@ -96,12 +101,24 @@ inline void rope_for(const spark_geom* g, int32_t cls, int* rotary_dim, double* 
 // first nb positions, computed in double on the host (at position 131072 an
 // fp32 angle would be off by ~1e-2 rad) and handed to the kernels as fp32
 // pairs: cs[b * stride + i] = (cos, sin).
+// theta^(-2i/r) for i < r/2, in double, computed once per (r, theta)
+inline const std::vector<double>& rope_inv_freq(int rotary_dim, double theta) {
+  static std::mutex mu;
+  static std::map<std::pair<int, double>, std::vector<double>> memo;
+  std::lock_guard<std::mutex> lock(mu);
+  std::vector<double>& f = memo[std::make_pair(rotary_dim, theta)];
+  if (f.empty())
+    for (int i = 0; i < rotary_dim / 2; ++i) f.push_back(pow(theta, -2.0 * i / (double)rotary_dim));
+  return f;  // entries of a std::map stay where they are
+}
+
 inline void fill_rope_table(float2* cs, int stride, int nb, const int32_t* positions, int rotary_dim,
                             double theta) {
+  const std::vector<double>& inv_freq = rope_inv_freq(rotary_dim, theta);
   for (int b = 0; b < nb; ++b)
     for (int i = 0; i < stride; ++i) {
       if (i < rotary_dim / 2) {
-        const double ang = (double)positions[b] * pow(theta, -2.0 * i / (double)rotary_dim);
+        const double ang = (double)positions[b] * inv_freq[i];
         cs[b * stride + i] = make_float2((float)cos(ang), (float)sin(ang));
       } else {
         cs[b * stride + i] = make_float2(1.f, 0.f);

@@ -37,11 +37,12 @@ enum GemvKind { kUp = 0, kHead = 1, kDown = 2 };
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
 // xs_b = m_b permuted for row_dot (no scaling); every thread issues kU float4
-// loads per sequence before it stores any.  m comes from another kernel:
-// loads bypass L1.
+// loads per sequence before it stores any (12 / NB: one round trip for a
+// 10240-float vector of one sequence).  m comes from another kernel: loads
+// bypass L1.
 template <int E, int NB>
 __device__ __forceinline__ void build_x_plain(const float* m, int n, int nb, float* xs, int xfloats, int t) {
-  constexpr int kU = 4;
+  constexpr int kU = 12 / NB;
   for (int base = t; 4 * base < n; base += kU * kThreads) {
     float4 v[NB][kU];
 #pragma unroll
