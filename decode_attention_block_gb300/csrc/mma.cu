@@ -30,18 +30,25 @@
 // result is as close to the fp32 GEMV's as rounding order allows, while the
 // HBM traffic is that of the bf16 weights alone.
 //
-// One kernel launch per projection and chunk of up to 128 sequences:
+// Two kernel launches per projection, for any batch (chunks of up to 128
+// sequences, one MMA's 256 hi/lo columns each, covered by one grid):
 //   k_prep_norm / k_prep_gate  build the activations' (hi, lo) rows and, for
 //                              qkv, each sequence's rope (cos, sin) table;
-//   k_proj_mma                 the GEMM.  Tiles of 128 weight rows are cut
-//                              along K into `splits` pieces (1..8) so that
-//                              the SMs stream weights.  The pieces of a tile
-//                              are added in split order: by the CTAs of a
-//                              thread-block cluster through DSMEM, each adding
-//                              and finishing a share of the sequences; or, for
+//   k_proj_mma                 the GEMM.  A CTA is (weight tile, chunk,
+//                              K-split); the chunks of a tile run side by side
+//                              so its rows come from L2 after the first.
+//                              Tiles of 128 weight rows are cut along K into
+//                              `splits` pieces (1..8) so that the SMs stream
+//                              weights.  The pieces of a tile are added in
+//                              split order: by the CTAs of a thread-block
+//                              cluster through DSMEM, each adding and
+//                              finishing a share of the sequences; or, for
 //                              small batches, through fp32 partials in the
 //                              workspace, the last CTA of the tile (an atomic
 //                              ticket) adding them and running the epilogue.
+//                              Long grids of unsplit tiles run two CTAs per
+//                              SM (up to two waves) or two weight tiles per
+//                              CTA (the head).
 //
 // Warp roles in k_proj_mma (192 threads): warp 0 issues the TMA loads (one
 // elected lane), warp 1 owns the tensor-memory columns and issues the MMAs
