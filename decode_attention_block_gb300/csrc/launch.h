@@ -53,7 +53,7 @@ cudaError_t launch_commit_rows(int cdtype, const void* ks, const void* vs, void*
 // The two projections for a batch on the tensor cores (mma.cu): same results
 // as launch_qkv_rope / launch_oproj, for bf16 weights.
 struct MmaWorkspace {
-  __nv_bfloat16* x;    // [2][bpad][max(hidden, q_dim)] activation rows (hi, lo)
+  __nv_bfloat16* x;    // [chunk][2][bpad][max(hidden, q_dim)] activation rows (hi, lo)
   float2* cs;          // [batch][head_dim / 2] rope (cos, sin)
   float* part;         // split-K partial results
   uint32_t* tickets;   // [kMmaMaxCtas] split-K tickets, zero between launches
@@ -77,7 +77,7 @@ cudaError_t launch_oproj_mma(const float* a, const float* g, const float* h, con
 //   mlp:  out[b] = h[b] + W_down (gelu(W_gate x_b) * (W_up x_b)), x_b = rms(h_b) * norm_w
 //   head: logits[b] = E rms(h_b) * norm_w
 // m ([batch][inter] fp32) holds the GELU products of the GEMV path; xd
-// ([2][bpad][inter] bf16) the (hi, lo) rows of the tensor-core path.
+// ([chunk][2][bpad][inter] bf16) the (hi, lo) rows of the tensor-core path.
 cudaError_t launch_mlp_gemv(int wdtype, const float* h, const void* norm_w, const void* gate_w,
                             const void* up_w, const void* down_w, float* m, float* out, uint32_t* err,
                             int hidden, int inter, int batch, float eps, cudaStream_t st);

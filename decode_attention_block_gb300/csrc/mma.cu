@@ -350,7 +350,7 @@ struct MmaParams {
   float* out;
   int hidden;  // output rows (hidden, or vocab for the head)
   // up epilogue
-  __nv_bfloat16* xd;  // [2][bpad][inter] (hi, lo) rows of the GELU product
+  __nv_bfloat16* xd;  // [chunk][2][bpad][inter] (hi, lo) rows of the GELU product (this chunk's in the kernel)
   int inter;
   // split-K and errors
   float* part;
