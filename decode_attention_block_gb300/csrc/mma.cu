@@ -979,11 +979,28 @@ Plan plan_with(int tiles, int kblocks, int bpad, int s) {
   return P;
 }
 
-// Split K so that the tiles cover the SMs once (a launch of several chunks:
-// the nearest multiple, e.g. 80 (tile, chunk) pairs on 152 SMs -> 2).
+// Split K so that the tiles cover the SMs once.  A launch of several chunks
+// (compute-bound: hundreds of (tile, chunk) pairs) takes the split with the
+// fewest K-blocks per SM over its waves, waves * ceil(kblocks / s), e.g. 80
+// pairs of 64 K-blocks on 152 SMs: s = 3 (2 waves of 22) rather than 1 (64)
+// or 2 (2 waves of 32).
 int default_splits(int tiles, int kblocks, bool chunked) {
   const int sms = device_sm_count();
-  int s = chunked ? (sms + tiles / 2) / tiles : sms / tiles;
+  if (chunked) {
+    int best = 1;
+    int64_t best_cost = INT64_MAX;
+    for (int s = 1; s <= kMaxSplits && s <= kblocks; ++s) {
+      if (s > 1 && s * tiles > kMmaMaxCtas) break;  // split partials and tickets are per CTA
+      const int64_t waves = (int64_t)(tiles * s + sms - 1) / sms;
+      const int64_t cost = waves * ((kblocks + s - 1) / s);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = s;
+      }
+    }
+    return best;
+  }
+  int s = sms / tiles;
   if (s > kMaxSplits) s = kMaxSplits;
   if (s > kblocks) s = kblocks;
   if (s * tiles > kMmaMaxCtas) s = kMmaMaxCtas / tiles;
