@@ -205,8 +205,10 @@ int spark_attn_decode_stack(const spark_geom* g, const float* h, int32_t n_layer
  * AUTO picks what spark_attn_decode runs: for batch <= 4, or fp32 weights,
  * the GEMV kernels, which read each weight once for up to 4 sequences; for
  * larger batches with bf16 weights, a GEMM on the tensor cores (tcgen05,
- * tensor-memory accumulator) that reads each weight once for up to 128
- * sequences, its fp32 activations carried as two bf16 halves (x = hi + lo).
+ * tensor-memory accumulator) that reads each weight from HBM once for the
+ * whole batch (one launch; chunks of 128 sequences after the first find the
+ * weight rows in L2), its fp32 activations carried as two bf16 halves
+ * (x = hi + lo).
  * GEMV and MMA force one; MMA needs bf16 weights, hidden % 64 == 0 and, for
  * q_k_v_proj, a rotary dim <= 128 or == head_dim (else UNSUPPORTED). */
 #define SPARK_PATH_AUTO 0
