@@ -286,3 +286,22 @@ def test_head_arguments_are_validated(B):
     assert _head(B, batch=8, path=B.SPARK_PATH_MMA, dtype=B.SPARK_F32) == -5
     assert _head(B, ws_bytes=64) == -4
     assert _head(B, ws=0) == -4
+
+
+def test_descriptors_cache_their_c_struct_until_a_field_changes(B, monkeypatch):
+    # the struct is built (and its tensors checked) once; reassigning a field
+    # drops it, so the next call builds it again from the new tensors
+    built = []
+
+    def fake_build(self):
+        built.append(self)
+        return object()
+
+    monkeypatch.setattr(B.LayerWeights, "_build_c", fake_build)
+    w = B.LayerWeights(None, None, None, None)
+    first = w.to_c()
+    assert w.to_c() is first and len(built) == 1
+    w.o_w = None                      # a field reassigned: the cache is dropped
+    second = w.to_c()
+    assert second is not first and len(built) == 2
+    assert w.to_c() is second
