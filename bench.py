@@ -6,14 +6,21 @@ attention, gate + o_proj + residual, per layer, through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Prints one JSON line.  ``value`` is decode tokens/s of the whole job (steps/s
-times the batch, summed over ranks) with every input resident in HBM; the
-weights and caches of several copies of the workload are rotated so the bytes
-a step reads are never in L2 from the step before.  ``e2e`` is the same metric
-through the public call with the step's input ``h`` copied from pinned host
-memory and the output read back every step.  ``roofline`` is for the kernel
-with the largest share of the step.  ``cpu_baseline`` (and ``--impl
+Prints one JSON line.  The default workload is the 64-sequence ragged batch
+(contexts uniform in [512, 32768], one full and one sliding layer), the
+largest that fits one GPU.  ``value`` is decode tokens/s of the whole job
+(steps/s times the batch, summed over ranks) with every input resident in HBM;
+the weights and caches of several copies of the workload are rotated so the
+bytes a step reads are never in L2 from the step before (one copy when a step
+alone reads more than four times the L2).  ``e2e`` is the same metric through
+the public call with the step's input ``h`` copied from pinned host memory and
+the output read back every step.  ``roofline`` is for the kernel with the
+largest share of the step.  ``targets`` times, in the same process, the
+8-sequence 131072-context workload: its full layer's attention kernel and its
+whole step against the HBM roofline.  ``cpu_baseline`` (and ``--impl
 reference``) time the float64 CPU oracle on a bounded sample of the workload.
+Without WORLD_SIZE in the environment, ``--gpus N`` (N > 1) starts N ranks
+itself, one per GPU, each an independent replica.
 """
 
 from __future__ import annotations
@@ -36,7 +43,12 @@ if ROOT not in sys.path:
 
 from decode_attention_block_gb300 import build_lib, synth  # noqa: E402
 
-DEFAULT_WORKLOAD = "full+sliding_bf16_b1_pos700"
+DEFAULT_WORKLOAD = "full+sliding_bf16_b64_ctx512-32768"
+# the long-context workload the HBM targets are stated on, timed beside the
+# default one: its full layer's attention kernel and its whole step
+TARGET_WORKLOAD = "full+sliding_bf16_b8_ctx131072"
+TARGET_ATTENTION_FRAC = 0.70
+TARGET_STEP_FRAC = 0.60
 METRIC = "decode attn-block steps/s & tokens/s; achieved HBM GB/s vs ~8 TB/s peak"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -72,6 +84,29 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as s_:
+        s_.bind(("127.0.0.1", 0))
+        return s_.getsockname()[1]
+
+
+def spawn_ranks(n: int, argv: list, script: str = None) -> int:
+    """Start n ranks of `script` (this file by default) with `argv`, one
+    process per GPU, rank r on device r, rendezvous on 127.0.0.1; rank 0's
+    output passes through, the others' stdout is dropped.  Returns the first
+    non-zero exit status, else 0."""
+    port = free_port()
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, script or os.path.abspath(__file__)] + list(argv),
+                                      env=env, stdout=None if r == 0 else subprocess.DEVNULL))
+    rcs = [p_.wait() for p_ in procs]
+    return next((rc for rc in rcs if rc != 0), 0)
+
+
 def job_tokens_per_s(batch: int, world: int, steps: int, ms_max: float) -> float:
     """Whole-job throughput: every rank decodes `steps` steps of its own
     `batch` sequences (weak scaling), timed by the slowest rank."""
@@ -87,11 +122,13 @@ def step_bytes(wl: synth.Workload) -> dict:
     a token attends to once (K and V).  h and out are not counted."""
     w = wl.weight_bytes_per_layer()
     q_dim, kv_dim, H, es = wl.n_q * wl.head_dim, wl.n_kv * wl.head_dim, wl.hidden, wl.elem_bytes
-    per = {"qkv_gate": 0, "split_rope": 0, "attention": 0, "gate_oproj": 0}
-    for li in range(len(wl.layers)):
+    per = {"qkv_gate": 0, "attention": 0, "gate_oproj": 0, "attention_full": 0, "attention_sliding": 0}
+    for li, spec in enumerate(wl.layers):
         per["qkv_gate"] += ((q_dim + 2 * kv_dim + wl.n_q) * H + H) * es
         per["gate_oproj"] += H * q_dim * es
-        per["attention"] += sum(wl.rows_read(li, b) for b in range(wl.batch)) * wl.kv_row_bytes()
+        kv = sum(wl.rows_read(li, b) for b in range(wl.batch)) * wl.kv_row_bytes()
+        per["attention"] += kv
+        per["attention_full" if spec.is_full else "attention_sliding"] += kv
     total = len(wl.layers) * w + per["attention"]
     assert total == per["qkv_gate"] + per["gate_oproj"] + per["attention"]
     return {"total": total, "per_kernel": per}
@@ -105,7 +142,7 @@ TRAFFIC = {
     ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_580_672,
     ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_021_696,
     ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_403_904,
-    ("full_bf16_b1_ctx131072", "attention"): 541_357_056,
+    ("full_bf16_b1_ctx131072", "attention_full"): 541_357_056,
 }
 ATTN_TRAFFIC_RATIO = 541_357_056 / 536_875_008
 
@@ -114,7 +151,7 @@ def measured_traffic(workload: str, kernel: str, bytes_per_launch: float):
     """(traffic per launch, how it was obtained) or (None, reason)."""
     if (workload, kernel) in TRAFFIC:
         return TRAFFIC[(workload, kernel)], "ncu capture of this workload"
-    if kernel == "attention":
+    if kernel.startswith("attention"):
         return int(bytes_per_launch * ATTN_TRAFFIC_RATIO), "ncu capture at 131072 rows, scaled by rows read"
     return None, "no capture of this kernel on this workload"
 
@@ -238,24 +275,35 @@ def stack_is_fused(wl) -> bool:
     return wl.dtype == "bf16" and wl.batch <= 4
 
 
-STAGES = ("qkv_rope", "attention", "gate_oproj")
+STAGES = ("qkv_rope", "attention_full", "attention_sliding", "gate_oproj")
+
+
+def stage_layers(wl, stage) -> list:
+    """Indices of the layers a stage's timing launches: every layer for the
+    projections, the layers of one class for attention."""
+    if stage == "attention_full":
+        return [i for i, s_ in enumerate(wl.layers) if s_.is_full]
+    if stage == "attention_sliding":
+        return [i for i, s_ in enumerate(wl.layers) if not s_.is_full]
+    return list(range(len(wl.layers)))
 
 
 def stage_launcher(B, geom, wl, cp, ws, bufs, stage):
-    """Launch one stage kernel for every layer of a copy (the same work that
-    stage does inside run_step)."""
+    """Launch one stage kernel for the stage's layers of a copy (the same work
+    that stage does inside run_step)."""
+    layers = stage_layers(wl, stage)
+
     def go():
-        cur = cp.h
-        for i, (spec, w, kv) in enumerate(cp.layers):
-            out = cp.buf[i % 2]
+        for i in layers:
+            spec, w, kv = cp.layers[i]
+            cur, out = (cp.h if i == 0 else cp.buf[(i - 1) % 2]), cp.buf[i % 2]
             cls = B.SPARK_FULL if spec.is_full else B.SPARK_SLIDING
             if stage == "qkv_rope":
                 B.spark_dbg_qkv_rope(geom, cur, w, kv, cls, wl.positions, bufs["q_rot"], bufs["g"], ws)
-            elif stage == "attention":
+            elif stage.startswith("attention"):
                 B.spark_dbg_attention(geom, bufs["q_rot"], kv, cls, wl.positions, bufs["a"], ws, 0)
             else:
                 B.spark_dbg_gate_oproj(geom, bufs["a"], bufs["g"], cur, w, out, ws)
-            cur = out
     return go
 
 
@@ -274,14 +322,10 @@ def capture(fn):
     return g
 
 
-def bench_ours(args, wl, rank, local, world):
-    from decode_attention_block_gb300 import binding as B
-
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    build_lib.build()
-    B.load()
-    geom = B.spark_geom_default()
+def measure_decode(args, wl, B, geom, device, world, steps, with_e2e=True):
+    """Time `steps` decode steps of a workload (graph replay, inputs resident,
+    rotating copies against L2), each stage's launches on their own, and,
+    with `with_e2e`, the public call end to end from pinned host memory."""
     stream = torch.cuda.current_stream(device)
     sb = step_bytes(wl)
     L = len(wl.layers)
@@ -290,9 +334,9 @@ def bench_ours(args, wl, rank, local, world):
     cps = [Copy(wl, B, device) for _ in range(copies)]
     ws = B.make_workspace(geom, wl.batch, device)
     H, q_dim = wl.hidden, wl.n_q * wl.head_dim
-    bufs = {"q_rot": torch.empty((wl.batch, q_dim), device=device),
-            "g": torch.empty((wl.batch, wl.n_q), device=device),
-            "a": torch.empty((wl.batch, q_dim), device=device)}
+    bufs = {"q_rot": torch.zeros((wl.batch, q_dim), device=device),
+            "g": torch.zeros((wl.batch, wl.n_q), device=device),
+            "a": torch.zeros((wl.batch, q_dim), device=device)}
     torch.cuda.synchronize()
 
     # one CUDA graph per copy: a step's launches replayed without host overhead
@@ -309,7 +353,6 @@ def bench_ours(args, wl, rank, local, world):
         step(i)
     torch.cuda.synchronize()
 
-    steps = args.steps
     if steps <= 0:   # auto: about two seconds of timed work
         t0 = time.perf_counter()
         for i in range(20):
@@ -319,7 +362,7 @@ def bench_ours(args, wl, rank, local, world):
         steps = int(min(50000, max(50, 2.0 / max(per, 1e-6))))
 
     # timed region: exactly `steps` steps
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(device.index or 0)
     with sampler:
         time.sleep(0.3)
         barrier(world)
@@ -337,13 +380,17 @@ def bench_ours(args, wl, rank, local, world):
     ms_per_step = ms_total / steps
     kernels_per_step = -(-L // 40) if fused else L * (2 * projection_launches(wl) + 1)
 
-    # per-kernel durations: each stage's launches (all layers, all copies)
+    # per-stage durations: each stage's launches (its layers, all copies)
     # replayed back to back in a graph between two events on this stream
-    kavg = {}
+    kavg, per_launch, launches = {}, {}, {}
+    bytes_key = {"qkv_rope": "qkv_gate", "gate_oproj": "gate_oproj"}
     for stage in STAGES:
+        n = len(stage_layers(wl, stage))
+        if n == 0:
+            continue
         fns = [stage_launcher(B, geom, wl, cp, ws, bufs, stage) for cp in cps]
         g = capture(lambda: [f() for f in fns])
-        reps = max(3, min(200, int(2000 / (L * copies))))
+        reps = max(3, min(200, int(2000 / (n * copies))))
         g.replay()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -353,44 +400,97 @@ def bench_ours(args, wl, rank, local, world):
             g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        kavg[stage] = e0.elapsed_time(e1) / (reps * L * copies)   # ms per launch
-    bytes_key = {"qkv_rope": "qkv_gate", "attention": "attention", "gate_oproj": "gate_oproj"}
-    per_launch = {k: sb["per_kernel"][bytes_key[k]] / L for k in STAGES}
-    launches = {k: L for k in STAGES}
+        kavg[stage] = e0.elapsed_time(e1) / (reps * n * copies)   # ms per launch
+        per_launch[stage] = sb["per_kernel"][bytes_key.get(stage, stage)] / n
+        launches[stage] = n
     if fused:
         # one persistent kernel per step (per 40 layers): its duration is the step
         kavg = {"decode_stack": ms_per_step / kernels_per_step, **{"layer_" + k: v for k, v in kavg.items()}}
         per_launch = {"decode_stack": sb["total"] / kernels_per_step,
                       **{"layer_" + k: v for k, v in per_launch.items()}}
-        launches = {"decode_stack": kernels_per_step, **{"layer_" + k: 0 for k in STAGES}}
+        launches = {"decode_stack": kernels_per_step, **{"layer_" + k: 0 for k in launches}}
     share = {k: kavg[k] * launches[k] for k in kavg}
     tot = sum(share.values())
     top = max(share, key=share.get)
-    peaks = measured_peaks()
-    achieved = per_launch[top] / (kavg[top] * 1e-3) / 1e9
-    traffic, traffic_src = measured_traffic(wl.name, top, per_launch[top])
+    kernels = {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": launches[k],
+                   "share": round(share[k] / tot, 4) if tot else None,
+                   "bytes_per_launch": int(per_launch[k]),
+                   "gbs": round(per_launch[k] / (kavg[k] * 1e-3) / 1e9, 1)} for k in kavg}
 
-    # end to end through the public call: h from pinned host, out read back
-    h_host = [synth.make_h(wl, "cpu").pin_memory() for _ in range(2)]
-    out_host = torch.empty((wl.batch, H), dtype=torch.float32).pin_memory()
-    e2e_steps = max(10, min(steps, 2000))
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        cp = cps[i % copies]
-        cp.h.copy_(h_host[i % 2], non_blocking=True)
-        res = run_step(B, geom, wl, cp, ws, stream, path)
-        out_host.copy_(res, non_blocking=True)
-        stream.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
+    e2e = None
+    if with_e2e:
+        # end to end through the public call: h from pinned host, out read back
+        h_host = [synth.make_h(wl, "cpu").pin_memory() for _ in range(2)]
+        out_host = torch.empty((wl.batch, H), dtype=torch.float32).pin_memory()
+        e2e_steps = max(10, min(steps, 2000))
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            cp = cps[i % copies]
+            cp.h.copy_(h_host[i % 2], non_blocking=True)
+            res = run_step(B, geom, wl, cp, ws, stream, path)
+            out_host.copy_(res, non_blocking=True)
+            stream.synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
+        e2e = {"value": round(wl.batch * world * e2e_steps / e2e_s, 3), "unit": "tokens/s",
+               "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * H * 4,
+               "launch": "direct calls, synchronised every step"}
     err = B.spark_attn_error_word(ws)
     if err != 0:
         raise RuntimeError(f"device error word {err:#x}")
+    return {"steps": steps, "ms_per_step": ms_per_step, "ms_total": ms_total, "clocks": clocks,
+            "kavg": kavg, "per_launch": per_launch, "kernels": kernels, "top": top, "copies": copies,
+            "l2": l2, "fused": fused, "kernels_per_step": kernels_per_step, "use_graph": use_graph,
+            "bytes": sb["total"], "e2e": e2e}
 
-    tokens = wl.batch * world
-    value = job_tokens_per_s(wl.batch, world, steps, ms_total)
-    gbs = sb["total"] / (ms_per_step * 1e-3) / 1e9
+
+def roofline_of(wl_name: str, m: dict, peaks: dict, kernel: str = None) -> dict:
+    """The roofline object of one kernel of a measurement: algorithmic bytes
+    per launch over its average launch time, against the measured copy
+    bandwidth, with the DRAM traffic of a capture where one exists."""
+    k = kernel or m["top"]
+    achieved = m["per_launch"][k] / (m["kavg"][k] * 1e-3) / 1e9
+    traffic, traffic_src = measured_traffic(wl_name, k, m["per_launch"][k])
+    return {"kernel": k, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "peak_source": peaks["source"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic, "traffic_source": traffic_src, "bytes_per_launch": int(m["per_launch"][k]),
+            "avg_launch_us": round(m["kavg"][k] * 1e3, 3)}
+
+
+def measure_targets(args, B, geom, device, world, peaks) -> dict:
+    """The long-context workload's full-layer attention kernel and whole step
+    against the HBM roofline, timed in this process."""
+    wl = synth.workloads()[TARGET_WORKLOAD]
+    m = measure_decode(args, wl, B, geom, device, world, max(args.steps, 20) if args.steps > 0 else 0,
+                       with_e2e=False)
+    att = roofline_of(wl.name, m, peaks, "attention_full")
+    gbs = m["bytes"] / (m["ms_per_step"] * 1e-3) / 1e9
+    step_frac = gbs / peaks["hbm_gbs"]
+    return {"workload": wl.name, "description": wl.description, "steps": m["steps"],
+            "full_layer_attention": {**att, "target_frac": TARGET_ATTENTION_FRAC,
+                                     "met": att["frac"] >= TARGET_ATTENTION_FRAC},
+            "whole_step": {"ms_per_step": round(m["ms_per_step"], 6), "hbm_bytes_per_step": m["bytes"],
+                           "hbm_gbs": round(gbs, 1), "frac": round(step_frac, 4),
+                           "target_frac": TARGET_STEP_FRAC, "met": step_frac >= TARGET_STEP_FRAC,
+                           "tokens_per_s": round(wl.batch * 1e3 / m["ms_per_step"], 3)},
+            "kernels": m["kernels"], "clocks": m["clocks"]}
+
+
+def bench_ours(args, wl, rank, local, world):
+    from decode_attention_block_gb300 import binding as B
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    build_lib.build()
+    B.load()
+    geom = B.spark_geom_default()
+    L = len(wl.layers)
+    peaks = measured_peaks()
+    m = measure_decode(args, wl, B, geom, device, world, args.steps)
+    steps, ms_per_step, copies = m["steps"], m["ms_per_step"], m["copies"]
+    value = job_tokens_per_s(wl.batch, world, steps, m["ms_total"])
+    gbs = m["bytes"] / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -411,31 +511,31 @@ def bench_ours(args, wl, rank, local, world):
                    "layers": ["full" if s.is_full else "sliding" for s in wl.layers][:8]
                    + (["..."] if L > 8 else []),
                    "parallelism": f"replicas x{world} (independent sequences, no collective)",
-                   "launch": "CUDA graph per step" if use_graph else "direct calls",
-                   "path": ("one persistent kernel per step (spark_attn_decode_stack)" if fused
-                            else "three kernels per layer"),
-                   "l2": f"{copies} rotating copies of weights+caches ({copies * sb['total'] / 1e6:.0f} MB) "
-                         f"vs {l2 / 1e6:.0f} MB L2"},
+                   "launch": "CUDA graph per step" if m["use_graph"] else "direct calls",
+                   "path": ("one persistent kernel per step (spark_attn_decode_stack)" if m["fused"]
+                            else "three kernels per layer" if projection_launches(wl) == 1 else
+                            "five kernels per layer (tensor-core projections)"),
+                   "l2": f"{copies} rotating copies of weights+caches ({copies * m['bytes'] / 1e6:.0f} MB) "
+                         f"vs {m['l2'] / 1e6:.0f} MB L2"},
         "steps_per_s": round(1e3 / ms_per_step * world, 3),
-        "hbm_bytes_per_step": sb["total"],
+        "hbm_bytes_per_step": m["bytes"],
         "hbm_gbs": round(gbs, 1),
         "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
-        "roofline": {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "traffic_source": traffic_src,
-                     "bytes_per_launch": int(per_launch[top]),
-                     "avg_launch_us": round(kavg[top] * 1e3, 3)},
-        "kernels": {k: {"avg_us": round(kavg[k] * 1e3, 3), "launches_per_step": launches[k],
-                        "share": round(share[k] / tot, 4) if tot else None,
-                        "bytes_per_launch": int(per_launch[k]),
-                        "gbs": round(per_launch[k] / (kavg[k] * 1e-3) / 1e9, 1)} for k in kavg},
-        "e2e": {"value": round(tokens * e2e_steps / e2e_s, 3), "unit": "tokens/s",
-                "h2d_bytes_per_step": wl.batch * H * 4, "d2h_bytes_per_step": wl.batch * H * 4,
-                "launch": "direct calls, synchronised every step"},
-        "gpu_launches": kernels_per_step * steps,
-        "clocks": clocks,
+        "roofline": roofline_of(wl.name, m, peaks),
+        "kernels": m["kernels"],
+        "e2e": m["e2e"],
+        "gpu_launches": m["kernels_per_step"] * steps,
+        "clocks": m["clocks"],
     }
+    if not args.no_targets and wl.name != TARGET_WORKLOAD:
+        torch.cuda.empty_cache()
+        line["targets"] = measure_targets(args, B, geom, device, world, peaks)
+    elif wl.name == TARGET_WORKLOAD:
+        att = roofline_of(wl.name, m, peaks, "attention_full")
+        line["targets"] = {"workload": wl.name, "full_layer_attention": {
+            **att, "target_frac": TARGET_ATTENTION_FRAC, "met": att["frac"] >= TARGET_ATTENTION_FRAC},
+            "whole_step": {"frac": line["hbm_frac"], "target_frac": TARGET_STEP_FRAC,
+                           "met": line["hbm_frac"] >= TARGET_STEP_FRAC}}
     return line
 
 
@@ -443,9 +543,37 @@ def bench_ours(args, wl, rank, local, world):
 # the oracle (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
+_ORACLE_LAYERS = {}
+
+
+def oracle_layer_sample(wl: synth.Workload, li: int, seqs: list):
+    """One layer's inputs for the oracle's timed sample, drawn once per
+    process: the weights and the caches of the sampled sequences only (each
+    [1, capacity, n_kv, d], the rows the device copy holds)."""
+    key = (wl.name, li, tuple(seqs))
+    if key not in _ORACLE_LAYERS:
+        w = {k: synth.to_numpy(v) for k, v in synth.make_weights(wl, li, "cpu").items()}
+        caches = {}
+        for b in seqs:
+            k, v = synth.make_sequence_cache(wl, li, b, "cpu")
+            caches[b] = (synth.to_numpy(k), synth.to_numpy(v))
+        _ORACLE_LAYERS[key] = (w, caches)
+    return _ORACLE_LAYERS[key]
+
+
+def oracle_sequences(wl: synth.Workload, n: int = 4) -> list:
+    """The sequences the oracle's sample takes: up to n, evenly spread over the
+    batch (a ragged batch's short and long histories alike)."""
+    k = max(1, min(wl.batch, n))
+    return sorted({(i * wl.batch) // k for i in range(k)})
+
+
 def time_oracle(wl: synth.Workload, budget_s: float) -> dict:
-    """Time the float64 CPU oracle on (layer, sequence) units of one step, in
-    order, until `budget_s` is spent; report the rate scaled to a whole step."""
+    """Time the float64 CPU oracle on (layer, sequence) units of one step
+    until `budget_s` is spent (passes over the sampled units, layer by layer;
+    at least one unit), and report the rate scaled to a whole step: units
+    timed / units of a step / seconds.  The sampled inputs (up to 4 sequences
+    per layer) are drawn once and reused by later calls."""
     import oracle
 
     geom = oracle.OracleGeometry(hidden=wl.hidden, n_q=wl.n_q, n_kv=wl.n_kv, head_dim=wl.head_dim,
@@ -454,26 +582,30 @@ def time_oracle(wl: synth.Workload, budget_s: float) -> dict:
     units_total = len(wl.layers) * wl.batch
     units = 0
     elapsed = 0.0
-    max_seqs = max(1, min(wl.batch, 2))
-    for li, spec in enumerate(wl.layers):
-        w = {k: synth.to_numpy(v) for k, v in synth.make_weights(wl, li, "cpu").items()}
-        seqs = list(range(max_seqs))
-        k, v = synth.make_cache(wl, li, "cpu", sequences=seqs)
-        kn, vn = synth.to_numpy(k), synth.to_numpy(v)
-        for b in seqs:
-            t0 = time.perf_counter()
-            oracle.decode_step(geom, h, w, kn, vn, spec.is_full, wl.positions, spec.ring_capacity, sequences=[b])
-            elapsed += time.perf_counter() - t0
-            units += 1
-            if elapsed >= budget_s:
+    seqs = oracle_sequences(wl)
+    done = False
+    passes = 0
+    while not done:
+        for li, spec in enumerate(wl.layers):
+            w, caches = oracle_layer_sample(wl, li, seqs)
+            for b in seqs:
+                kn, vn = caches[b]
+                t0 = time.perf_counter()
+                oracle.decode_step(geom, h[b:b + 1], w, kn, vn, spec.is_full, [wl.positions[b]],
+                                   spec.ring_capacity)
+                elapsed += time.perf_counter() - t0
+                units += 1
+                if elapsed >= budget_s:
+                    done = True
+                    break
+            if done:
                 break
-        if elapsed >= budget_s:
-            break
+        passes += 1
     steps_per_s = (units / units_total) / elapsed
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(steps_per_s * wl.batch, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{units} of {units_total} (layer, sequence) decode units of one step "
-                      f"({elapsed:.1f} s, numpy float64, BLAS threads up to {cores} cores)"}
+            "sample": f"{units} (layer, sequence) decode units of the {units_total} of one step, over "
+                      f"sequences {seqs} ({elapsed:.1f} s, numpy float64, BLAS threads up to {cores} cores)"}
 
 
 def time_oracle_prefill(wl: synth.Workload, m: int, budget_s: float) -> dict:
@@ -524,11 +656,11 @@ def time_oracle_decoder(wl: synth.Workload, inter: int, vocab: int) -> dict:
     n_l = min(len(wl.layers), 4)
     for li, spec in enumerate(wl.layers[:n_l]):
         w = {k: synth.to_numpy(v) for k, v in synth.make_weights(wl, li, "cpu").items()}
-        k, v = synth.make_cache(wl, li, "cpu", sequences=[0])
+        k, v = synth.make_sequence_cache(wl, li, 0, "cpu")
         mw = {k_: synth.to_numpy(v_) for k_, v_ in
               synth.make_mlp_weights(wl.seed * 100 + li, wl.hidden, inter, dt, "cpu").items()}
         t0 = time.perf_counter()
-        r = oracle.decode_step(geom, h, w, synth.to_numpy(k)[:1], synth.to_numpy(v)[:1], spec.is_full, pos,
+        r = oracle.decode_step(geom, h, w, synth.to_numpy(k), synth.to_numpy(v), spec.is_full, pos,
                                spec.ring_capacity)
         h = oracle.mlp_block(geom, r["out"], mw)["out"]
         elapsed += time.perf_counter() - t0
@@ -816,9 +948,16 @@ def main():
                     help="time whole decoder steps: attention block + MLP per layer, then the head")
     ap.add_argument("--prefill", type=int, default=0,
                     help="time chunks of this many consecutive tokens (spark_attn_prefill) instead of decode")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the long-context workload's attention and step fractions")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU, each an independent replica of the workload
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
     rank, local, world = dist_env()
+    if args.gpus > 1 and world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE is {world}")
     wl = synth.workloads()[args.workload]
 
     if args.impl == "reference":

@@ -110,6 +110,7 @@ _SIGNATURES = {
     "spark_dbg_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, ctypes.POINTER(SparkKvLayer),
                                                    ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                                    _P, _P]),
+    "spark_dbg_attention_noalloc_error_word": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _P]),
     "spark_dbg_gate_oproj": (ctypes.c_int, [ctypes.POINTER(SparkGeom), _P, _P, _P,
                                             ctypes.POINTER(SparkLayerWeights), ctypes.c_int32, _P,
                                             ctypes.c_int32, _P, ctypes.c_size_t, _P]),
@@ -371,6 +372,15 @@ def spark_dbg_attention_noalloc(geom: SparkGeom, q_rot: torch.Tensor, kv: KvLaye
                                               ctypes.byref(kc), int(layer_class), pos, len(positions),
                                               _dev_ptr(a, "a", torch.float32), _stream(stream)),
            "spark_dbg_attention_noalloc")
+
+
+def spark_dbg_attention_noalloc_error_word(stream=None) -> int:
+    """Read and clear the error word of the no-workspace attention's fixed
+    array on the current device (synchronises the stream)."""
+    word = ctypes.c_uint32(0)
+    _check(load().spark_dbg_attention_noalloc_error_word(ctypes.byref(word), _stream(stream)),
+           "spark_dbg_attention_noalloc_error_word")
+    return int(word.value)
 
 
 def spark_dbg_gate_oproj(geom: SparkGeom, a: torch.Tensor, g_logits: torch.Tensor, h: torch.Tensor,

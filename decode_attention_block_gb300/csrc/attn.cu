@@ -386,7 +386,7 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
                      const int32_t* positions, int batch, float* a, float* part,
                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                     size_t l2_pf_bytes, const ChunkSrc& chunk, cudaStream_t st) {
+                     size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st) {
   using S = Smem<CT, NS, NC>;
   AttnArgs<MAXB> args;
   args.prefix[0] = 0;
@@ -404,7 +404,7 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
   if (cl > kMaxCluster) cl = kMaxCluster;
   if (n_ctas > 0 || cl < 2 || max_rows > kClusterMaxRows ||
-      (int64_t)groups * cl > device_sm_count())
+      (int64_t)groups * cl > device_sm_count() || (int64_t)groups * cl > max_ctas)
     cl = 0;
   int G = cl > 0 ? groups * cl : n_ctas;
   if (cl == 0 && G <= 0) {
@@ -414,6 +414,7 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   }
   if (G < 1) G = 1;
   if (G > kMaxAttnCtas) G = kMaxAttnCtas;
+  if (G > max_ctas) G = max_ctas;
 
   // a chunk's tokens share one sequence's cache; decode rows are per sequence
   const int64_t cache_rows = chunk.p0 >= 0 ? capacity : (int64_t)batch * capacity;
@@ -455,16 +456,16 @@ cudaError_t launch_ns(const float* q_rot, const void* kc, const void* vc, int n_
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                      size_t l2_pf_bytes, const ChunkSrc& chunk, cudaStream_t st) {
+                      size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st) {
   if (batch <= 8)
     return launch_t<CT, NS, NC, MINB, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                               positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
+                               positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
   if (batch <= 64)
     return launch_t<CT, NS, NC, MINB, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
+                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
   return launch_t<CT, NS, NC, MINB, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
                                            window, scale, positions, batch, a, part, counters, err,
-                                           n_ctas, l2_pf, l2_pf_bytes, chunk, st);
+                                           n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
 }
 
 template <typename CT>
@@ -472,16 +473,16 @@ cudaError_t launch_ct(const float* q_rot, const void* kc, const void* vc, int n_
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                      size_t l2_pf_bytes, const ChunkSrc& chunk, cudaStream_t st) {
+                      size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st) {
   int64_t rows = 0;
   for (int b = 0; b < batch; ++b) rows += window_of(positions[b], full, window, ring_capacity).rows;
   if ((int64_t)n_kv * rows >= kDeepRows)
     return launch_ns<CT, CacheT<CT>::kDeep, kConsumers, CacheT<CT>::kDeepBlocks>(
         q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale, positions, batch, a, part,
-        counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
+        counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
   return launch_ns<CT, CacheT<CT>::kShallow, kConsumers, 1>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
                                        scale, positions, batch, a, part, counters, err, n_ctas,
-                                       l2_pf, l2_pf_bytes, chunk, st);
+                                       l2_pf, l2_pf_bytes, chunk, max_ctas, st);
 }
 
 }  // namespace
@@ -491,12 +492,13 @@ cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, con
                              int window, float scale, const int32_t* positions, int batch,
                              float* a, float* part, uint32_t* counters, uint32_t* err,
                              int n_ctas, const void* l2_pf, size_t l2_pf_bytes, cudaStream_t st,
-                             const ChunkSrc& chunk) {
+                             const ChunkSrc& chunk, int max_ctas) {
   if (cdtype == SPARK_BF16)
     return launch_ct<__nv_bfloat16>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
-                                    scale, positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
+                                    scale, positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk,
+                                    max_ctas, st);
   return launch_ct<float>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                          positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, st);
+                          positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
 }
 
 namespace {

@@ -29,13 +29,15 @@ struct ChunkSrc {
 
 // Split-K GQA decode attention with the log-sum-exp merge.  With a chunk,
 // `positions` are the tokens' positions, the cache is one sequence's, and
-// rows at positions >= chunk.p0 come from the staged rows.
+// rows at positions >= chunk.p0 come from the staged rows.  The grid never
+// exceeds max_ctas CTAs (`part` holds max_ctas + batch * n_kv partials).
 cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, const void* vc,
                              int n_kv, int64_t capacity, int ring_capacity, bool full,
                              int window, float scale, const int32_t* positions, int batch,
                              float* a, float* part, uint32_t* counters, uint32_t* err,
                              int n_ctas, const void* l2_prefetch, size_t l2_prefetch_bytes,
-                             cudaStream_t st, const ChunkSrc& chunk = ChunkSrc());
+                             cudaStream_t st, const ChunkSrc& chunk = ChunkSrc(),
+                             int max_ctas = kMaxAttnCtas);
 
 // The same attention for a chunk, grouped by query (attn_chunk.cu): one CTA
 // per (group of consecutive tokens, KV head) reads the union of the tokens'

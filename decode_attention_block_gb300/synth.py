@@ -124,6 +124,11 @@ def workloads() -> dict:
                  "bf16: the batched projections with caches small enough to profile",
                  "bf16", _ragged_positions(1006, 64, 512, 1023),
                  [LayerSpec(True, 0), LayerSpec(False, RING)], seed=1006),
+        Workload("full_bf16_b16_ctx512-32768",
+                 "the full layer of the first 16 sequences of the 64-sequence ragged batch "
+                 "(contexts in [512, 32768], the same rows): its attention at a size a profiler "
+                 "can capture",
+                 "bf16", _ragged_positions(1003, 64, 512, 32768)[:16], [LayerSpec(True, 0)], seed=1003),
         Workload("full_bf16_b1_ctx131072",
                  "one full layer (rotary 64 @ 5e6), bf16, one sequence at context 131072 "
                  "(a single long-context attention)",
@@ -168,11 +173,19 @@ def make_weights(wl: Workload, li: int, device="cpu", gen_device=None) -> dict:
     return {k: v.to(device) for k, v in out.items()}
 
 
+def _draw_sequence_rows(wl: Workload, li: int, b: int, k_out, v_out, gd) -> None:
+    """Sequence b's K and V rows of layer li into k_out, v_out [capacity, n_kv, d]:
+    the generator is seeded per (layer, sequence), so a sequence's rows do not
+    depend on which other sequences are drawn."""
+    g = _gen(wl.seed * 1000003 + 17 * li + 7 + 104729 * (b + 1), gd)
+    k_out.copy_(_randn(tuple(k_out.shape), g, gd, dtype=wl.torch_dtype))
+    v_out.copy_(_randn(tuple(v_out.shape), g, gd, dtype=wl.torch_dtype))
+
+
 def make_cache(wl: Workload, li: int, device="cpu", gen_device=None, sequences=None):
     """One layer's K and V caches [batch, capacity, n_kv, d], every row ~ N(0, 1).
     With ``sequences``, only those batch entries are drawn (the others are
-    zero): the generator is seeded per (layer, sequence), so a sequence's rows
-    do not depend on which others are drawn."""
+    zero)."""
     gd = gen_device or device
     cap = wl.capacity(li)
     shape = (wl.batch, cap, wl.n_kv, wl.head_dim)
@@ -180,9 +193,18 @@ def make_cache(wl: Workload, li: int, device="cpu", gen_device=None, sequences=N
     v = torch.zeros(shape, dtype=wl.torch_dtype, device=device)
     seqs = range(wl.batch) if sequences is None else sequences
     for b in seqs:
-        g = _gen(wl.seed * 1000003 + 17 * li + 7 + 104729 * (b + 1), gd)
-        k[b] = _randn(shape[1:], g, gd, dtype=wl.torch_dtype).to(device)
-        v[b] = _randn(shape[1:], g, gd, dtype=wl.torch_dtype).to(device)
+        _draw_sequence_rows(wl, li, b, k[b], v[b], gd)
+    return k, v
+
+
+def make_sequence_cache(wl: Workload, li: int, b: int, device="cpu", gen_device=None):
+    """Sequence b's entry of make_cache alone, as [1, capacity, n_kv, d]
+    tensors (the same rows, without the other sequences' memory)."""
+    gd = gen_device or device
+    shape = (1, wl.capacity(li), wl.n_kv, wl.head_dim)
+    k = torch.empty(shape, dtype=wl.torch_dtype, device=device)
+    v = torch.empty(shape, dtype=wl.torch_dtype, device=device)
+    _draw_sequence_rows(wl, li, b, k[0], v[0], gd)
     return k, v
 
 

@@ -243,26 +243,37 @@ int spark_dbg_attention(const spark_geom* g, const float* q_rot, const spark_kv_
                         float* a, int32_t n_ctas, void* workspace, size_t workspace_bytes,
                         void* stream);
 
-/* The same attention for callers that cannot allocate device memory (code
- * running while a stream is captured into a CUDA graph, hosts whose memory
- * pool owns the whole device, loops that must not allocate).  It takes no
- * workspace: its scratch -- the split-K partial results, the merge tickets
- * and an error word -- is a fixed array of about 2 MiB inside the library,
- * which every GPU that loads the library holds until the process exits.  No
- * counterpart on the source pages: this entry point is this library's own.
- *   Arguments and results as spark_dbg_attention, without n_ctas and the
- *   workspace.  Limit: batch * n_kv <= 256, else SPARK_ERR_WORKSPACE (nothing
- *   enqueued).  Allocates nothing (no cudaMalloc, no allocating library call).
+/* The same attention for callers that cannot allocate device memory: hosts
+ * whose own memory pool owns the whole device and forbids allocations by
+ * plug-ins, and latency-critical loops that must not allocate mid-run.  It
+ * takes no workspace: its scratch -- the split-K partial results, the merge
+ * tickets and an error word -- is a fixed array of about 2.4 MiB inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  No counterpart on the source pages: this entry point is this
+ * library's own.
+ *   Arguments, checks and results as spark_dbg_attention, without n_ctas
+ *   and the workspace; the grid is the one spark_dbg_attention chooses by
+ *   itself, at most 320 CTAs.  Limit: batch * n_kv <= 256, else
+ *   SPARK_ERR_WORKSPACE (nothing enqueued).  Allocates nothing (no
+ *   cudaMalloc, no cudaFree, no allocating library call).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.  Every call clears the array's tickets and
- *   error word and then shares the array: calls that overlap on the GPU (on
- *   different streams, or on one stream without ordering) race and must not
- *   be issued. */
+ *   before any stream capture.  Every call clears the array's merge tickets
+ *   and then shares the array: calls that overlap on the GPU (on different
+ *   streams, or on one stream without ordering) race and must not be
+ *   issued.  Failures a kernel records (bits as spark_attn_error_word) stay
+ *   in the array's error word until spark_dbg_attention_noalloc_error_word
+ *   reads it. */
 int spark_dbg_attention_noalloc(const spark_geom* g, const float* q_rot,
                                 const spark_kv_layer* kv, int32_t layer_class,
                                 const int32_t* positions, int32_t batch, float* a,
                                 void* stream);
+
+/* Read and clear the error word of spark_dbg_attention_noalloc's fixed array
+ * on the current device (the bits of every call since the last read).
+ * SYNCHRONISES `stream`; allocates nothing.  No counterpart on the source
+ * pages. */
+int spark_dbg_attention_noalloc_error_word(uint32_t* word, void* stream);
 
 /* Head gate + o_proj + raw residual (attn.rs: encode_sigmoid_head_gate_mul
  * and the o_proj GEMV; mod.rs: encode_residual_add).

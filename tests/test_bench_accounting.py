@@ -50,8 +50,27 @@ def test_ragged_batch_counts_each_sequence_window():
     assert bench.step_bytes(wl)["total"] == want
 
 
+def test_attention_bytes_split_by_layer_class():
+    wl = synth.workloads()["full+sliding_bf16_b8_ctx131072"]
+    per = bench.step_bytes(wl)["per_kernel"]
+    # the full layer's attention alone: 8 sequences x 131073 rows
+    assert per["attention_full"] == 8 * 131073 * ROW_BF16 == 4_295_000_064
+    assert per["attention_sliding"] == 8 * 512 * ROW_BF16
+    assert per["attention_full"] + per["attention_sliding"] == per["attention"]
+    assert bench.stage_layers(wl, "attention_full") == [0]
+    assert bench.stage_layers(wl, "attention_sliding") == [1]
+    assert bench.stage_layers(wl, "qkv_rope") == [0, 1]
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    wls = synth.workloads()
+    sizes = {n: bench.step_bytes(w)["total"] for n, w in wls.items()}
+    assert bench.DEFAULT_WORKLOAD == max(sizes, key=sizes.get)
+    assert bench.TARGET_WORKLOAD in wls
+
+
 def test_attention_traffic_scales_with_the_rows_read():
-    t, src = bench.measured_traffic("some_other_workload", "attention", 1_000_000)
+    t, src = bench.measured_traffic("some_other_workload", "attention_full", 1_000_000)
     assert t == int(1_000_000 * bench.ATTN_TRAFFIC_RATIO) and "scaled" in src
     assert 1.0 <= bench.ATTN_TRAFFIC_RATIO < 1.02
     t, src = bench.measured_traffic("full+sliding_bf16_b1_pos700", "qkv_rope", 0)
