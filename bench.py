@@ -143,14 +143,24 @@ TRAFFIC = {
     ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_021_696,
     ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_403_904,
     ("full_bf16_b1_ctx131072", "attention_full"): 541_357_056,
+    ("full_bf16_b16_ctx512-32768", "attention_full"): 1_119_738_880,
 }
+# DRAM bytes per algorithmic byte of the attention kernel in two captures:
+# one sequence of 131072 rows (537 MB read), and the first 16 sequences of
+# the ragged 64-sequence batch (1.11 GB over contexts of 6568 to 28494 rows)
 ATTN_TRAFFIC_RATIO = 541_357_056 / 536_875_008
+ATTN_RAGGED_TRAFFIC_RATIO = 1_119_738_880 / 1_111_035_904
+# workloads whose attention scales the ragged capture (the same sequences' rows)
+RAGGED_ATTENTION = ("full+sliding_bf16_b64_ctx512-32768",)
 
 
 def measured_traffic(workload: str, kernel: str, bytes_per_launch: float):
     """(traffic per launch, how it was obtained) or (None, reason)."""
     if (workload, kernel) in TRAFFIC:
         return TRAFFIC[(workload, kernel)], "ncu capture of this workload"
+    if kernel == "attention_full" and workload in RAGGED_ATTENTION:
+        return (int(bytes_per_launch * ATTN_RAGGED_TRAFFIC_RATIO),
+                "ncu capture of its first 16 sequences (full_bf16_b16_ctx512-32768), scaled by rows read")
     if kernel.startswith("attention"):
         return int(bytes_per_launch * ATTN_TRAFFIC_RATIO), "ncu capture at 131072 rows, scaled by rows read"
     return None, "no capture of this kernel on this workload"

@@ -73,6 +73,13 @@ def test_attention_traffic_scales_with_the_rows_read():
     t, src = bench.measured_traffic("some_other_workload", "attention_full", 1_000_000)
     assert t == int(1_000_000 * bench.ATTN_TRAFFIC_RATIO) and "scaled" in src
     assert 1.0 <= bench.ATTN_TRAFFIC_RATIO < 1.02
+    t, src = bench.measured_traffic("full+sliding_bf16_b64_ctx512-32768", "attention_full", 1_000_000)
+    assert t == int(1_000_000 * bench.ATTN_RAGGED_TRAFFIC_RATIO) and "16 sequences" in src
+    assert 1.0 <= bench.ATTN_RAGGED_TRAFFIC_RATIO < 1.02
+    # the capture's algorithmic bytes: the rows its 16 sequences read
+    wl = synth.workloads()["full_bf16_b16_ctx512-32768"]
+    assert bench.step_bytes(wl)["per_kernel"]["attention_full"] == 1_111_035_904
+    assert wl.positions == synth.workloads()["full+sliding_bf16_b64_ctx512-32768"].positions[:16]
     t, src = bench.measured_traffic("full+sliding_bf16_b1_pos700", "qkv_rope", 0)
     assert t == bench.TRAFFIC[("full+sliding_bf16_b1_pos700", "qkv_rope")]
     assert bench.measured_traffic("x", "gate_oproj", 1)[0] is None
