@@ -11,6 +11,7 @@
 //    seq_len exceeds its capacity;
 //  * RealForwardError::{Unsupported, Gpu} become the status codes.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -30,6 +31,14 @@ int device_sm_count() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
   if (dev < 64) cached[dev] = n;
   return n;
+}
+
+namespace {
+uint64_t* g_layer_trace = nullptr;  // trace region of the decode call being enqueued, or null
+}
+
+uint64_t* layer_trace(int kind) {
+  return g_layer_trace ? g_layer_trace + (size_t)kind * kTraceCtas * kTraceEvs : nullptr;
 }
 
 EncodeTiledFn tensor_map_encoder() {
@@ -238,6 +247,10 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
   int rotary_dim;
   double theta;
   rope_for(g, layer_class, &rotary_dim, &theta);
+  static const bool tracing = getenv("SPARK_TRACE_LAYER") != nullptr;
+  static unsigned calls = 0;
+  if (tracing)
+    g_layer_trace = ws_at<uint64_t>(workspace, L.trace) + (size_t)(calls++ & 1) * 3 * kTraceCtas * kTraceEvs;
   cudaError_t e = run_qkv(pick_path(SPARK_PATH_AUTO, w->dtype, g, rotary_dim, batch), g, h, w, kv,
                           rotary_dim, theta, positions, batch, q_rot, g_logits, err, workspace, L, st);
   if (e == cudaSuccess)
@@ -248,6 +261,7 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
   if (e == cudaSuccess)
     e = run_oproj(pick_path(SPARK_PATH_AUTO, w->dtype, g, 0, batch), g, a, g_logits, h, w, batch, out,
                   err, workspace, L, st);
+  g_layer_trace = nullptr;
   return cuda_status(e);
 }
 

@@ -45,6 +45,11 @@ constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from
 // 512-row sliding layers now take 8 CTAs instead of 6); clusters of up to
 // 16 CTAs (non-portable size) were no faster.
 constexpr int kMaxCluster = 8;
+// When the next kernel may launch: 1 = once this CTA's tiles are all in and
+// its states merged or published (measured on the 36-layer step at batch 1:
+// 941 -> 932 us; the next kernel's weight stream otherwise queues ahead of
+// the last tile's and the merge's loads); 0 = right after the dependency wait.
+constexpr int kLateTrigger = 1;
 constexpr int kClusterRowsPerCta = 64;
 constexpr int64_t kClusterMaxRows = 1536;
 
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
                   float* __restrict__ part, uint32_t* __restrict__ counters, uint32_t* err,
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
-                  const __grid_constant__ AttnArgs<MAXB> args) {
+                  int trig, uint64_t* trace, const __grid_constant__ AttnArgs<MAXB> args) {
   using S = Smem<CT, NS, NC>;
   constexpr int kCT = NC * 32;  // consumer threads
   extern __shared__ unsigned char smem_raw[];
@@ -154,6 +159,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
+    cta_stamp(trace, 0);
     // A hint for the kernel after this one: its weights (o_proj) do not
     // depend on attention, so this CTA pulls its share of them into L2 while
     // HBM is otherwise idle.
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   if (warp == NC) {
    if (lane != 0) {
       pdl_wait();
-      pdl_trigger();
+      if (trig == 0) pdl_trigger();
    } else {
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
         // (decode), or any row of the chunk's staging buffer
         if ((chunk_p0 >= 0 ? staged : e == rows) && !waited) {
           pdl_wait();
-          pdl_trigger();
+          if (trig == 0) pdl_trigger();
           fence_proxy_async_global();
           waited = true;
         }
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     }
     if (!waited) {
       pdl_wait();
-      pdl_trigger();
+      if (trig == 0) pdl_trigger();
     }
    }
     __syncwarp();
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   MmaState mst;
   if (f0 >= f1) {  // cluster mode, no rows: an empty state
     pdl_wait();
-    pdl_trigger();
+    if (trig == 0) pdl_trigger();
     if (tid < kGroup) {
       cst[tid] = -INFINITY;
       cst[4 + tid] = 0.f;
@@ -293,12 +299,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     named_bar_sync(kBarConsumers, kCT);  // the previous group's merge is done
     if (!waited) {
       pdl_wait();
-      pdl_trigger();
+      if (trig == 0) pdl_trigger();
       waited = true;
+      if (tid == 0) cta_stamp(trace, 1);
     }
     const float* qg = q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
     attn_load_q<kCT>(q_s, qg, tid);
     named_bar_sync(kBarConsumers, kCT);
+    if (tid == 0 && r0 == sh.f - gs && sh.f == f0) cta_stamp(trace, 2);
     if constexpr (kMma) {
       mma_q_from_smem(mq, q_s);
       mst.reset();
@@ -334,6 +342,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       r = e;
     }
 
+    if (tid == 0) cta_stamp(trace, 3);
     const int g = b * n_kv + j;
     const int c_first = cta_of(gs, total, G), c_last = cta_of(gs + rows - 1, total, G);
     float* a_head0 = a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
@@ -344,10 +353,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     if (cl > 0)
       attn_cta_state<NC>(msm, cst);
     else
-      attn_merge_group<NC, 16>(msm, flags, part, counters, a_head0, g, c, c_first, c_last - c_first + 1);
+      attn_merge_group<NC, 16>(msm, flags, part, counters, a_head0, g, c, c_first, c_last - c_first + 1, trace);
     sh.f = gs + r1;
     if (++sh.j == n_kv) { sh.j = 0; ++sh.b; }
   }
+  if (tid == 0) cta_stamp(trace, 4);
+  // trig 1: the next kernel may launch once this CTA's tiles are all in and
+  // its group states merged or published
+  if (trig == 1) pdl_trigger();
   }  // consumers
 
   if (cl > 0) {
@@ -359,6 +372,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       attn_cluster_merge(cst, cl, a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, flags);
     }
     cluster_sync_all();
+    if (tid == 0) cta_stamp(trace, 5);
   }
 }
 
@@ -448,7 +462,9 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   cfg.numAttrs = cl > 0 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, mk, mv, mks, mvs, (int64_t)chunk.p0, cl, q_rot, a, part, counters,
                             err, batch, n_kv, capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
-                            static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes, args);
+                            static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes,
+                            kLateTrigger,
+                            chunk.p0 < 0 ? layer_trace(1) : (uint64_t*)nullptr, args);
 }
 
 template <typename CT, int NS, int NC, int MINB>

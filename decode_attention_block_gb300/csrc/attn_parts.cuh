@@ -267,7 +267,7 @@ __device__ __forceinline__ void attn_store_state(const AttnState& st, const Merg
 template <int NW, int KB = 8>
 __device__ __forceinline__ void attn_merge_group(const MergeSmem& sm, volatile int* flags, float* part,
                                                  uint32_t* counters, float* a_head0, int g, int c,
-                                                 int c_first, int cnt);
+                                                 int c_first, int cnt, uint64_t* trace = nullptr);
 
 template <int NW>
 __device__ __forceinline__ void attn_finish_group(const AttnState& st, const MergeSmem& sm,
@@ -285,7 +285,7 @@ __device__ __forceinline__ void attn_finish_group(const AttnState& st, const Mer
 template <int NW, int KB>
 __device__ __forceinline__ void attn_merge_group(const MergeSmem& sm, volatile int* flags, float* part,
                                                  uint32_t* counters, float* a_head0, int g, int c,
-                                                 int c_first, int cnt) {
+                                                 int c_first, int cnt, uint64_t* trace) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   named_bar_sync(kBarConsumers, NW * 32);
   if (warp >= kGroup) return;
@@ -337,6 +337,7 @@ __device__ __forceinline__ void attn_merge_group(const MergeSmem& sm, volatile i
   named_bar_sync(kBarMerge, kGroup * 32);
   if (flags[1]) {
     __threadfence();
+    if (threadIdx.x == 0) cta_stamp(trace, 6);
     const float* P0 = part + (int64_t)(c_first + g) * kPartFloats;
     float M2 = -INFINITY, L2 = 0.f, O2[8];
 #pragma unroll
@@ -381,6 +382,7 @@ __device__ __forceinline__ void attn_merge_group(const MergeSmem& sm, volatile i
     reinterpret_cast<float4*>(a_dst)[0] = make_float4(O2[0] * inv, O2[1] * inv, O2[2] * inv, O2[3] * inv);
     reinterpret_cast<float4*>(a_dst)[1] = make_float4(O2[4] * inv, O2[5] * inv, O2[6] * inv, O2[7] * inv);
     if (tid == 0) counters[g] = 0;  // ready for the next call
+    if (tid == 0) cta_stamp(trace, 7);
   }
 }
 

@@ -91,7 +91,7 @@ struct WsLayout {
   size_t total = 0;
 };
 
-constexpr int kTraceWords = 4096;
+constexpr int kTraceWords = 8192;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -349,6 +349,14 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
       : "l"(p));
   return r;
+}
+
+// Opt-in timeline of the per-layer kernels: slot `ev` of this CTA's eight
+// stamps (CTAs past kTraceCtas are not traced).
+constexpr int kTraceCtas = 160;
+constexpr int kTraceEvs = 8;
+__device__ __forceinline__ void cta_stamp(uint64_t* trace, int ev) {
+  if (trace != nullptr && blockIdx.x < kTraceCtas) trace[blockIdx.x * kTraceEvs + ev] = global_timer_ns();
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

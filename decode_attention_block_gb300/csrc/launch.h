@@ -93,6 +93,13 @@ cudaError_t launch_mlp_mma(const float* h, const void* norm_w, const void* gate_
 cudaError_t launch_head_mma(const float* h, const void* norm_w, const void* embed, float* logits, uint32_t* err,
                             int hidden, int vocab, int batch, float eps, const MmaWorkspace& ws, cudaStream_t st);
 
+// Opt-in per-CTA timeline of spark_attn_decode's kernels (SPARK_TRACE_LAYER
+// set in the environment): the stamp array of kernel `kind` (0 the
+// projections and rope, 1 attention, 2 the gate and o_proj) of the call being
+// enqueued -- two calls alternate between two halves of the workspace's trace
+// region -- or null.
+uint64_t* layer_trace(int kind);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                const WT* __restrict__ qkv_w, const WT* __restrict__ g_w, float* __restrict__ q_rot,
                CT* __restrict__ kc, CT* __restrict__ vc, float* __restrict__ g_out, uint32_t* err,
                int hidden, int n_q, int n_kv, int nb, int64_t capacity, int ring_capacity,
-               int rotary_dim, int stages, float eps, const __grid_constant__ QkvArgs<NB> args) {
+               int rotary_dim, int stages, float eps, uint64_t* trace,
+               const __grid_constant__ QkvArgs<NB> args) {
   constexpr int E = Chunk<WT>::kElems;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
     abort_flag = 0;
     fence_mbar_init();
+    cta_stamp(trace, 0);
   }
   __syncthreads();
 
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
   pdl_wait();
   pdl_trigger();  // the next kernel starts only once the one before this has completed
+  if (threadIdx.x == 0) cta_stamp(trace, 1);
 
   // activations: x = h * w (unscaled) and sum(h^2) per sequence
   float ss[NB];
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     inv_rms[threadIdx.x] = 1.0f / sqrtf(t / (float)hidden + eps);
   }
   __syncthreads();
+  if (threadIdx.x == 0) cta_stamp(trace, 2);
 
   for (int k = warp; warp < nw && k < cnt; k += nw) {
     const int s = k % stages;
@@ -141,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc_a[b] = acc_b[b] = make_float2(0.f, 0.f);
     const bool ok = wait_stage(&bars[s], parity, &abort_flag, err);
+    if (threadIdx.x == 0) cta_stamp(trace, k == 0 ? 3 : 4);
     if (ok) {
       const unsigned char* st = pool + (size_t)s * unit_bytes;
       row_dot2<WT, NB>(st, st + row_bytes, xs, xfloats, nchunk, acc_a, acc_b);
@@ -187,6 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (trace != nullptr) {
+    __syncthreads();
+    if (threadIdx.x == 0) cta_stamp(trace, 5);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -196,7 +205,7 @@ template <typename WT, int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     k_oproj(const float* __restrict__ a, const float* __restrict__ g, const float* h,
             const WT* __restrict__ o_w, float* out, uint32_t* err, int hidden, int q_dim, int n_q,
-            int nb, int stages) {
+            int nb, int stages, uint64_t* trace) {
   constexpr int E = Chunk<WT>::kElems;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -217,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
     abort_flag = 0;
     fence_mbar_init();
+    cta_stamp(trace, 0);
   }
   __syncthreads();
 
@@ -230,10 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
   pdl_wait();
   pdl_trigger();  // the next kernel starts only once the one before this has completed
+  if (threadIdx.x == 0) cta_stamp(trace, 1);
 
   // gated attention output: a * sigmoid(g), one gate scalar per head
   build_x_gated<E, NB, kThreads, kMaxPer>(a, g, q_dim, n_q, nb, xs, xfloats, threadIdx.x);
   __syncthreads();
+  if (threadIdx.x == 0) cta_stamp(trace, 2);
 
   for (int k = warp; warp < nw && k < cnt; k += nw) {
     const int s = k % stages;
@@ -242,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = make_float2(0.f, 0.f);
     const bool ok = wait_stage(&bars[s], parity, &abort_flag, err);
+    if (threadIdx.x == 0) cta_stamp(trace, k == 0 ? 3 : 4);
     if (ok) row_dot<WT, NB>(pool + (size_t)s * row_bytes, xs, xfloats, nchunk, acc);
     __syncwarp();
     if (ok && lane == 0 && k + stages < cnt) issue(k + stages);
@@ -256,6 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t idx = (int64_t)lane * hidden + r0 + k;
       out[idx] = h[idx] + v;  // read and written by the same thread: out may alias h
     }
+  }
+  if (trace != nullptr) {
+    __syncthreads();
+    if (threadIdx.x == 0) cta_stamp(trace, 5);
   }
 }
 
@@ -294,7 +311,7 @@ cudaError_t qkv_launch(const float* h, const void* norm_w, const void* qkv_w, co
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, h, (const WT*)norm_w,
                     (const WT*)qkv_w, (const WT*)g_w, q_rot, (CT*)kc, (CT*)vc, g_out, err, hidden,
-                    n_q, n_kv, nb, capacity, ring_capacity, rotary_dim, stages, eps, args);
+                    n_q, n_kv, nb, capacity, ring_capacity, rotary_dim, stages, eps, layer_trace(0), args);
 }
 
 template <typename WT, typename CT>
@@ -328,7 +345,7 @@ cudaError_t oproj_launch(const float* a, const float* g, const float* h, const v
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, a, g, h, (const WT*)o_w, out, err,
-                    hidden, q_dim, n_q, nb, stages);
+                    hidden, q_dim, n_q, nb, stages, layer_trace(2));
 }
 
 template <typename WT>
