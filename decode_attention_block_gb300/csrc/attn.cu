@@ -45,6 +45,7 @@ constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from
 // 512-row sliding layers now take 8 CTAs instead of 6); clusters of up to
 // 16 CTAs (non-portable size) were no faster.
 constexpr int kMaxCluster = 8;
+constexpr int kStateBytes = (8 + kGroup * kHeadDim) * 4;  // a CTA's state: m[4], l[4], o[4][256]
 // When the next kernel may launch: 1 = once this CTA's tiles are all in and
 // its states merged or published (measured on the 36-layer step at batch 1:
 // 941 -> 932 us; the next kernel's weight stream otherwise queues ahead of
@@ -67,8 +68,11 @@ struct Smem {
   static constexpr int kO = kL + NC * 4 * 4;
   static constexpr int kBars = kO + NC * 4 * kHeadDim * 4;
   static constexpr int kCst = kBars + 2 * kStages * 8;       // cluster mode: the CTA's state
-  static constexpr int kFlags = kCst + (8 + 4 * kHeadDim) * 4;
-  static constexpr int kBytes = kFlags + 16;
+  static constexpr int kFlags = kCst + kStateBytes;
+  static constexpr int kRecv = kFlags + 16;                   // cluster rank 0: the other ranks' states
+  static constexpr int kMergeBar = kRecv + (kMaxCluster - 1) * kStateBytes;
+  static constexpr int kBytes = kMergeBar + 16;
+  static_assert(kCst % 16 == 0 && kRecv % 16 == 0, "bulk copies of the states need 16-byte alignment");
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 (128B swizzle)
 };
 
@@ -149,12 +153,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + S::kBars);
   uint64_t* empty_bar = full_bar + NS;
   volatile int* flags = reinterpret_cast<volatile int*>(base + S::kFlags);  // [0] abort, [1] last
+  uint64_t* merge_bar = reinterpret_cast<uint64_t*>(base + S::kMergeBar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
+    }
+    if (cl > 0 && blockIdx.x % cl == 0) {
+      // cluster rank 0 receives the other ranks' states: one phase, their bytes
+      mbar_init(merge_bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(merge_bar, (uint32_t)((cl - 1) * kStateBytes));
     }
     flags[0] = 0;
     flags[1] = 0;
@@ -173,6 +184,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     }
   }
   __syncthreads();
+  // cluster mode: rank 0's merge barrier is ready once every rank has passed
+  // here (the matching wait comes before a rank sends its state)
+  if (cl > 0) cluster_arrive();
 
   // Programmatic dependent launch.  q_rot and the token's own cache row
   // (the last row of each (sequence, KV head) group) come from the kernel
@@ -364,14 +378,44 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   }  // consumers
 
   if (cl > 0) {
-    // every thread of the cluster: the CTA states are complete, rank 0
-    // merges them into the output, and no CTA leaves before it has
-    cluster_sync_all();
-    if (c % cl == 0 && warp < kGroup) {
+    // Every rank but 0 stores its state into rank 0's shared memory with
+    // remote stores that complete on rank 0's merge barrier, and leaves; rank
+    // 0 merges the states in rank order and writes the group's output.
+    // (Rank 0 pulling the states through DSMEM took a cluster barrier before
+    // and after the reads.)
+    __syncthreads();  // this CTA's state is complete
+    cluster_wait();   // rank 0's merge barrier is initialised
+    const int r = c % cl;
+    if (r != 0) {
+      if (warp < kGroup) {  // head `warp`: m, l and lane's 8 dims of o
+        const int h = warp;
+        const uint32_t dst = cluster_addr(base + S::kRecv + (r - 1) * kStateBytes, 0);
+        const uint32_t bar = cluster_addr(merge_bar, 0);
+        const float4* src = reinterpret_cast<const float4*>(cst + 8 + h * kHeadDim + 8 * lane);
+        const uint32_t o = dst + (uint32_t)(8 + h * kHeadDim + 8 * lane) * 4;
+        st_async_f32x4(o, src[0], bar);
+        st_async_f32x4(o + 16, src[1], bar);
+        if (lane == 0) {
+          st_async_f32(dst + (uint32_t)h * 4, cst[h], bar);
+          st_async_f32(dst + (uint32_t)(4 + h) * 4, cst[4 + h], bar);
+        }
+      }
+    } else if (warp < kGroup) {
       const int g = c / cl, b = g / n_kv, j = g % n_kv;
-      attn_cluster_merge(cst, cl, a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, flags);
+      // bounded; on time-out the merge still waits (bounded again) so that
+      // no copy lands in the shared memory of an exited CTA
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(merge_bar, 0, flags, kWaitLimitNs));
+      if (!ok) {
+        if (lane == 0 && !flags[0]) {
+          flags[0] = 1;
+          atomicOr(err, kErrWaitTimeout);
+        }
+        int never = 0;
+        mbar_wait_bounded(merge_bar, 0, &never, kWaitLimitNs);
+      }
+      attn_cluster_merge_local(cst, reinterpret_cast<const float*>(base + S::kRecv), cl,
+                               a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, flags);
     }
-    cluster_sync_all();
     if (tid == 0) cta_stamp(trace, 5);
   }
 }

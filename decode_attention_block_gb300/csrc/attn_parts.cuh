@@ -625,6 +625,30 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t ra) {
   return v;
 }
 
+// the cluster barrier split in two: arrive (release) early, wait (acquire)
+// where the other CTAs' earlier writes are needed
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Remote stores into the shared memory of a CTA of the cluster (addr, bar:
+// shared::cluster addresses) whose bytes complete that CTA's mbarrier
+// transaction count; the data leaves from registers.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+               "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+               : "memory");
+}
+
 // The CTA's state of its group from the NW warps' states in `sm`: warp h < 4
 // merges head h into cst ([4] m, [4] l, [4][256] unnormalised o).
 template <int NW>
@@ -660,47 +684,42 @@ __device__ __forceinline__ void attn_cta_state(const MergeSmem& sm, float* cst) 
   dst[1] = make_float4(O[4], O[5], O[6], O[7]);
 }
 
-// Rank 0 of a cluster, warp h < 4: merge the cl CTA states (DSMEM, rank
-// order, eight ranks' loads issued together per round, a running max across
-// rounds) and write head h of the group's output.
-__device__ __forceinline__ void attn_cluster_merge(const float* cst, int cl, float* a_head0,
-                                                   volatile int* flags) {
+// Rank 0 of a cluster, warp h < 4: merge its own state and the cl - 1 states
+// the other ranks sent into `recv` (rank r at slot r - 1), in rank order, and
+// write head h of the group's output.
+__device__ __forceinline__ void attn_cluster_merge_local(const float* cst, const float* recv, int cl,
+                                                         float* a_head0, volatile int* flags) {
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float M = -INFINITY, L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int q0 = 0; q0 < cl; q0 += 8) {
-    float mq[8], lq[8];
-    float4 x0[8], x1[8];
+  constexpr int kF = 8 + kGroup * kHeadDim;  // floats of a state
+  float mq[8], lq[8];
+  float4 x0[8], x1[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (q0 + q < cl) {
-        mq[q] = ld_cluster_f32(cluster_addr(cst + h, (uint32_t)(q0 + q)));
-        lq[q] = ld_cluster_f32(cluster_addr(cst + 4 + h, (uint32_t)(q0 + q)));
-        const uint32_t ra = cluster_addr(cst + 8 + h * kHeadDim + 8 * lane, (uint32_t)(q0 + q));
-        x0[q] = ld_cluster_f4(ra);
-        x1[q] = ld_cluster_f4(ra + 16);
-      } else {
-        mq[q] = -INFINITY;
-        lq[q] = 0.f;
-        x0[q] = x1[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+  for (int q = 0; q < 8; ++q) {
+    if (q < cl) {
+      const float* st = q == 0 ? cst : recv + (q - 1) * kF;
+      mq[q] = st[h];
+      lq[q] = st[4 + h];
+      const float4* src = reinterpret_cast<const float4*>(st + 8 + h * kHeadDim + 8 * lane);
+      x0[q] = src[0];
+      x1[q] = src[1];
+    } else {
+      mq[q] = -INFINITY;
+      lq[q] = 0.f;
+      x0[q] = x1[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float mb = M;
+  }
+  float M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) mb = fmaxf(mb, mq[q]);
-    const float rs = M == -INFINITY ? 0.f : exp2f(M - mb);  // rescale the earlier rounds
-    L *= rs;
+  for (int q = 0; q < 8; ++q) M = fmaxf(M, mq[q]);
+  float L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) O[i] *= rs;
-    M = mb;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float scl = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
-      L = fmaf(lq[q], scl, L);
-      O[0] = fmaf(x0[q].x, scl, O[0]); O[1] = fmaf(x0[q].y, scl, O[1]);
-      O[2] = fmaf(x0[q].z, scl, O[2]); O[3] = fmaf(x0[q].w, scl, O[3]);
-      O[4] = fmaf(x1[q].x, scl, O[4]); O[5] = fmaf(x1[q].y, scl, O[5]);
-      O[6] = fmaf(x1[q].z, scl, O[6]); O[7] = fmaf(x1[q].w, scl, O[7]);
-    }
+  for (int q = 0; q < 8; ++q) {
+    const float scl = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
+    L = fmaf(lq[q], scl, L);
+    O[0] = fmaf(x0[q].x, scl, O[0]); O[1] = fmaf(x0[q].y, scl, O[1]);
+    O[2] = fmaf(x0[q].z, scl, O[2]); O[3] = fmaf(x0[q].w, scl, O[3]);
+    O[4] = fmaf(x1[q].x, scl, O[4]); O[5] = fmaf(x1[q].y, scl, O[5]);
+    O[6] = fmaf(x1[q].z, scl, O[6]); O[7] = fmaf(x1[q].w, scl, O[7]);
   }
   if (!flags[0]) {
     const float inv = 1.0f / L;

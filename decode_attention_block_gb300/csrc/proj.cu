@@ -52,6 +52,15 @@ constexpr int kMaxPer = 8192 / 4 / kThreads;  // float4 of an activation vector 
 #define SPARK_GEMV_SMEM_KB 200
 #endif
 constexpr size_t kSmemBudget = SPARK_GEMV_SMEM_KB * 1024;
+// q_k_v_proj units (row pairs) each CTA requests before the dependency wait;
+// the rest go out once x is built.  Loads issued after a CTA-wide weight
+// stream wait for it: with every stage requested up front, h arrived 4.3 us
+// after the wait, with 6 (60 KB of 207 KB) after 2.5 us, and the launch
+// ended 1.5 us sooner (36-layer step at batch 1: 925 -> 910 us).  Holding
+// the whole share (21 units, 222 KB) instead of 16 stages did not help.
+constexpr int kQkvPre = 6;
+// o_proj rows per CTA whose residual is loaded with the activations
+constexpr int kOprojHRows = 64;
 
 template <int NB>
 struct QkvArgs {
@@ -112,10 +121,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bulk_load(dst + row_bytes, row_ptr(un.row_b), (uint32_t)row_bytes, &bars[s]);
   };
 
-  // The weight stream does not depend on the previous kernel: request every
-  // stage now (each warp the units it will consume first).
-  if (lane == 0 && warp < nw)
-    for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
+  // The weight stream does not depend on the previous kernel: request the
+  // first kQkvPre stages now (each warp the units it will consume first),
+  // the rest after x is built.
+  auto issue_range = [&](int lo, int hi) {
+    if (lane == 0 && warp < nw)
+      for (int k = warp; k < hi && k < cnt; k += nw)
+        if (k >= lo) issue(k);
+  };
+  issue_range(0, kQkvPre < stages ? kQkvPre : stages);
   pdl_wait();
   pdl_trigger();  // the next kernel starts only once the one before this has completed
   if (threadIdx.x == 0) cta_stamp(trace, 1);
@@ -136,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0) cta_stamp(trace, 2);
+  issue_range(kQkvPre < stages ? kQkvPre : stages, stages);
 
   for (int k = warp; warp < nw && k < cnt; k += nw) {
     const int s = k % stages;
@@ -216,11 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* pool = smem + sizeof(float) * NB * xfloats;
   uint64_t* bars = reinterpret_cast<uint64_t*>(pool + (size_t)stages * row_bytes);
   __shared__ int abort_flag;
+  __shared__ float hs[kOprojHRows * NB];  // the residual rows of the share, loaded with the activations
 
   const int r0 = (int)((int64_t)hidden * blockIdx.x / gridDim.x);
   const int r1 = (int)((int64_t)hidden * (blockIdx.x + 1) / gridDim.x);
   const int cnt = r1 - r0;
   const int nw = stages < kWarps ? stages : kWarps;
+  // every row of the share resident: warps take rows in pairs, one pass over
+  // the activations for both (at batch 1 the fp32 activation vector, twice the
+  // bytes of a bf16 row, otherwise dominates the shared-memory reads)
+  const bool pairs = stages >= cnt;
+  const bool h_smem = cnt <= kOprojHRows;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
@@ -242,12 +263,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();  // the next kernel starts only once the one before this has completed
   if (threadIdx.x == 0) cta_stamp(trace, 1);
 
+  // the residual rows, requested with the activations so that the epilogue
+  // needs no round trip of its own (out may alias h: every element is read
+  // here, before this CTA writes it)
+  const int hk = threadIdx.x / NB, hb = threadIdx.x - hk * NB;
+  float hv = 0.f;
+  if (h_smem && hk < cnt && hb < nb) hv = h[(int64_t)hb * hidden + r0 + hk];
   // gated attention output: a * sigmoid(g), one gate scalar per head
   build_x_gated<E, NB, kThreads, kMaxPer>(a, g, q_dim, n_q, nb, xs, xfloats, threadIdx.x);
+  if (h_smem && hk < cnt && hb < nb) hs[hk * NB + hb] = hv;
   __syncthreads();
   if (threadIdx.x == 0) cta_stamp(trace, 2);
 
-  for (int k = warp; warp < nw && k < cnt; k += nw) {
+  auto finish = [&](int k, const float2 (&acc)[NB]) {  // out = h + the row's dot product
+    float v = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float sb = warp_sum(acc[b].x + acc[b].y);
+      if (lane == b) v = sb;
+    }
+    if (lane < nb) {
+      const int64_t idx = (int64_t)lane * hidden + r0 + k;
+      out[idx] = (h_smem ? hs[k * NB + lane] : h[idx]) + v;  // read and written by the same thread
+    }
+  };
+  if (pairs) {
+    for (int p = warp; p < (cnt + 1) / 2; p += kWarps) {
+      const int k0 = 2 * p, k1 = 2 * p + 1;
+      float2 acc0[NB], acc1[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
+      bool ok = wait_stage(&bars[k0], 0, &abort_flag, err);
+      if (k1 < cnt) ok = ok && wait_stage(&bars[k1], 0, &abort_flag, err);
+      if (threadIdx.x == 0) cta_stamp(trace, p == 0 ? 3 : 4);
+      if (!ok) continue;
+      if (k1 < cnt) {
+        row_dot2<WT, NB>(pool + (size_t)k0 * row_bytes, pool + (size_t)k1 * row_bytes, xs, xfloats, nchunk, acc0,
+                         acc1);
+        finish(k0, acc0);
+        finish(k1, acc1);
+      } else {
+        row_dot<WT, NB>(pool + (size_t)k0 * row_bytes, xs, xfloats, nchunk, acc0);
+        finish(k0, acc0);
+      }
+    }
+  }
+  for (int k = warp; !pairs && warp < nw && k < cnt; k += nw) {
     const int s = k % stages;
     const uint32_t parity = (uint32_t)((k / stages) & 1);
     float2 acc[NB];
@@ -259,16 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (ok && lane == 0 && k + stages < cnt) issue(k + stages);
     if (!ok) continue;
-    float v = 0.f;
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float sb = warp_sum(acc[b].x + acc[b].y);
-      if (lane == b) v = sb;
-    }
-    if (lane < nb) {
-      const int64_t idx = (int64_t)lane * hidden + r0 + k;
-      out[idx] = h[idx] + v;  // read and written by the same thread: out may alias h
-    }
+    finish(k, acc);
   }
   if (trace != nullptr) {
     __syncthreads();
