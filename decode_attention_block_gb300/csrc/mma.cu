@@ -72,6 +72,11 @@
 namespace spark {
 namespace {
 
+// Weight stages the producer requests before the dependency wait; the
+// activations of the first stages follow the wait, then the rest of their
+// weights.  With every stage's weights requested first, the activations
+// queued behind them (batch 64: 1% slower per step than 2 or 4).
+constexpr int kMmaPreW = 4;
 constexpr int kMmaThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kKBlock = 64;                                   // K elements per stage = one 128 B row
@@ -737,15 +742,16 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         }
       };
       const int pre = nk < p.stages ? nk : p.stages;
-      for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full_bar[i], a_bytes + x_bytes);
-        load_w(i, kb0 + i);
-      }
+      const int pre_w = pre < kMmaPreW ? pre : kMmaPreW;  // weight stages requested before the wait
+      for (int i = 0; i < pre; ++i) mbar_arrive_expect_tx(&full_bar[i], a_bytes + x_bytes);
+      for (int i = 0; i < pre_w; ++i) load_w(i, kb0 + i);
       pdl_wait();
       pdl_trigger();
       fence_proxy_async_global();
+      // the activations of the first stages, then the rest of their weights
       for (int i = 0; i < pre; ++i)
         tma_load_2d(stage(i) + kABytes * mt, &tm_x, &full_bar[i], (kb0 + i) * kKBlock, x_row);
+      for (int i = pre_w; i < pre; ++i) load_w(i, kb0 + i);
       stamp(p, kTrXIssued);
       int issued = pre;
       for (int i = pre; i < nk; ++i) {
