@@ -44,6 +44,8 @@ if ROOT not in sys.path:
 from decode_attention_block_gb300 import build_lib, synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "full+sliding_bf16_b64_ctx512-32768"
+# the workload of --prefill (one sequence) and --decoder unless --workload is given
+DEFAULT_CHUNK_WORKLOAD = "full+sliding_bf16_b1_pos700"
 # the long-context workload the HBM targets are stated on, timed beside the
 # default one: its full layer's attention kernel and its whole step
 TARGET_WORKLOAD = "full+sliding_bf16_b8_ctx131072"
@@ -947,7 +949,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about two seconds' worth)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.workloads()))
+    ap.add_argument("--workload", default=None, choices=sorted(synth.workloads()),
+                    help=f"default: {DEFAULT_WORKLOAD}; with --prefill or --decoder: {DEFAULT_CHUNK_WORKLOAD}")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--copies", type=int, default=0, help="rotating input copies (0: enough to beat L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -968,6 +971,8 @@ def main():
     rank, local, world = dist_env()
     if args.gpus > 1 and world != args.gpus:
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE is {world}")
+    if args.workload is None:
+        args.workload = DEFAULT_CHUNK_WORKLOAD if (args.prefill > 0 or args.decoder) else DEFAULT_WORKLOAD
     wl = synth.workloads()[args.workload]
 
     if args.impl == "reference":

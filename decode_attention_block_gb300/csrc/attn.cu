@@ -46,6 +46,8 @@ constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from
 // 16 CTAs (non-portable size) were no faster.
 constexpr int kMaxCluster = 8;
 constexpr int kStateBytes = (8 + kGroup * kHeadDim) * 4;  // a CTA's state: m[4], l[4], o[4][256]
+template <int MINB>
+constexpr int kRecvSlots = MINB == 1 ? kMaxCluster - 1 : 0;  // cluster mode only with one CTA per SM
 // When the next kernel may launch: 1 = once this CTA's tiles are all in and
 // its states merged or published (measured on the 36-layer step at batch 1:
 // 941 -> 932 us; the next kernel's weight stream otherwise queues ahead of
@@ -54,7 +56,10 @@ constexpr int kLateTrigger = 1;
 constexpr int kClusterRowsPerCta = 64;
 constexpr int64_t kClusterMaxRows = 1536;
 
-template <typename CT, int NS, int NC>
+// RECV: slots for the other ranks' states in cluster mode (0 in the
+// two-CTAs-per-SM kernel, which never runs in cluster mode: the slots would
+// keep its second CTA off the SM)
+template <typename CT, int NS, int NC, int RECV>
 struct Smem {
   static_assert(NS % NC == 0, "each stage must belong to one consumer warp");
   static constexpr int kStages = NS;
@@ -70,7 +75,7 @@ struct Smem {
   static constexpr int kCst = kBars + 2 * kStages * 8;       // cluster mode: the CTA's state
   static constexpr int kFlags = kCst + kStateBytes;
   static constexpr int kRecv = kFlags + 16;                   // cluster rank 0: the other ranks' states
-  static constexpr int kMergeBar = kRecv + (kMaxCluster - 1) * kStateBytes;
+  static constexpr int kMergeBar = kRecv + RECV * kStateBytes;
   static constexpr int kBytes = kMergeBar + 16;
   static_assert(kCst % 16 == 0 && kRecv % 16 == 0, "bulk copies of the states need 16-byte alignment");
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 (128B swizzle)
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
                   int trig, uint64_t* trace, const __grid_constant__ AttnArgs<MAXB> args) {
-  using S = Smem<CT, NS, NC>;
+  using S = Smem<CT, NS, NC, kRecvSlots<MINB>>;
   constexpr int kCT = NC * 32;  // consumer threads
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base =
@@ -445,7 +450,7 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
                      const int32_t* positions, int batch, float* a, float* part,
                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
                      size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st) {
-  using S = Smem<CT, NS, NC>;
+  using S = Smem<CT, NS, NC, kRecvSlots<MINB>>;
   AttnArgs<MAXB> args;
   args.prefix[0] = 0;
   for (int b = 0; b < MAXB; ++b) {
@@ -462,8 +467,8 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
   if (cl > kMaxCluster) cl = kMaxCluster;
   if (n_ctas > 0 || cl < 2 || max_rows > kClusterMaxRows ||
-      (int64_t)groups * cl > device_sm_count() || (int64_t)groups * cl > max_ctas)
-    cl = 0;
+      (int64_t)groups * cl > device_sm_count() || (int64_t)groups * cl > max_ctas || MINB > 1)
+    cl = 0;  // cluster mode only in the kernel of one CTA per SM (it holds the ranks' state slots)
   int G = cl > 0 ? groups * cl : n_ctas;
   if (cl == 0 && G <= 0) {
     const int64_t want = (total + kMinRowsPerCta - 1) / kMinRowsPerCta;
