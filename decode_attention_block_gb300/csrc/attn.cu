@@ -81,6 +81,14 @@ struct Smem {
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 (128B swizzle)
 };
 
+// The long-history kernel runs two CTAs per SM: both must fit the SM's
+// 228 KB of shared memory (1 KB of it reserved per CTA).
+static_assert(CacheT<__nv_bfloat16>::kDeepBlocks *
+                      (Smem<__nv_bfloat16, CacheT<__nv_bfloat16>::kDeep, kConsumers,
+                            kRecvSlots<CacheT<__nv_bfloat16>::kDeepBlocks>>::kAlloc + 1024) <=
+                  228 * 1024,
+              "the two-CTAs-per-SM attention kernel no longer fits two CTAs on an SM");
+
 template <int MAXB>
 struct AttnArgs {
   int64_t prefix[MAXB + 1];  // rows read by sequences before b
