@@ -90,7 +90,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   volatile int* flags = reinterpret_cast<volatile int*>(base + S::kFlags);  // [0] abort
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = blockIdx.x % n_kv, grp = blockIdx.x / n_kv;
+  // the last groups (the latest tokens, the longest windows) first: with
+  // more CTAs than fit at once, the short ones then fill the tail
+  const int rb = (int)gridDim.x - 1 - (int)blockIdx.x;
+  const int j = rb % n_kv, grp = rb / n_kv;
   const int t0 = grp * NC, t1 = t0 + NC < m ? t0 + NC : m;
   const Span sp = span_of(p0, t0, t1, full != 0, window, ring);
   if (tid == 0) {
