@@ -48,11 +48,15 @@ constexpr int kMaxCluster = 8;
 constexpr int kStateBytes = (8 + kGroup * kHeadDim) * 4;  // a CTA's state: m[4], l[4], o[4][256]
 template <int MINB>
 constexpr int kRecvSlots = MINB == 1 ? kMaxCluster - 1 : 0;  // cluster mode only with one CTA per SM
-// When the next kernel may launch: 1 = once this CTA's tiles are all in and
-// its states merged or published (measured on the 36-layer step at batch 1:
-// 941 -> 932 us; the next kernel's weight stream otherwise queues ahead of
-// the last tile's and the merge's loads); 0 = right after the dependency wait.
-constexpr int kLateTrigger = 1;
+// When the next kernel may launch: 0 = right after the dependency wait, 1 =
+// once this CTA's tiles are all in and its states merged or published.  Since
+// every decode tile is requested before the wait (the token's own row comes
+// from L2 after it), an early o_proj weight stream no longer delays the tiles
+// at small batch: the two-layer batch-1 step 50.0 -> 49.1 us, the 36-layer one
+// 865 -> 859 us.  Batches of more than kEarlyTriggerBatch keep the late
+// trigger (64 sequences: 737.5 vs 740.7 us; at 64 short contexts 149.3 vs
+// 152.7 us).
+constexpr int kEarlyTriggerBatch = 4;
 constexpr int kClusterRowsPerCta = 64;
 constexpr int64_t kClusterMaxRows = 1536;
 
@@ -147,7 +151,7 @@ template <typename CT, int NS, int NC, int MINB, int MAXB>
 __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     k_attn_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
-                  int64_t chunk_p0, int cl, const float* __restrict__ q_rot, float* __restrict__ a_out,
+                  const void* kcache, const void* vcache, int64_t chunk_p0, int cl, const float* __restrict__ q_rot, float* __restrict__ a_out,
                   float* __restrict__ part, uint32_t* __restrict__ counters, uint32_t* err,
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
@@ -254,9 +258,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
         if (r < w.c_rows && e > w.c_rows) e = w.c_rows;
         const bool staged = r >= w.c_rows;
         const int64_t slot = r < w.len_a ? w.first_slot + r : r - w.len_a;
-        // tiles holding rows the previous kernel wrote: the token's own row
-        // (decode), or any row of the chunk's staging buffer
-        if ((chunk_p0 >= 0 ? staged : e == rows) && !waited) {
+        // tiles holding rows the previous kernel wrote: any row of the
+        // chunk's staging buffer.  (In decode the token's own row is written
+        // over its tile by the consumer after the wait.)
+        if (chunk_p0 >= 0 && staged && !waited) {
           pdl_wait();
           if (trig == 0) pdl_trigger();
           fence_proxy_async_global();
@@ -330,6 +335,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       waited = true;
       if (tid == 0) cta_stamp(trace, 1);
     }
+    // decode: the token's own row, if this share holds the group's last row
+    const bool own_row = chunk_p0 < 0 && r1 == rows;
+    NewRow<CT> nr;
+    if (own_row) {
+      const int64_t off = (((int64_t)b * capacity + write_slot_of(pos[b], ring_capacity)) * n_kv + j) * kHeadDim;
+      nr.load(reinterpret_cast<const CT*>(kcache) + off, reinterpret_cast<const CT*>(vcache) + off, lane);
+    }
     const float* qg = q_rot + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
     attn_load_q<kCT>(q_s, qg, tid);
     named_bar_sync(kBarConsumers, kCT);
@@ -357,11 +369,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
           }
         } else {
           unsigned char* kst = stages + s * S::kStage;
+          const bool patch = own_row && e == rows;
+          if (patch) {
+            nr.store(kst, kst + S::kHalf, n - 1, lane);
+            __syncwarp();
+          }
           if constexpr (kMma)
             attn_tile_mma(kst, kst + S::kHalf, n, mq, reinterpret_cast<float*>(p_s + warp * kTile), scale_log2, mst);
           else
             attn_tile<CT>(kst, kst + S::kHalf, n, q_s, p_s + warp * kTile, scale_log2, st);
         }
+        if (own_row && e == rows) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills the stage
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
@@ -452,6 +470,33 @@ bool make_cache_map(CUtensorMap* map, const void* base, int n_kv, int64_t rows) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The grid of a launch: `total` rows x KV heads, the longest group
+// `max_rows`, `groups` = batch x KV heads.
+struct AttnPlan {
+  int ctas;     // CTAs of the launch
+  int cluster;  // CTAs per cluster (cluster mode), 0 otherwise
+};
+template <int MINB>
+AttnPlan plan_attention(int64_t total, int64_t max_rows, int groups, int n_ctas, int max_ctas) {
+  // Short histories in small launches: one cluster of cl CTAs per group,
+  // merging through DSMEM (no partials in the workspace, no ticket).
+  int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
+  if (cl > kMaxCluster) cl = kMaxCluster;
+  if (n_ctas > 0 || cl < 2 || max_rows > kClusterMaxRows ||
+      (int64_t)groups * cl > device_sm_count() || (int64_t)groups * cl > max_ctas || MINB > 1)
+    cl = 0;  // cluster mode only in the kernel of one CTA per SM (it holds the ranks' state slots)
+  int G = cl > 0 ? groups * cl : n_ctas;
+  if (cl == 0 && G <= 0) {
+    const int64_t want = (total + kMinRowsPerCta - 1) / kMinRowsPerCta;
+    const int cap = MINB * device_sm_count();
+    G = (int)(want < cap ? want : cap);
+  }
+  if (G < 1) G = 1;
+  if (G > kMaxAttnCtas) G = kMaxAttnCtas;
+  if (G > max_ctas) G = max_ctas;
+  return {G, cl};
+}
+
 template <typename CT, int NS, int NC, int MINB, int MAXB>
 cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_kv,
                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
@@ -467,25 +512,10 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
     args.pos[b] = b < batch ? positions[b] : 0;
   }
   const int64_t total = (int64_t)n_kv * args.prefix[batch];
-  // Short histories in small launches: one cluster of cl CTAs per group,
-  // merging through DSMEM (no partials in the workspace, no ticket).
   int64_t max_rows = 0;
   for (int b = 0; b < batch; ++b) max_rows = std::max(max_rows, args.prefix[b + 1] - args.prefix[b]);
-  const int groups = batch * n_kv;
-  int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
-  if (cl > kMaxCluster) cl = kMaxCluster;
-  if (n_ctas > 0 || cl < 2 || max_rows > kClusterMaxRows ||
-      (int64_t)groups * cl > device_sm_count() || (int64_t)groups * cl > max_ctas || MINB > 1)
-    cl = 0;  // cluster mode only in the kernel of one CTA per SM (it holds the ranks' state slots)
-  int G = cl > 0 ? groups * cl : n_ctas;
-  if (cl == 0 && G <= 0) {
-    const int64_t want = (total + kMinRowsPerCta - 1) / kMinRowsPerCta;
-    const int cap = MINB * device_sm_count();
-    G = (int)(want < cap ? want : cap);
-  }
-  if (G < 1) G = 1;
-  if (G > kMaxAttnCtas) G = kMaxAttnCtas;
-  if (G > max_ctas) G = max_ctas;
+  const AttnPlan plan = plan_attention<MINB>(total, max_rows, batch * n_kv, n_ctas, max_ctas);
+  const int G = plan.ctas, cl = plan.cluster;
 
   // a chunk's tokens share one sequence's cache; decode rows are per sequence
   const int64_t cache_rows = chunk.p0 >= 0 ? capacity : (int64_t)batch * capacity;
@@ -517,10 +547,10 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cl > 0 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, mk, mv, mks, mvs, (int64_t)chunk.p0, cl, q_rot, a, part, counters,
+  return cudaLaunchKernelEx(&cfg, kern, mk, mv, mks, mvs, kc, vc, (int64_t)chunk.p0, cl, q_rot, a, part, counters,
                             err, batch, n_kv, capacity, ring_capacity, full ? 1 : 0, window, scale_log2,
                             static_cast<const unsigned char*>(l2_pf), (int64_t)l2_pf_bytes,
-                            kLateTrigger,
+                            chunk.p0 < 0 && batch <= kEarlyTriggerBatch ? 0 : 1,
                             chunk.p0 < 0 ? layer_trace(1) : (uint64_t*)nullptr, args);
 }
 

@@ -89,6 +89,35 @@ __device__ __forceinline__ void load8<float>(const unsigned char* half, int t, i
   v[3] = make_float2(b.z, b.w);
 }
 
+// The token's own cache row of one KV head (K and V, written by the kernel
+// before attention) as one warp holds it: lane l the 16-byte chunks
+// [kU l, kU l + kU) of each.  A tile that holds this row is loaded before the
+// dependency wait, so its copy of the row may be stale; the warp that folds
+// the tile reads the row after the wait and writes it over tile row t.
+template <typename CT>
+struct NewRow {
+  static constexpr int kU = sizeof(CT) / 2;  // chunks per lane: 1 (bf16), 2 (fp32)
+  uint4 k[kU], v[kU];
+  __device__ __forceinline__ void load(const CT* krow, const CT* vrow, int lane) {
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      k[u] = __ldcg(reinterpret_cast<const uint4*>(krow) + kU * lane + u);
+      v[u] = __ldcg(reinterpret_cast<const uint4*>(vrow) + kU * lane + u);
+    }
+  }
+  // chunk c of a row sits in 128-byte box c / 8 at chunk (c % 8) ^ (t % 8)
+  // of the row's line (the TMA 128-byte swizzle)
+  __device__ __forceinline__ void store(unsigned char* khalf, unsigned char* vhalf, int t, int lane) const {
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int c = kU * lane + u;
+      const int off = (c >> 3) * kSubBytes + t * kLine + (((c & 7) ^ (t & 7)) << 4);
+      *reinterpret_cast<uint4*>(khalf + off) = k[u];
+      *reinterpret_cast<uint4*>(vhalf + off) = v[u];
+    }
+  }
+};
+
 // One warp's running softmax state for the 4 query heads of a KV head: max
 // and sum per head (base 2), and the unnormalised output, lane l holding dims
 // [8 l, 8 l + 8) of each head.

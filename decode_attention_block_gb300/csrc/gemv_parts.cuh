@@ -70,22 +70,33 @@ __device__ __forceinline__ float4 load_w4(const __nv_bfloat16* w, int n) {
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// The RMSNorm weight elements a thread of build_x_norm uses: they do not
+// depend on the previous kernel, so a kernel may load them before its
+// dependency wait.
+template <typename WT, int NT, int MAXPER>
+__device__ __forceinline__ void load_norm_w(const WT* w, int n, float4 (&wv)[MAXPER], int t) {
+#pragma unroll
+  for (int k = 0; k < MAXPER; ++k) {
+    const int n4 = 4 * (t + k * NT);
+    wv[k] = n4 < n ? load_w4(w, n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 // The activation prologue of the q_k_v_proj GEMV for up to NB sequences:
 // xs_b = h_b * w (the RMSNorm's weight; the 1/rms scale is applied to the dot
 // products), permuted for row_dot with E-element chunks, and ss[b] = sum h_b^2
 // over this thread's elements.  NT threads take float4 groups t, t + NT, ...;
 // each thread issues every load before it computes, so the prologue costs one
 // memory round trip.  h comes from another CTA or kernel: loads bypass L1.
-template <int E, typename WT, int NB, int NT, int MAXPER>
-__device__ __forceinline__ void build_x_norm(const float* h, const WT* w, int n, int nb, float* xs,
-                                             int xfloats, float (&ss)[NB], int t) {
+// wv holds the thread's norm weights (load_norm_w).
+template <int E, int NB, int NT, int MAXPER>
+__device__ __forceinline__ void build_x_norm_w(const float* h, const float4 (&wv)[MAXPER], int n, int nb,
+                                               float* xs, int xfloats, float (&ss)[NB], int t) {
   float4 hv[NB][MAXPER];
-  float4 wv[MAXPER];
 #pragma unroll
   for (int k = 0; k < MAXPER; ++k) {
     const int n4 = 4 * (t + k * NT);
     if (n4 < n) {
-      wv[k] = load_w4(w, n4);
 #pragma unroll
       for (int b = 0; b < NB; ++b)
         hv[b][k] = b < nb ? __ldcg(reinterpret_cast<const float4*>(h + (int64_t)b * n + n4))
@@ -108,6 +119,14 @@ __device__ __forceinline__ void build_x_norm(const float* h, const WT* w, int n,
       }
     }
   }
+}
+
+template <int E, typename WT, int NB, int NT, int MAXPER>
+__device__ __forceinline__ void build_x_norm(const float* h, const WT* w, int n, int nb, float* xs,
+                                             int xfloats, float (&ss)[NB], int t) {
+  float4 wv[MAXPER];
+  load_norm_w<WT, NT, MAXPER>(w, n, wv, t);
+  build_x_norm_w<E, NB, NT, MAXPER>(h, wv, n, nb, xs, xfloats, ss, t);
 }
 
 // The activation prologue of o_proj: xs_b = a_b * sigmoid(g_b[head]) (the

@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = warp; k < hi && k < cnt; k += nw)
         if (k >= lo) issue(k);
   };
+  // the norm weights first: after the wait only h is still to come
+  float4 wv[kMaxPer];
+  load_norm_w<WT, kThreads, kMaxPer>(norm_w, hidden, wv, threadIdx.x);
   issue_range(0, kQkvPre < stages ? kQkvPre : stages);
   pdl_wait();
   pdl_trigger();  // the next kernel starts only once the one before this has completed
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // activations: x = h * w (unscaled) and sum(h^2) per sequence
   float ss[NB];
-  build_x_norm<E, WT, NB, kThreads, kMaxPer>(h, norm_w, hidden, nb, xs, xfloats, ss, threadIdx.x);
+  build_x_norm_w<E, NB, kThreads, kMaxPer>(h, wv, hidden, nb, xs, xfloats, ss, threadIdx.x);
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const float v = warp_sum(ss[b]);
