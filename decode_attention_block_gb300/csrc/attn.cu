@@ -234,10 +234,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
 
   // ------------------------------------------------------------ producer
   if (warp == NC) {
-   if (lane != 0) {
-      pdl_wait();
-      if (trig == 0) pdl_trigger();
-   } else {
+   if (lane == 0) {
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     if (chunk_p0 >= 0) {
@@ -289,6 +286,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
           }
         }
         ++k;
+        if (cl > 0 && k == (uint32_t)NS) cta_stamp(trace, 6);  // timeline: a ring's worth of tiles requested
         r = e;
       }
       sh.f = gs + r1;
@@ -299,6 +297,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       if (trig == 0) pdl_trigger();
     }
    }
+    // The other lanes wait only once lane 0 has issued its tiles: had they
+    // waited in a divergent branch of their own, that branch could run first
+    // and hold lane 0's requests until the previous kernel completed.
+    __syncwarp();
+    if (lane != 0) {
+      pdl_wait();
+      if (trig == 0) pdl_trigger();
+    }
     __syncwarp();
     if (cl == 0) return;
   } else {
@@ -368,6 +374,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
             atomicOr(err, kErrWaitTimeout);
           }
         } else {
+          // timeline (cluster mode): consumer warp 0's first tile in
+          const bool stamp = cl > 0 && warp == 0 && lane == 0 && u == 0;
+          if (stamp) cta_stamp(trace, 7);
           unsigned char* kst = stages + s * S::kStage;
           const bool patch = own_row && e == rows;
           if (patch) {

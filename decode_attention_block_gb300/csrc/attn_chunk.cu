@@ -153,11 +153,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
         pdl_wait();
         pdl_trigger();
       }
-    } else {
+    }
+    __syncwarp();  // the other lanes wait only once lane 0 has issued its tiles
+    if (lane != 0) {
       pdl_wait();
       pdl_trigger();
     }
-    __syncwarp();
     return;
   }
 

@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the weight stream does not depend on the previous kernel
   if (lane == 0 && warp < nw)
     for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
+  __syncwarp();  // every lane waits only once its warp's requests are out
   pdl_wait();
   pdl_trigger();  // the next kernel starts only once the one before this has completed
 

@@ -771,11 +771,12 @@ k_proj_mma(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         for (int i = issued > p.stages ? issued - p.stages : 0; i < issued; ++i)
           mbar_wait_bounded(&full_bar[i % p.stages], (i / p.stages) & 1, &no_abort, kWaitLimitNs);
       }
-    } else {
+    }
+    __syncwarp();  // the other lanes wait only once lane 0 has issued its requests
+    if (lane != 0) {
       pdl_wait();
       pdl_trigger();
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ---- MMA issuer: 4 MMAs of K = 16 per stage, then free the stage
     pdl_wait();

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float4 wv[kMaxPer];
   load_norm_w<WT, kThreads, kMaxPer>(norm_w, hidden, wv, threadIdx.x);
   issue_range(0, kQkvPre < stages ? kQkvPre : stages);
+  __syncwarp();  // every lane waits only once its warp's requests are out
   pdl_wait();
   pdl_trigger();  // the next kernel starts only once the one before this has completed
   if (threadIdx.x == 0) cta_stamp(trace, 1);
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (lane == 0 && warp < nw)
     for (int k = warp; k < stages && k < cnt; k += nw) issue(k);
+  __syncwarp();  // every lane waits only once its warp's requests are out
   pdl_wait();
   pdl_trigger();  // the next kernel starts only once the one before this has completed
   if (threadIdx.x == 0) cta_stamp(trace, 1);
