@@ -279,11 +279,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
           const CUtensorMap* mv = staged ? &tm_vs : &tm_v;
           const int z = staged ? (int)(w.kv_start + r - chunk_p0)
                                : (int)((int64_t)(chunk_p0 >= 0 ? 0 : sh.b) * capacity + slot);
-#pragma unroll
-          for (int q = 0; q < S::kSubs; ++q) {
-            tma_load_3d(kd + q * kSubBytes, mk, &full_bar[s], q * CacheT<CT>::kLineElems, sh.j, z);
-            tma_load_3d(vd + q * kSubBytes, mv, &full_bar[s], q * CacheT<CT>::kLineElems, sh.j, z);
-          }
+          tma_load_4d(kd, mk, &full_bar[s], 0, z, 0, sh.j);
+          tma_load_4d(vd, mv, &full_bar[s], 0, z, 0, sh.j);
         }
         ++k;
         if (cl > 0 && k == (uint32_t)NS) cta_stamp(trace, 6);  // timeline: a ring's worth of tiles requested
@@ -463,20 +460,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// [rows = batch * capacity][n_kv][256] cache viewed as a 3-D tensor; boxes of
-// kTile rows x one KV head x 128 bytes, 128-byte swizzle.
 template <typename CT>
 bool make_cache_map(CUtensorMap* map, const void* base, int n_kv, int64_t rows) {
-  EncodeTiledFn enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t es = sizeof(CT);
-  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_kv, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {kHeadDim * es, (cuuint64_t)n_kv * kHeadDim * es};
-  const cuuint32_t box[3] = {(cuuint32_t)CacheT<CT>::kLineElems, 1, (cuuint32_t)kTile};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CacheT<CT>::kTma, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_kv_tile_map(map, base, std::is_same<CT, __nv_bfloat16>::value, n_kv, rows);
 }
 
 // The grid of a launch: `total` rows x KV heads, the longest group
@@ -598,6 +584,21 @@ cudaError_t launch_ct(const float* q_rot, const void* kc, const void* vc, int n_
 }
 
 }  // namespace
+
+bool make_kv_tile_map(CUtensorMap* map, const void* base, bool bf16, int n_kv, int64_t rows) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t es = bf16 ? 2 : 4;
+  const cuuint64_t line = kLine / es;  // elements of a 128-byte line
+  const cuuint64_t dims[4] = {line, (cuuint64_t)rows, kHeadDim / line, (cuuint64_t)n_kv};
+  const cuuint64_t strides[3] = {(cuuint64_t)n_kv * kHeadDim * es, (cuuint64_t)kLine, kHeadDim * es};
+  const cuuint32_t box[4] = {(cuuint32_t)line, (cuuint32_t)kTile, (cuuint32_t)(kHeadDim / line), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, const void* vc,
                              int n_kv, int64_t capacity, int ring_capacity, bool full,

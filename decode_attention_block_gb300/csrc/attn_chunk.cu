@@ -141,11 +141,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
           const int z = staged ? (int)(sp.lo + r - p0) : (int)slot;
           const CUtensorMap* mk = staged ? &tm_ks : &tm_k;
           const CUtensorMap* mv = staged ? &tm_vs : &tm_v;
-#pragma unroll
-          for (int q = 0; q < kHeadDim / 64; ++q) {
-            tma_load_3d(kd + q * kSubBytes, mk, &full_bar[s], q * 64, j, z);
-            tma_load_3d(vd + q * kSubBytes, mv, &full_bar[s], q * 64, j, z);
-          }
+          tma_load_4d(kd, mk, &full_bar[s], 0, z, 0, j);
+          tma_load_4d(vd, mv, &full_bar[s], 0, z, 0, j);
         }
         r = e;
       }
@@ -251,15 +248,7 @@ cudaError_t launch_nc(const CUtensorMap& mk, const CUtensorMap& mv, const CUtens
 
 // the cache's [rows][n_kv][256] bf16 view for TMA, as the decode kernel's
 bool chunk_cache_map(CUtensorMap* map, const void* base, int n_kv, int64_t rows) {
-  EncodeTiledFn enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_kv, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {kHeadDim * 2, (cuuint64_t)n_kv * kHeadDim * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_kv_tile_map(map, base, true, n_kv, rows);
 }
 
 }  // namespace

@@ -103,6 +103,15 @@ uint64_t* layer_trace(int kind);
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// A KV cache [rows][n_kv][256] (bf16 or fp32) as the attention kernels load
+// it: one TMA box per K or V half of a 16-row tile of one KV head, landing in
+// shared memory as 128-byte lines [line of the row][row][128 bytes] with the
+// 128-byte swizzle.  The view is 4-D {elements of a line, rows, lines of a
+// row, heads} with strides {row, 128 bytes, head}: one request replaces one
+// per 128-byte line (a request costs the SM's TMA unit ~30 ns to issue, so a
+// 16 KB tile took ~0.25 us to request as eight).
+bool make_kv_tile_map(CUtensorMap* map, const void* base, bool bf16, int n_kv, int64_t rows);
+
 // cuTensorMapEncodeTiled from the driver (null if the driver has none).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

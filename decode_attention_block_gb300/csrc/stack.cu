@@ -349,11 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r < w.len_a && e > w.len_a) e = w.len_a;
             const int64_t slot = r < w.len_a ? w.first_slot + r : r - w.len_a;
             const int z = (int)((int64_t)b * L.capacity + slot);
-#pragma unroll
-            for (int s4 = 0; s4 < kHeadDim / 64; ++s4) {
-              tma_prefetch_l2_3d(&args.tm[l][0], s4 * 64, j, z);
-              tma_prefetch_l2_3d(&args.tm[l][1], s4 * 64, j, z);
-            }
+            tma_prefetch_l2_4d(&args.tm[l][0], 0, z, 0, j);  // the caches' 4-D tile view (make_kv_tile_map)
+            tma_prefetch_l2_4d(&args.tm[l][1], 0, z, 0, j);
             r = e;
           }
           f = gs + r1;
@@ -384,11 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char* vd = kd + kv_half_bytes<__nv_bfloat16>();
             mbar_arrive_expect_tx(bar, 2 * kv_half_bytes<__nv_bfloat16>());
             const int z = (int)((int64_t)b * L.capacity + slot);
-#pragma unroll
-            for (int s4 = 0; s4 < kHeadDim / 64; ++s4) {
-              tma_load_3d(kd + s4 * kSubBytes, &args.tm[l][0], bar, s4 * 64, j, z);
-              tma_load_3d(vd + s4 * kSubBytes, &args.tm[l][1], bar, s4 * 64, j, z);
-            }
+            tma_load_4d(kd, &args.tm[l][0], bar, 0, z, 0, j);
+            tma_load_4d(vd, &args.tm[l][1], bar, 0, z, 0, j);
             ring_publish(ring, i);
             r = e;
           }
@@ -642,15 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 bool make_bf16_cache_map(CUtensorMap* map, const void* base, int n_kv, int64_t rows) {
-  EncodeTiledFn enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_kv, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {kHeadDim * 2, (cuuint64_t)n_kv * kHeadDim * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_kv_tile_map(map, base, true, n_kv, rows);
 }
 
 int xfloats_of(int cols) { return ((cols / 8 + 31) / 32) * 32 * 8; }
