@@ -254,6 +254,9 @@ __device__ __forceinline__ void chunk_rows(__nv_bfloat16* x, int bb, int bpad, i
 // cs[b][i] = (cos, sin) of pos_b * theta^(-2i/r), the angle formed and
 // reduced modulo 2 pi in double (at position 131072 an fp32 angle would be
 // off by ~1e-2 rad), then evaluated in fp32.
+// float4 groups of an activation row per prologue thread (rows of up to 8192)
+constexpr int kPrepPer = 8192 / 4 / kPrepThreads;
+
 __global__ void __launch_bounds__(kPrepThreads)
 k_prep_norm(const float* __restrict__ h, const __nv_bfloat16* __restrict__ norm_w,
             __nv_bfloat16* __restrict__ x, float2* __restrict__ cs, int hidden, int nb, int bpad,
@@ -262,6 +265,13 @@ k_prep_norm(const float* __restrict__ h, const __nv_bfloat16* __restrict__ norm_
   const int b = blockIdx.x;
   __nv_bfloat16 *xh, *xl;
   chunk_rows(x, b, bpad, hidden, xh, xl);
+  // the norm weights do not depend on the previous kernel
+  uint2 wr[kPrepPer];
+#pragma unroll
+  for (int k = 0; k < kPrepPer; ++k) {
+    const int i = 4 * (threadIdx.x + k * kPrepThreads);
+    if (i < hidden) wr[k] = __ldg(reinterpret_cast<const uint2*>(norm_w + i));
+  }
   pdl_wait();
   pdl_trigger();
   if (b >= nb) {
@@ -271,34 +281,48 @@ k_prep_norm(const float* __restrict__ h, const __nv_bfloat16* __restrict__ norm_
     }
     return;
   }
+  // every load of h before any arithmetic: one round trip
+  const float* hb = h + (size_t)b * hidden;
+  float4 v[kPrepPer];
+#pragma unroll
+  for (int k = 0; k < kPrepPer; ++k) {
+    const int i = 4 * (threadIdx.x + k * kPrepThreads);
+    v[k] = i < hidden ? __ldcg(reinterpret_cast<const float4*>(hb + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (threadIdx.x < rotary_dim / 2) {
+    // the angle's whole turns: rint(ang / 2 pi), with the quotient formed as
+    // a product (a correctly rounded division is a long fp64 sequence here);
+    // the nearest integer is all that is needed, the reduction itself is the
+    // fp64 fma below
     const int i = threadIdx.x;
     const double ang = (double)args.pos[b] * args.inv_freq[i];
     const double two_pi = 6.283185307179586476925;
-    const double k = rint(ang / two_pi);
+    const double k = rint(ang * (1.0 / two_pi));
     const float r = (float)fma(-k, two_pi, ang);
-    float s, c;
-    sincosf(r, &s, &c);
-    cs[(size_t)b * kMaxPairs + i] = make_float2(c, s);
+    float sn, cn;
+    sincosf(r, &sn, &cn);
+    cs[(size_t)b * kMaxPairs + i] = make_float2(cn, sn);
   }
-  const float* hb = h + (size_t)b * hidden;
   float ss = 0.f;
-  for (int i = 4 * threadIdx.x; i < hidden; i += 4 * kPrepThreads) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(hb + i));
-    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-  }
+#pragma unroll
+  for (int k = 0; k < kPrepPer; ++k)
+    ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, fmaf(v[k].w, v[k].w, ss))));
   const float inv = 1.0f / sqrtf(block_sum(ss, red) / (float)hidden + eps);
-  for (int i = 4 * threadIdx.x; i < hidden; i += 4 * kPrepThreads) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(hb + i));
-    const uint2 wr = __ldg(reinterpret_cast<const uint2*>(norm_w + i));
-    const float2 w01 = bf16x2_to_f32x2(wr.x), w23 = bf16x2_to_f32x2(wr.y);
-    store_split4(xh, xl, i,
-                 make_float4(v.x * w01.x * inv, v.y * w01.y * inv, v.z * w23.x * inv, v.w * w23.y * inv));
+#pragma unroll
+  for (int k = 0; k < kPrepPer; ++k) {
+    const int i = 4 * (threadIdx.x + k * kPrepThreads);
+    if (i < hidden) {
+      const float2 w01 = bf16x2_to_f32x2(wr[k].x), w23 = bf16x2_to_f32x2(wr[k].y);
+      store_split4(xh, xl, i,
+                   make_float4(v[k].x * w01.x * inv, v[k].y * w01.y * inv, v[k].z * w23.x * inv,
+                               v[k].w * w23.y * inv));
+    }
   }
 }
 
 // One CTA per (padded) sequence: the gated attention output a_b * sigmoid(g_b)
 // (one gate per query head, broadcast over head_dim) split into hi / lo rows.
+// Every load is issued before any arithmetic (one round trip).
 __global__ void __launch_bounds__(kPrepThreads)
 k_prep_gate(const float* __restrict__ a, const float* __restrict__ g, __nv_bfloat16* __restrict__ x,
             int q_dim, int n_q, int nb, int bpad) {
@@ -315,10 +339,23 @@ k_prep_gate(const float* __restrict__ a, const float* __restrict__ g, __nv_bfloa
     return;
   }
   const float* ab = a + (size_t)b * q_dim;
-  for (int i = 4 * threadIdx.x; i < q_dim; i += 4 * kPrepThreads) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(ab + i));
-    const float s = 1.0f / (1.0f + expf(-__ldcg(g + (size_t)b * n_q + i / kHeadDim)));
-    store_split4(xh, xl, i, make_float4(v.x * s, v.y * s, v.z * s, v.w * s));
+  float4 v[kPrepPer];
+  float gv[kPrepPer];
+#pragma unroll
+  for (int k = 0; k < kPrepPer; ++k) {
+    const int i = 4 * (threadIdx.x + k * kPrepThreads);
+    if (i < q_dim) {
+      v[k] = __ldcg(reinterpret_cast<const float4*>(ab + i));
+      gv[k] = __ldcg(g + (size_t)b * n_q + i / kHeadDim);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPrepPer; ++k) {
+    const int i = 4 * (threadIdx.x + k * kPrepThreads);
+    if (i < q_dim) {
+      const float sg = 1.0f / (1.0f + expf(-gv[k]));
+      store_split4(xh, xl, i, make_float4(v[k].x * sg, v[k].y * sg, v[k].z * sg, v[k].w * sg));
+    }
   }
 }
 
