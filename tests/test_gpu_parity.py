@@ -233,6 +233,11 @@ ATTN_CASES = [
     ("split64_ragged", True, 0, None, [5, 700, 3000, 17, 1], 64, "bf16"),
     ("split1000_ragged", True, 0, None, [5, 700, 3000, 17, 1], 1000, "bf16"),
     ("big_batch_bucket", False, 512, 512, list(range(0, 2000, 10)), 0, "bf16"),
+    # long equal histories at small batch
+    ("split_clusters_b1", True, 0, None, [8192], 0, "bf16"),
+    ("split_clusters_b2", True, 0, None, [5000, 5000], 0, "bf16"),
+    ("split_clusters_b4", True, 0, None, [2000] * 4, 0, "bf16"),
+    ("split_clusters_f32", True, 0, None, [4000], 0, "f32"),
 ]
 
 
@@ -299,6 +304,30 @@ def test_attention_split_count_invariance_and_reuse(B):
         assert ma < 1e-5
     ws_host = ws.cpu()
     assert int(ws_host[256:256 + 4 * 3 * 4].view(torch.int32).abs().sum()) == 0   # tickets back at 0
+
+
+def test_equal_long_histories_reuse_and_split_invariance(B):
+    """Equal long histories at batch 2: the default grid gives the result of an
+    explicit 152-CTA split, call after call on one workspace, with the merge
+    tickets back at 0."""
+    positions = [6000, 6000]
+    wl = synth.Workload("t", "", "bf16", positions, [synth.LayerSpec(True)], seed=412)
+    kc, vc = synth.make_cache(wl, 0, "cuda")
+    q = torch.randn((2, Q_DIM), generator=_gen(413), device="cuda")
+    geom = B.spark_geom_default()
+    ws = B.make_workspace(geom, 2)
+    results = []
+    for n in (0, 0, 152, 0):
+        a = torch.empty((2, Q_DIM), device="cuda")
+        B.spark_dbg_attention(geom, q, B.KvLayer(kc, vc, 0), B.SPARK_FULL, positions, a, ws, n_ctas=n)
+        results.append(a.cpu().numpy())
+    assert B.spark_attn_error_word(ws) == 0
+    for r in results[1:]:
+        ma, _ = err_stats(r, results[0])
+        assert ma < 1e-5
+    assert np.array_equal(results[0], results[1]) and np.array_equal(results[0], results[3])
+    ws_host = ws.cpu()
+    assert int(ws_host[256:256 + 4 * 2 * 4].view(torch.int32).abs().sum()) == 0   # tickets back at 0
 
 
 # ---------------------------------------------------------------------------
