@@ -472,7 +472,7 @@ struct AttnPlan {
   int cluster;  // CTAs per cluster (cluster mode), 0 otherwise
 };
 template <int MINB>
-AttnPlan plan_attention(int64_t total, int64_t max_rows, int groups, int n_ctas, int max_ctas) {
+AttnPlan plan_attention(int64_t total, int64_t max_rows, int64_t min_rows, int groups, int n_ctas, int max_ctas) {
   // Short histories in small launches: one cluster of cl CTAs per group,
   // merging through DSMEM (no partials in the workspace, no ticket).
   int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
@@ -485,6 +485,11 @@ AttnPlan plan_attention(int64_t total, int64_t max_rows, int groups, int n_ctas,
     const int64_t want = (total + kMinRowsPerCta - 1) / kMinRowsPerCta;
     const int cap = MINB * device_sm_count();
     G = (int)(want < cap ? want : cap);
+    // Groups of equal length that nearly fill the GPU (the sliding layer of
+    // a large batch): one CTA per group, no partials and no merge tail (64
+    // sequences of 512 rows: 34.8 -> 30.7 us per launch, the default
+    // 64-sequence step 725.6 -> 720.3 us)
+    if (max_rows == min_rows && groups <= cap && 4 * groups >= 3 * cap && groups <= max_ctas) G = groups;
   }
   if (G < 1) G = 1;
   if (G > kMaxAttnCtas) G = kMaxAttnCtas;
@@ -507,9 +512,12 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
     args.pos[b] = b < batch ? positions[b] : 0;
   }
   const int64_t total = (int64_t)n_kv * args.prefix[batch];
-  int64_t max_rows = 0;
-  for (int b = 0; b < batch; ++b) max_rows = std::max(max_rows, args.prefix[b + 1] - args.prefix[b]);
-  const AttnPlan plan = plan_attention<MINB>(total, max_rows, batch * n_kv, n_ctas, max_ctas);
+  int64_t max_rows = 0, min_rows = INT64_MAX;
+  for (int b = 0; b < batch; ++b) {
+    max_rows = std::max(max_rows, args.prefix[b + 1] - args.prefix[b]);
+    min_rows = std::min(min_rows, args.prefix[b + 1] - args.prefix[b]);
+  }
+  const AttnPlan plan = plan_attention<MINB>(total, max_rows, min_rows, batch * n_kv, n_ctas, max_ctas);
   const int G = plan.ctas, cl = plan.cluster;
 
   // a chunk's tokens share one sequence's cache; decode rows are per sequence

@@ -238,6 +238,9 @@ ATTN_CASES = [
     ("split_clusters_b2", True, 0, None, [5000, 5000], 0, "bf16"),
     ("split_clusters_b4", True, 0, None, [2000] * 4, 0, "bf16"),
     ("split_clusters_f32", True, 0, None, [4000], 0, "f32"),
+    # equal groups that nearly fill the GPU: one CTA per (sequence, KV head), no merge
+    ("whole_groups_b64_ring", False, 512, 512, [700] * 64, 0, "bf16"),
+    ("whole_groups_b30_full", True, 0, None, [299] * 30, 0, "bf16"),
 ]
 
 
