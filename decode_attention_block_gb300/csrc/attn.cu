@@ -486,10 +486,12 @@ AttnPlan plan_attention(int64_t total, int64_t max_rows, int64_t min_rows, int g
     const int cap = MINB * device_sm_count();
     G = (int)(want < cap ? want : cap);
     // Groups of equal length that nearly fill the GPU (the sliding layer of
-    // a large batch): one CTA per group, no partials and no merge tail (64
-    // sequences of 512 rows: 34.8 -> 30.7 us per launch, the default
-    // 64-sequence step 725.6 -> 720.3 us)
-    if (max_rows == min_rows && groups <= cap && 4 * groups >= 3 * cap && groups <= max_ctas) G = groups;
+    // a large batch), or so short that the default grid has fewer CTAs than
+    // groups: one CTA per group, no partials and no merge tail (64 sequences
+    // of 512 rows: 34.8 -> 30.7 us per launch, the default 64-sequence step
+    // 725.6 -> 720.3 us)
+    if (max_rows == min_rows && groups <= cap && (4 * groups >= 3 * cap || want <= groups) && groups <= max_ctas)
+      G = groups;
   }
   if (G < 1) G = 1;
   if (G > kMaxAttnCtas) G = kMaxAttnCtas;
