@@ -45,9 +45,16 @@ constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from
 // 512-row sliding layers now take 8 CTAs instead of 6); clusters of up to
 // 16 CTAs (non-portable size) were no faster.
 constexpr int kMaxCluster = 8;
+// Long histories at small batch (more than kClusterMaxRows rows, few
+// groups): one cluster of kLongCluster CTAs per group (a non-portable
+// cluster size) when the clusters all fit at once.  The 8192-row full layers
+// of the 36-layer batch-1 step: 16 CTAs per KV head merging through DSMEM
+// instead of 38 with a ticket merge, 828.3 -> 821.7 us per step (the 64
+// CTAs stream the rows more slowly, 2.8 TB/s, but the merge tail shrinks).
+constexpr int kLongCluster = 16;
 constexpr int kStateBytes = (8 + kGroup * kHeadDim) * 4;  // a CTA's state: m[4], l[4], o[4][256]
 template <int MINB>
-constexpr int kRecvSlots = MINB == 1 ? kMaxCluster - 1 : 0;  // cluster mode only with one CTA per SM
+constexpr int kRecvSlots = MINB == 1 ? kLongCluster - 1 : 0;  // cluster mode only with one CTA per SM
 // When the next kernel may launch: 0 = right after the dependency wait, 1 =
 // once this CTA's tiles are all in and its states merged or published.  Since
 // every decode tile is requested before the wait (the token's own row comes
@@ -472,7 +479,8 @@ struct AttnPlan {
   int cluster;  // CTAs per cluster (cluster mode), 0 otherwise
 };
 template <int MINB>
-AttnPlan plan_attention(int64_t total, int64_t max_rows, int64_t min_rows, int groups, int n_ctas, int max_ctas) {
+AttnPlan plan_attention(int64_t total, int64_t max_rows, int64_t min_rows, int groups, int n_ctas, int max_ctas,
+                        int long_clusters) {
   // Short histories in small launches: one cluster of cl CTAs per group,
   // merging through DSMEM (no partials in the workspace, no ticket).
   int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
@@ -480,6 +488,10 @@ AttnPlan plan_attention(int64_t total, int64_t max_rows, int64_t min_rows, int g
   if (n_ctas > 0 || cl < 2 || max_rows > kClusterMaxRows ||
       (int64_t)groups * cl > device_sm_count() || (int64_t)groups * cl > max_ctas || MINB > 1)
     cl = 0;  // cluster mode only in the kernel of one CTA per SM (it holds the ranks' state slots)
+  // longer histories at small batch: clusters of kLongCluster, if they all fit
+  if (cl == 0 && n_ctas <= 0 && MINB == 1 && max_rows > kClusterMaxRows && groups <= long_clusters &&
+      (int64_t)groups * kLongCluster <= max_ctas)
+    cl = kLongCluster;
   int G = cl > 0 ? groups * cl : n_ctas;
   if (cl == 0 && G <= 0) {
     const int64_t want = (total + kMinRowsPerCta - 1) / kMinRowsPerCta;
@@ -519,7 +531,36 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
     max_rows = std::max(max_rows, args.prefix[b + 1] - args.prefix[b]);
     min_rows = std::min(min_rows, args.prefix[b + 1] - args.prefix[b]);
   }
-  const AttnPlan plan = plan_attention<MINB>(total, max_rows, min_rows, batch * n_kv, n_ctas, max_ctas);
+  auto kern = k_attn_decode<CT, NS, NC, MINB, MAXB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
+  if (e != cudaSuccess) return e;
+  // clusters of kLongCluster CTAs that fit at once, per device (0: none)
+  static int long_clusters[64];
+  static bool long_known[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (MINB == 1 && dev >= 0 && dev < 64 && !long_known[dev]) {
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(kLongCluster * 8);
+      qc.blockDim = dim3((NC + 1) * 32);
+      qc.dynamicSmemBytes = S::kAlloc;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = kLongCluster;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();  // a refused query or attribute leaves no sticky error
+    long_clusters[dev] = n;
+    long_known[dev] = true;
+  }
+  const int long_cl = MINB == 1 && dev >= 0 && dev < 64 ? long_clusters[dev] : 0;
+  const AttnPlan plan = plan_attention<MINB>(total, max_rows, min_rows, batch * n_kv, n_ctas, max_ctas, long_cl);
   const int G = plan.ctas, cl = plan.cluster;
 
   // a chunk's tokens share one sequence's cache; decode rows are per sequence
@@ -534,9 +575,6 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
     mks = mk;
     mvs = mv;
   }
-  auto kern = k_attn_decode<CT, NS, NC, MINB, MAXB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-  if (e != cudaSuccess) return e;
   const float scale_log2 = scale * 1.4426950408889634f;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);

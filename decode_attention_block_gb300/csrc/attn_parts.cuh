@@ -724,35 +724,44 @@ __device__ __forceinline__ void attn_cluster_merge_local(const float* cst, const
                                                          float* a_head0, volatile int* flags) {
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kF = 8 + kGroup * kHeadDim;  // floats of a state
-  float mq[8], lq[8];
-  float4 x0[8], x1[8];
+  constexpr int kB = 8;                      // states per round (clusters of up to 16: two rounds)
+  float M = -INFINITY, L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int q0 = 0; q0 < cl; q0 += kB) {
+    float mq[kB], lq[kB];
+    float4 x0[kB], x1[kB];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    if (q < cl) {
-      const float* st = q == 0 ? cst : recv + (q - 1) * kF;
-      mq[q] = st[h];
-      lq[q] = st[4 + h];
-      const float4* src = reinterpret_cast<const float4*>(st + 8 + h * kHeadDim + 8 * lane);
-      x0[q] = src[0];
-      x1[q] = src[1];
-    } else {
-      mq[q] = -INFINITY;
-      lq[q] = 0.f;
-      x0[q] = x1[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = 0; t < kB; ++t) {
+      const int q = q0 + t;
+      if (q < cl) {
+        const float* st = q == 0 ? cst : recv + (q - 1) * kF;
+        mq[t] = st[h];
+        lq[t] = st[4 + h];
+        const float4* src = reinterpret_cast<const float4*>(st + 8 + h * kHeadDim + 8 * lane);
+        x0[t] = src[0];
+        x1[t] = src[1];
+      } else {
+        mq[t] = -INFINITY;
+        lq[t] = 0.f;
+        x0[t] = x1[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-  }
-  float M = -INFINITY;
+    float mb = M;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) M = fmaxf(M, mq[q]);
-  float L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int t = 0; t < kB; ++t) mb = fmaxf(mb, mq[t]);
+    const float rs = M == -INFINITY ? 0.f : exp2f(M - mb);  // rescale the rounds before
+    L *= rs;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float scl = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
-    L = fmaf(lq[q], scl, L);
-    O[0] = fmaf(x0[q].x, scl, O[0]); O[1] = fmaf(x0[q].y, scl, O[1]);
-    O[2] = fmaf(x0[q].z, scl, O[2]); O[3] = fmaf(x0[q].w, scl, O[3]);
-    O[4] = fmaf(x1[q].x, scl, O[4]); O[5] = fmaf(x1[q].y, scl, O[5]);
-    O[6] = fmaf(x1[q].z, scl, O[6]); O[7] = fmaf(x1[q].w, scl, O[7]);
+    for (int i = 0; i < 8; ++i) O[i] *= rs;
+    M = mb;
+#pragma unroll
+    for (int t = 0; t < kB; ++t) {
+      const float scl = mq[t] == -INFINITY ? 0.f : exp2f(mq[t] - M);
+      L = fmaf(lq[t], scl, L);
+      O[0] = fmaf(x0[t].x, scl, O[0]); O[1] = fmaf(x0[t].y, scl, O[1]);
+      O[2] = fmaf(x0[t].z, scl, O[2]); O[3] = fmaf(x0[t].w, scl, O[3]);
+      O[4] = fmaf(x1[t].x, scl, O[4]); O[5] = fmaf(x1[t].y, scl, O[5]);
+      O[6] = fmaf(x1[t].z, scl, O[6]); O[7] = fmaf(x1[t].w, scl, O[7]);
+    }
   }
   if (!flags[0]) {
     const float inv = 1.0f / L;
