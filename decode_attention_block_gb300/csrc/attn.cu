@@ -42,8 +42,8 @@ constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from
 // Cluster mode (short histories): up to 8 CTAs per group, about 64 rows
 // each, for groups of at most 1536 rows.  Measured against 96 rows per CTA:
 // default step 53.0 -> 52.7 us, 36-layer stack 0.944 -> 0.925 ms (its
-// 512-row sliding layers now take 8 CTAs instead of 6); clusters of up to
-// 16 CTAs (non-portable size) were no faster.
+// 512-row sliding layers now take 8 CTAs instead of 6); for these short
+// histories clusters of up to 16 CTAs (non-portable size) were no faster.
 constexpr int kMaxCluster = 8;
 // Long histories at small batch (more than kClusterMaxRows rows, few
 // groups): one cluster of kLongCluster CTAs per group (a non-portable
@@ -473,7 +473,10 @@ bool make_cache_map(CUtensorMap* map, const void* base, int n_kv, int64_t rows) 
 }
 
 // The grid of a launch: `total` rows x KV heads, the longest group
-// `max_rows`, `groups` = batch x KV heads.
+// `max_rows` and the shortest `min_rows`, `groups` = batch x KV heads,
+// `n_ctas` > 0 an explicit grid (stream-K split, no cluster), `max_ctas` the
+// partial slots available, `long_clusters` the clusters of kLongCluster CTAs
+// of this kernel that fit on the GPU at once.
 struct AttnPlan {
   int ctas;     // CTAs of the launch
   int cluster;  // CTAs per cluster (cluster mode), 0 otherwise
