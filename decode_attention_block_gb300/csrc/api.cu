@@ -122,10 +122,10 @@ cudaError_t run_qkv(int path, const spark_geom* g, const float* h, const spark_l
 
 cudaError_t run_oproj(int path, const spark_geom* g, const float* a, const float* g_logits,
                       const float* h, const spark_layer_weights* w, int32_t batch, float* out,
-                      uint32_t* err, void* ws, const WsLayout& L, cudaStream_t st) {
+                      uint32_t* err, void* ws, const WsLayout& L, cudaStream_t st, int free_sms = -1) {
   if (path == SPARK_PATH_MMA)
     return launch_oproj_mma(a, g_logits, h, w->o_w, out, err, g->hidden, g->n_q, batch, mma_ws(ws, L), st);
-  return launch_oproj(w->dtype, a, g_logits, h, w->o_w, out, err, g->hidden, g->n_q, batch, st);
+  return launch_oproj(w->dtype, a, g_logits, h, w->o_w, out, err, g->hidden, g->n_q, batch, st, free_sms);
 }
 
 }  // namespace
@@ -253,14 +253,16 @@ int spark_attn_decode(const spark_geom* g, const float* h, const spark_layer_wei
     g_layer_trace = ws_at<uint64_t>(workspace, L.trace) + (size_t)(calls++ & 1) * 3 * kTraceCtas * kTraceEvs;
   cudaError_t e = run_qkv(pick_path(SPARK_PATH_AUTO, w->dtype, g, rotary_dim, batch), g, h, w, kv,
                           rotary_dim, theta, positions, batch, q_rot, g_logits, err, workspace, L, st);
+  int held = 0;  // SMs attention's CTAs hold while o_proj's first CTAs start
   if (e == cudaSuccess)
     e = launch_attention(kv->dtype, q_rot, kv->k, kv->v, g->n_kv, kv->capacity,
                          kv->ring_capacity, layer_class == SPARK_FULL, g->window, g->scale,
                          positions, batch, a, ws_at<float>(workspace, L.part),
-                         ws_at<uint32_t>(workspace, L.counters), err, 0, nullptr, 0, st);
+                         ws_at<uint32_t>(workspace, L.counters), err, 0, nullptr, 0, st, ChunkSrc(),
+                         kMaxAttnCtas, &held);
   if (e == cudaSuccess)
     e = run_oproj(pick_path(SPARK_PATH_AUTO, w->dtype, g, 0, batch), g, a, g_logits, h, w, batch, out,
-                  err, workspace, L, st);
+                  err, workspace, L, st, held > 0 ? device_sm_count() - held : -1);
   g_layer_trace = nullptr;
   return cuda_status(e);
 }

@@ -53,8 +53,21 @@ constexpr int kMaxCluster = 8;
 // CTAs stream the rows more slowly, 2.8 TB/s, but the merge tail shrinks).
 constexpr int kLongCluster = 16;
 constexpr int kStateBytes = (8 + kGroup * kHeadDim) * 4;  // a CTA's state: m[4], l[4], o[4][256]
+// Cluster mode merges a group's state spread over the ranks: rank r owns the
+// units [merge_unit0(r), merge_unit0(r + 1)) of o (a unit: 8 floats, one
+// lane's dims of one head) and receives from every other rank q, in slot q
+// of its receive area, that rank's m[4], l[4] and its values of those units.
+constexpr int kMergeUnits = kGroup * kHeadDim / 8;
+__host__ __device__ constexpr int merge_unit0(int r, int cl) { return kMergeUnits * r / cl; }
+__host__ __device__ constexpr int merge_slot_floats(int cl) { return 8 + 8 * ((kMergeUnits + cl - 1) / cl); }
+constexpr int merge_recv_bytes_max() {
+  int most = 0;
+  for (int cl = 2; cl <= kLongCluster; ++cl)
+    if (cl * merge_slot_floats(cl) * 4 > most) most = cl * merge_slot_floats(cl) * 4;
+  return most;
+}
 template <int MINB>
-constexpr int kRecvSlots = MINB == 1 ? kLongCluster - 1 : 0;  // cluster mode only with one CTA per SM
+constexpr int kRecvBytes = MINB == 1 ? merge_recv_bytes_max() : 0;  // cluster mode only with one CTA per SM
 // When the next kernel may launch: 0 = right after the dependency wait, 1 =
 // once this CTA's tiles are all in and its states merged or published.  Since
 // every decode tile is requested before the wait (the token's own row comes
@@ -67,14 +80,12 @@ constexpr int kEarlyTriggerBatch = 4;
 constexpr int kClusterRowsPerCta = 64;
 constexpr int64_t kClusterMaxRows = 1536;
 
-// RECV: slots for the other ranks' states in cluster mode (0 in the
-// two-CTAs-per-SM kernel, which never runs in cluster mode: the slots would
-// keep its second CTA off the SM)
+// RECV: bytes of the receive area of the cluster merge (0 in the
+// two-CTAs-per-SM kernel, which never runs in cluster mode)
 template <typename CT, int NS, int NC, int RECV>
 struct Smem {
   static_assert(NS % NC == 0, "each stage must belong to one consumer warp");
   static constexpr int kStages = NS;
-  static constexpr int kSubs = kHeadDim / CacheT<CT>::kLineElems;
   static constexpr int kHalf = kv_half_bytes<CT>();  // the K (or V) half of a stage
   static constexpr int kStage = 2 * kHalf;
   static constexpr int kQ = kStages * kStage;
@@ -85,8 +96,8 @@ struct Smem {
   static constexpr int kBars = kO + NC * 4 * kHeadDim * 4;
   static constexpr int kCst = kBars + 2 * kStages * 8;       // cluster mode: the CTA's state
   static constexpr int kFlags = kCst + kStateBytes;
-  static constexpr int kRecv = kFlags + 16;                   // cluster rank 0: the other ranks' states
-  static constexpr int kMergeBar = kRecv + RECV * kStateBytes;
+  static constexpr int kRecv = kFlags + 16;                   // cluster mode: the other ranks' slices
+  static constexpr int kMergeBar = kRecv + RECV;
   static constexpr int kBytes = kMergeBar + 16;
   static_assert(kCst % 16 == 0 && kRecv % 16 == 0, "bulk copies of the states need 16-byte alignment");
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 (128B swizzle)
@@ -96,7 +107,7 @@ struct Smem {
 // 228 KB of shared memory (1 KB of it reserved per CTA).
 static_assert(CacheT<__nv_bfloat16>::kDeepBlocks *
                       (Smem<__nv_bfloat16, CacheT<__nv_bfloat16>::kDeep, kConsumers,
-                            kRecvSlots<CacheT<__nv_bfloat16>::kDeepBlocks>>::kAlloc + 1024) <=
+                            kRecvBytes<CacheT<__nv_bfloat16>::kDeepBlocks>>::kAlloc + 1024) <=
                   228 * 1024,
               "the two-CTAs-per-SM attention kernel no longer fits two CTAs on an SM");
 
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
                   int batch, int n_kv, int64_t capacity, int ring_capacity, int full,
                   int window, float scale_log2, const unsigned char* l2_pf, int64_t l2_pf_bytes,
                   int trig, uint64_t* trace, const __grid_constant__ AttnArgs<MAXB> args) {
-  using S = Smem<CT, NS, NC, kRecvSlots<MINB>>;
+  using S = Smem<CT, NS, NC, kRecvBytes<MINB>>;
   constexpr int kCT = NC * 32;  // consumer threads
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base =
@@ -185,11 +196,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    if (cl > 0 && blockIdx.x % cl == 0) {
-      // cluster rank 0 receives the other ranks' states: one phase, their bytes
+    if (cl > 0) {
+      // every rank receives the other ranks' m, l and its units: one phase
+      const int r = (int)(blockIdx.x % cl);
+      const int units = merge_unit0(r + 1, cl) - merge_unit0(r, cl);
       mbar_init(merge_bar, 1);
       fence_mbar_init();
-      mbar_arrive_expect_tx(merge_bar, (uint32_t)((cl - 1) * kStateBytes));
+      mbar_arrive_expect_tx(merge_bar, (uint32_t)((cl - 1) * 32 * (1 + units)));
     }
     flags[0] = 0;
     flags[1] = 0;
@@ -208,8 +221,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     }
   }
   __syncthreads();
-  // cluster mode: rank 0's merge barrier is ready once every rank has passed
-  // here (the matching wait comes before a rank sends its state)
+  // cluster mode: every rank's merge barrier is ready once every rank has
+  // passed here (the matching wait comes before a rank sends its state)
   if (cl > 0) cluster_arrive();
 
   // Programmatic dependent launch.  q_rot and the token's own cache row
@@ -422,32 +435,41 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   }  // consumers
 
   if (cl > 0) {
-    // Every rank but 0 stores its state into rank 0's shared memory with
-    // remote stores that complete on rank 0's merge barrier, and leaves; rank
-    // 0 merges the states in rank order and writes the group's output.
-    // (Rank 0 pulling the states through DSMEM took a cluster barrier before
-    // and after the reads.)
+    // The group's state is merged spread over the ranks.  Each rank sends,
+    // with remote stores that complete on the receiver's merge barrier, its
+    // m and l to every other rank and each unit of its o to the unit's owner;
+    // each rank then merges its own units over the ranks, in rank order, and
+    // writes them.  (Every state to rank 0, which merged them all: its 28 KB
+    // (8 ranks) to 60 KB (16) of incoming stores landed 1.0-1.7 us after the
+    // last was sent, and its merge took 1.6-2.0 us more.)
     __syncthreads();  // this CTA's state is complete
-    cluster_wait();   // rank 0's merge barrier is initialised
+    cluster_wait();   // every rank's merge barrier is initialised
     const int r = c % cl;
-    if (r != 0) {
-      if (warp < kGroup) {  // head `warp`: m, l and lane's 8 dims of o
-        const int h = warp;
-        const uint32_t dst = cluster_addr(base + S::kRecv + (r - 1) * kStateBytes, 0);
-        const uint32_t bar = cluster_addr(merge_bar, 0);
-        const float4* src = reinterpret_cast<const float4*>(cst + 8 + h * kHeadDim + 8 * lane);
-        const uint32_t o = dst + (uint32_t)(8 + h * kHeadDim + 8 * lane) * 4;
-        st_async_f32x4(o, src[0], bar);
-        st_async_f32x4(o + 16, src[1], bar);
-        if (lane == 0) {
-          st_async_f32(dst + (uint32_t)h * 4, cst[h], bar);
-          st_async_f32(dst + (uint32_t)(4 + h) * 4, cst[4 + h], bar);
-        }
+    const int sf = merge_slot_floats(cl);
+    if (tid < kMergeUnits) {  // consumer thread u sends unit u (and m, l to rank u)
+      const int u = tid;
+      int q = u * cl / kMergeUnits;  // the unit's owner
+      while (q + 1 < cl && merge_unit0(q + 1, cl) <= u) ++q;
+      while (merge_unit0(q, cl) > u) --q;
+      if (q != r) {
+        const uint32_t bar = cluster_addr(merge_bar, (uint32_t)q);
+        const uint32_t dst = cluster_addr(base + S::kRecv + (r * sf + 8 + 8 * (u - merge_unit0(q, cl))) * 4, (uint32_t)q);
+        const float4* src = reinterpret_cast<const float4*>(cst + 8 + 8 * u);
+        st_async_f32x4(dst, src[0], bar);
+        st_async_f32x4(dst + 16, src[1], bar);
       }
-    } else if (warp < kGroup) {
-      const int g = c / cl, b = g / n_kv, j = g % n_kv;
+      if (u < cl && u != r) {
+        const uint32_t bar = cluster_addr(merge_bar, (uint32_t)u);
+        const uint32_t dst = cluster_addr(base + S::kRecv + r * sf * 4, (uint32_t)u);
+        const float4* src = reinterpret_cast<const float4*>(cst);
+        st_async_f32x4(dst, src[0], bar);
+        st_async_f32x4(dst + 16, src[1], bar);
+      }
+    }
+    const int u0 = merge_unit0(r, cl), nu = merge_unit0(r + 1, cl) - u0;
+    if (tid < kCT) {
       // bounded; on time-out the merge still waits (bounded again) so that
-      // no copy lands in the shared memory of an exited CTA
+      // no store lands in the shared memory of an exited CTA
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(merge_bar, 0, flags, kWaitLimitNs));
       if (!ok) {
         if (lane == 0 && !flags[0]) {
@@ -457,8 +479,42 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
         int never = 0;
         mbar_wait_bounded(merge_bar, 0, &never, kWaitLimitNs);
       }
-      attn_cluster_merge_local(cst, reinterpret_cast<const float*>(base + S::kRecv), cl,
-                               a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim, flags);
+      // One lane per (unit, rank): the ranks of a unit sit in an aligned
+      // group of ql lanes that takes the max and the sums by shuffles (a
+      // loop over the ranks on one thread per unit took 1.1 us at 8 ranks
+      // and 1.7-2.5 us at 16).  Fixed order: the results do not vary.
+      const int ql = cl <= 2 ? 2 : cl <= 4 ? 4 : cl <= 8 ? 8 : 16;
+      const float* rv = reinterpret_cast<const float*>(base + S::kRecv);
+      const int g = c / cl, b = g / n_kv, j = g % n_kv;
+      float* a_grp = a_out + ((int64_t)b * (kGroup * n_kv) + kGroup * j) * kHeadDim;
+      for (int i0 = 0; i0 < nu * ql; i0 += kCT) {  // the same trip count in every lane
+        const int i = i0 + tid, t = i / ql, q = i % ql;
+        const int u = u0 + t, h = u / 32;
+        const bool live = t < nu && q < cl;
+        float m = -INFINITY, l = 0.f;
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (live) {
+          const float* sq = q == r ? cst : rv + q * sf;
+          const float4* oq = reinterpret_cast<const float4*>(q == r ? cst + 8 + 8 * u : sq + 8 + 8 * t);
+          m = sq[h];
+          l = sq[4 + h];
+          x0 = oq[0];
+          x1 = oq[1];
+        }
+        float M = m;
+        for (int o = ql >> 1; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float sc = m == -INFINITY ? 0.f : exp2f(m - M);
+        float v[9] = {l * sc, x0.x * sc, x0.y * sc, x0.z * sc, x0.w * sc, x1.x * sc, x1.y * sc, x1.z * sc, x1.w * sc};
+        for (int o = ql >> 1; o > 0; o >>= 1)
+#pragma unroll
+          for (int k = 0; k < 9; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+        if (q == 0 && t < nu && !flags[0]) {
+          const float inv = 1.0f / v[0];
+          float4* dst = reinterpret_cast<float4*>(a_grp + 8 * u);
+          dst[0] = make_float4(v[1] * inv, v[2] * inv, v[3] * inv, v[4] * inv);
+          dst[1] = make_float4(v[5] * inv, v[6] * inv, v[7] * inv, v[8] * inv);
+        }
+      }
     }
     if (tid == 0) cta_stamp(trace, 5);
   }
@@ -519,8 +575,8 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
                      int64_t capacity, int ring_capacity, bool full, int window, float scale,
                      const int32_t* positions, int batch, float* a, float* part,
                      uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                     size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st) {
-  using S = Smem<CT, NS, NC, kRecvSlots<MINB>>;
+                     size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st, int* held) {
+  using S = Smem<CT, NS, NC, kRecvBytes<MINB>>;
   AttnArgs<MAXB> args;
   args.prefix[0] = 0;
   for (int b = 0; b < MAXB; ++b) {
@@ -565,6 +621,9 @@ cudaError_t launch_t(const float* q_rot, const void* kc, const void* vc, int n_k
   const int long_cl = MINB == 1 && dev >= 0 && dev < 64 ? long_clusters[dev] : 0;
   const AttnPlan plan = plan_attention<MINB>(total, max_rows, min_rows, batch * n_kv, n_ctas, max_ctas, long_cl);
   const int G = plan.ctas, cl = plan.cluster;
+  // one CTA per SM: G SMs; two per SM: where they land is the scheduler's
+  // choice, so every SM counts as held
+  if (held) *held = MINB == 1 && G < device_sm_count() ? G : device_sm_count();
 
   // a chunk's tokens share one sequence's cache; decode rows are per sequence
   const int64_t cache_rows = chunk.p0 >= 0 ? capacity : (int64_t)batch * capacity;
@@ -605,16 +664,16 @@ cudaError_t launch_ns(const float* q_rot, const void* kc, const void* vc, int n_
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                      size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st) {
+                      size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st, int* held) {
   if (batch <= 8)
     return launch_t<CT, NS, NC, MINB, 8>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                               positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
+                               positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st, held);
   if (batch <= 64)
     return launch_t<CT, NS, NC, MINB, 64>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
+                                positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st, held);
   return launch_t<CT, NS, NC, MINB, SPARK_MAX_BATCH>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full,
                                            window, scale, positions, batch, a, part, counters, err,
-                                           n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
+                                           n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st, held);
 }
 
 template <typename CT>
@@ -622,16 +681,16 @@ cudaError_t launch_ct(const float* q_rot, const void* kc, const void* vc, int n_
                       int64_t capacity, int ring_capacity, bool full, int window, float scale,
                       const int32_t* positions, int batch, float* a, float* part,
                       uint32_t* counters, uint32_t* err, int n_ctas, const void* l2_pf,
-                      size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st) {
+                      size_t l2_pf_bytes, const ChunkSrc& chunk, int max_ctas, cudaStream_t st, int* held) {
   int64_t rows = 0;
   for (int b = 0; b < batch; ++b) rows += window_of(positions[b], full, window, ring_capacity).rows;
   if ((int64_t)n_kv * rows >= kDeepRows)
     return launch_ns<CT, CacheT<CT>::kDeep, kConsumers, CacheT<CT>::kDeepBlocks>(
         q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale, positions, batch, a, part,
-        counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
+        counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st, held);
   return launch_ns<CT, CacheT<CT>::kShallow, kConsumers, 1>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
                                        scale, positions, batch, a, part, counters, err, n_ctas,
-                                       l2_pf, l2_pf_bytes, chunk, max_ctas, st);
+                                       l2_pf, l2_pf_bytes, chunk, max_ctas, st, held);
 }
 
 }  // namespace
@@ -656,13 +715,14 @@ cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, con
                              int window, float scale, const int32_t* positions, int batch,
                              float* a, float* part, uint32_t* counters, uint32_t* err,
                              int n_ctas, const void* l2_pf, size_t l2_pf_bytes, cudaStream_t st,
-                             const ChunkSrc& chunk, int max_ctas) {
+                             const ChunkSrc& chunk, int max_ctas, int* sms_held) {
   if (cdtype == SPARK_BF16)
     return launch_ct<__nv_bfloat16>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window,
                                     scale, positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk,
-                                    max_ctas, st);
+                                    max_ctas, st, sms_held);
   return launch_ct<float>(q_rot, kc, vc, n_kv, capacity, ring_capacity, full, window, scale,
-                          positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st);
+                          positions, batch, a, part, counters, err, n_ctas, l2_pf, l2_pf_bytes, chunk, max_ctas, st,
+                          sms_held);
 }
 
 namespace {

@@ -717,60 +717,6 @@ __device__ __forceinline__ void attn_cta_state(const MergeSmem& sm, float* cst) 
   dst[1] = make_float4(O[4], O[5], O[6], O[7]);
 }
 
-// Rank 0 of a cluster, warp h < 4: merge its own state and the cl - 1 states
-// the other ranks sent into `recv` (rank r at slot r - 1), in rank order, and
-// write head h of the group's output.
-__device__ __forceinline__ void attn_cluster_merge_local(const float* cst, const float* recv, int cl,
-                                                         float* a_head0, volatile int* flags) {
-  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kF = 8 + kGroup * kHeadDim;  // floats of a state
-  constexpr int kB = 8;                      // states per round (clusters of up to 16: two rounds)
-  float M = -INFINITY, L = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int q0 = 0; q0 < cl; q0 += kB) {
-    float mq[kB], lq[kB];
-    float4 x0[kB], x1[kB];
-#pragma unroll
-    for (int t = 0; t < kB; ++t) {
-      const int q = q0 + t;
-      if (q < cl) {
-        const float* st = q == 0 ? cst : recv + (q - 1) * kF;
-        mq[t] = st[h];
-        lq[t] = st[4 + h];
-        const float4* src = reinterpret_cast<const float4*>(st + 8 + h * kHeadDim + 8 * lane);
-        x0[t] = src[0];
-        x1[t] = src[1];
-      } else {
-        mq[t] = -INFINITY;
-        lq[t] = 0.f;
-        x0[t] = x1[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    float mb = M;
-#pragma unroll
-    for (int t = 0; t < kB; ++t) mb = fmaxf(mb, mq[t]);
-    const float rs = M == -INFINITY ? 0.f : exp2f(M - mb);  // rescale the rounds before
-    L *= rs;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) O[i] *= rs;
-    M = mb;
-#pragma unroll
-    for (int t = 0; t < kB; ++t) {
-      const float scl = mq[t] == -INFINITY ? 0.f : exp2f(mq[t] - M);
-      L = fmaf(lq[t], scl, L);
-      O[0] = fmaf(x0[t].x, scl, O[0]); O[1] = fmaf(x0[t].y, scl, O[1]);
-      O[2] = fmaf(x0[t].z, scl, O[2]); O[3] = fmaf(x0[t].w, scl, O[3]);
-      O[4] = fmaf(x1[t].x, scl, O[4]); O[5] = fmaf(x1[t].y, scl, O[5]);
-      O[6] = fmaf(x1[t].z, scl, O[6]); O[7] = fmaf(x1[t].w, scl, O[7]);
-    }
-  }
-  if (!flags[0]) {
-    const float inv = 1.0f / L;
-    float4* dst = reinterpret_cast<float4*>(a_head0 + h * kHeadDim + 8 * lane);
-    dst[0] = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-    dst[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
-  }
-}
-
 #endif  // __CUDACC__
 
 }  // namespace spark

@@ -60,6 +60,45 @@ __device__ __forceinline__ void dot_chunk<float>(uint4 w, const float4* xp, floa
   acc = ffma2(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), make_float2(x0.z, x0.w), acc);
 }
 
+// The same sum with the chunk's activations in registers (E/4 float4s).
+template <typename WT>
+__device__ __forceinline__ void dot_chunk_reg(uint4 w, const float4* x, float2& acc);
+
+template <>
+__device__ __forceinline__ void dot_chunk_reg<__nv_bfloat16>(uint4 w, const float4* x, float2& acc) {
+  acc = ffma2(bf16x2_to_f32x2(w.x), make_float2(x[0].x, x[0].y), acc);
+  acc = ffma2(bf16x2_to_f32x2(w.y), make_float2(x[0].z, x[0].w), acc);
+  acc = ffma2(bf16x2_to_f32x2(w.z), make_float2(x[1].x, x[1].y), acc);
+  acc = ffma2(bf16x2_to_f32x2(w.w), make_float2(x[1].z, x[1].w), acc);
+}
+
+template <>
+__device__ __forceinline__ void dot_chunk_reg<float>(uint4 w, const float4* x, float2& acc) {
+  acc = ffma2(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), make_float2(x[0].x, x[0].y), acc);
+  acc = ffma2(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), make_float2(x[0].z, x[0].w), acc);
+}
+
+// Eight warp sums at once: on entry lane l holds its term v[i] of sum i; on
+// exit v[0] on lane l is sum l / 4 (added in a fixed order).  The first three
+// rounds halve the values a lane keeps, exchanging the other half with the
+// lane 16, 8 and then 4 apart; two more rounds add over the remaining lanes:
+// 9 shuffles for eight sums instead of 40.
+__device__ __forceinline__ void warp_sums8(float (&v)[8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16, n = 4; o >= 4; o >>= 1, n >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float send = up ? v[i] : v[i + n];
+      const float keep = up ? v[i + n] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 // Four consecutive weight elements as fp32 (read-only path).
 __device__ __forceinline__ float4 load_w4(const float* w, int n) {
   return __ldg(reinterpret_cast<const float4*>(w + n));

@@ -14,9 +14,11 @@ cudaError_t launch_qkv_rope(int wdtype, int cdtype, const float* h, const void* 
                             float eps, const int32_t* positions, cudaStream_t st);
 
 // Head gate + o_proj + raw residual: out[b] = h[b] + W_o (a[b] * sigmoid(g[b])).
+// free_sms > 0: SMs the previous kernel leaves free while it runs (one
+// sequence: the grid is shaped so that most rows are requested on them).
 cudaError_t launch_oproj(int wdtype, const float* a, const float* g, const float* h,
                          const void* o_w, float* out, uint32_t* err, int hidden, int n_q, int batch,
-                         cudaStream_t st);
+                         cudaStream_t st, int free_sms = -1);
 
 // The rows a chunk of consecutive tokens of one sequence produces, staged
 // ([tokens][n_kv][head_dim] in the cache type) until attention has run.
@@ -31,13 +33,14 @@ struct ChunkSrc {
 // `positions` are the tokens' positions, the cache is one sequence's, and
 // rows at positions >= chunk.p0 come from the staged rows.  The grid never
 // exceeds max_ctas CTAs (`part` holds max_ctas + batch * n_kv partials).
+// sms_held (optional): the SMs the launch's CTAs hold until it ends.
 cudaError_t launch_attention(int cdtype, const float* q_rot, const void* kc, const void* vc,
                              int n_kv, int64_t capacity, int ring_capacity, bool full,
                              int window, float scale, const int32_t* positions, int batch,
                              float* a, float* part, uint32_t* counters, uint32_t* err,
                              int n_ctas, const void* l2_prefetch, size_t l2_prefetch_bytes,
                              cudaStream_t st, const ChunkSrc& chunk = ChunkSrc(),
-                             int max_ctas = kMaxAttnCtas);
+                             int max_ctas = kMaxAttnCtas, int* sms_held = nullptr);
 
 // The same attention for a chunk, grouped by query (attn_chunk.cu): one CTA
 // per (group of consecutive tokens, KV head) reads the union of the tokens'

@@ -337,7 +337,7 @@ def test_equal_long_histories_reuse_and_split_invariance(B):
 # stage 3: head gate + o_proj + residual
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("dtype,batch,path", [("bf16", 1, "auto"), ("bf16", 5, "auto"), ("f32", 2, "auto"),
+@pytest.mark.parametrize("dtype,batch,path", [("bf16", 1, "auto"), ("bf16", 2, "auto"), ("bf16", 5, "auto"), ("f32", 2, "auto"),
                                               ("bf16", 4, "auto"), ("bf16", 1, "mma"), ("bf16", 4, "gemv"),
                                               ("bf16", 64, "auto"), ("bf16", 130, "auto")])
 def test_gate_oproj_matches_oracle(B, dtype, batch, path):
