@@ -236,14 +236,25 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   const int64_t total = (int64_t)n_kv * args.prefix[batch];
   const int G = gridDim.x, c = blockIdx.x;
   int64_t f0, f1;
+  Share sh0{};  // cluster mode: where this CTA's share starts
+  int64_t pos0 = 0;  // cluster mode: the group's position
   if (cl > 0) {
     // cluster mode: the cl CTAs of a cluster split one group's rows evenly
-    // (a CTA may get none) and merge through DSMEM
+    // (a CTA may get none) and merge through DSMEM.  The group follows from
+    // the CTA's index, and its arguments are read together: the producer's
+    // first tile waits on these reads, and a search over the sequences
+    // (dependent reads of the argument block) held it back by ~1 us.
     const int g = c / cl, r = c % cl, b = g / n_kv, j = g % n_kv;
-    const int64_t rows_g = args.prefix[b + 1] - args.prefix[b];
-    const int64_t gs = (int64_t)n_kv * args.prefix[b] + j * rows_g;
+    const int64_t p_lo = args.prefix[b], p_hi = args.prefix[b + 1];
+    pos0 = args.pos[b];
+    const int64_t rows_g = p_hi - p_lo;
+    const int64_t gs = (int64_t)n_kv * p_lo + j * rows_g;
     f0 = gs + rows_g * r / cl;
     f1 = gs + rows_g * (r + 1) / cl;
+    sh0.f = f0;
+    sh0.f1 = f1;
+    sh0.b = b;
+    sh0.j = j;
   } else {
     f0 = total * c / G;
     f1 = total * (c + 1) / G;
@@ -263,12 +274,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     }
     uint32_t k = 0;
     bool ok = true, waited = false;
-    Share sh = share_begin(args, batch, n_kv, f0, f1);
+    Share sh = cl > 0 ? sh0 : share_begin(args, batch, n_kv, f0, f1);
     while (sh.f < sh.f1) {
       const int64_t rows = args.prefix[sh.b + 1] - args.prefix[sh.b];
       const int64_t gs = (int64_t)n_kv * args.prefix[sh.b] + sh.j * rows;
       const int64_t r0 = sh.f - gs, r1 = min(sh.f1, gs + rows) - gs;
-      const Rows w = rows_of(pos[sh.b], full != 0, window, ring_capacity, chunk_p0);
+      const Rows w = rows_of(cl > 0 ? pos0 : pos[sh.b], full != 0, window, ring_capacity, chunk_p0);
       for (int64_t r = r0; r < r1;) {
         int64_t e = min(r1, r + kTile);
         if (r < w.len_a && e > w.len_a) e = w.len_a;
@@ -330,7 +341,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
   constexpr bool kMma = std::is_same<CT, __nv_bfloat16>::value;
   const MergeSmem msm{ms, ls, os};
   uint32_t k = 0;
-  Share sh = share_begin(args, batch, n_kv, f0, f1);
+  Share sh = cl > 0 ? sh0 : share_begin(args, batch, n_kv, f0, f1);
   bool waited = false;
   AttnState st;
   MmaQ mq;
