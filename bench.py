@@ -143,16 +143,16 @@ def step_bytes(wl: synth.Workload) -> dict:
 # follows the rows read, so other workloads scale the captured ratio.
 TRAFFIC = {
     ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_584_768,
-    ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_035_264,
+    ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_047_040,
     ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_560_576,
-    ("full_bf16_b1_ctx131072", "attention_full"): 540_826_880,
-    ("full_bf16_b16_ctx512-32768", "attention_full"): 1_119_864_320,
+    ("full_bf16_b1_ctx131072", "attention_full"): 541_030_912,
+    ("full_bf16_b16_ctx512-32768", "attention_full"): 1_119_880_448,
 }
 # DRAM bytes per algorithmic byte of the attention kernel in two captures:
 # one sequence of 131072 rows (537 MB read), and the first 16 sequences of
 # the ragged 64-sequence batch (1.11 GB over contexts of 6568 to 28494 rows)
-ATTN_TRAFFIC_RATIO = 540_826_880 / 536_875_008
-ATTN_RAGGED_TRAFFIC_RATIO = 1_119_864_320 / 1_111_035_904
+ATTN_TRAFFIC_RATIO = 541_030_912 / 536_875_008
+ATTN_RAGGED_TRAFFIC_RATIO = 1_119_880_448 / 1_111_035_904
 # workloads whose attention scales the ragged capture (the same sequences' rows)
 RAGGED_ATTENTION = ("full+sliding_bf16_b64_ctx512-32768",)
 

@@ -42,8 +42,9 @@ constexpr int64_t kDeepRows = 1 << 16;        // rows (x KV heads) per call from
 // Cluster mode (short histories): up to 8 CTAs per group, about 64 rows
 // each, for groups of at most 1536 rows.  Measured against 96 rows per CTA:
 // default step 53.0 -> 52.7 us, 36-layer stack 0.944 -> 0.925 ms (its
-// 512-row sliding layers now take 8 CTAs instead of 6); for these short
-// histories clusters of up to 16 CTAs (non-portable size) were no faster.
+// 512-row sliding layers now take 8 CTAs instead of 6).  Launches whose
+// groups all fit as 16-CTA clusters (batch 1) take up to 16 CTAs of 32 rows
+// (plan_attention).
 constexpr int kMaxCluster = 8;
 // Long histories at small batch (more than kClusterMaxRows rows, few
 // groups): one cluster of kLongCluster CTAs per group (a non-portable
@@ -555,6 +556,15 @@ AttnPlan plan_attention(int64_t total, int64_t max_rows, int64_t min_rows, int g
   // merging through DSMEM (no partials in the workspace, no ticket).
   int cl = (int)((max_rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta);
   if (cl > kMaxCluster) cl = kMaxCluster;
+  // Groups few enough that they all fit as kLongCluster-CTA clusters at
+  // once (batch 1): half the rows per CTA, up to kLongCluster CTAs.  With
+  // the merge spread over the ranks, 16 CTAs of 32 rows beat 8 of 64 for
+  // the 513-row sliding layers: the 36-layer batch-1 step 776 -> 762 us.
+  if (MINB == 1 && cl >= 2 && groups <= long_clusters) {
+    const int half = kClusterRowsPerCta / 2;
+    const int cl_half = (int)((max_rows + half - 1) / half);
+    cl = cl_half < kLongCluster ? cl_half : kLongCluster;
+  }
   if (n_ctas > 0 || cl < 2 || max_rows > kClusterMaxRows ||
       (int64_t)groups * cl > device_sm_count() || (int64_t)groups * cl > max_ctas || MINB > 1)
     cl = 0;  // cluster mode only in the kernel of one CTA per SM (it holds the ranks' state slots)
