@@ -76,7 +76,8 @@ constexpr int kRecvBytes = MINB == 1 ? merge_recv_bytes_max() : 0;  // cluster m
 // at small batch: the two-layer batch-1 step 50.0 -> 49.1 us, the 36-layer one
 // 865 -> 859 us.  Batches of more than kEarlyTriggerBatch keep the late
 // trigger (64 sequences: 737.5 vs 740.7 us; at 64 short contexts 149.3 vs
-// 152.7 us).
+// 152.7 us).  With o_proj's column path, the late trigger at batch 1 cost
+// the 36-layer step 762 -> 794 us.
 constexpr int kEarlyTriggerBatch = 4;
 constexpr int kClusterRowsPerCta = 64;
 constexpr int64_t kClusterMaxRows = 1536;

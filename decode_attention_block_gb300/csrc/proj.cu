@@ -55,10 +55,11 @@ constexpr size_t kSmemBudget = SPARK_GEMV_SMEM_KB * 1024;
 // q_k_v_proj units (row pairs) each CTA requests before the dependency wait;
 // the rest go out once x is built.  Loads issued after a CTA-wide weight
 // stream wait for it: with every stage requested up front, h arrived 4.3 us
-// after the wait, with 6 (60 KB of 207 KB) after 2.5 us, and the launch
-// ended 1.5 us sooner (36-layer step at batch 1: 925 -> 910 us).  Holding
-// the whole share (21 units, 222 KB) instead of 16 stages did not help.
-constexpr int kQkvPre = 6;
+// after the wait, with 6 (60 KB of 207 KB) after 2.5 us.  Swept again after
+// o_proj's column path (its CTAs now leave the SMs sooner): 4 / 6 / 8 / 10 /
+// 12 / 16 units give the 36-layer batch-1 step 783 / 762 / 751-754 / 753 /
+// 759 / 768 us, and 8 is the best for the fp32 one-layer step too.
+constexpr int kQkvPre = 8;
 // o_proj rows per CTA whose residual is loaded with the activations
 constexpr int kOprojHRows = 64;
 // o_proj by columns (every row of the share resident, up to 2 sequences):
