@@ -142,8 +142,8 @@ def step_bytes(wl: synth.Workload) -> dict:
 # the profile summaries give each capture's command.  Attention traffic
 # follows the rows read, so other workloads scale the captured ratio.
 TRAFFIC = {
-    ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_584_768,
-    ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_047_040,
+    ("full+sliding_bf16_b1_pos700", "qkv_rope"): 31_586_240,
+    ("full+sliding_bf16_b1_pos700", "gate_oproj"): 21_047_232,
     ("full+sliding_bf16_b1_pos700", "decode_stack"): 113_560_576,
     ("full_bf16_b1_ctx131072", "attention_full"): 541_030_912,
     ("full_bf16_b16_ctx512-32768", "attention_full"): 1_119_880_448,
@@ -597,7 +597,6 @@ def time_oracle(wl: synth.Workload, budget_s: float) -> dict:
     elapsed = 0.0
     seqs = oracle_sequences(wl)
     done = False
-    passes = 0
     while not done:
         for li, spec in enumerate(wl.layers):
             w, caches = oracle_layer_sample(wl, li, seqs)
@@ -613,12 +612,12 @@ def time_oracle(wl: synth.Workload, budget_s: float) -> dict:
                     break
             if done:
                 break
-        passes += 1
     steps_per_s = (units / units_total) / elapsed
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(steps_per_s * wl.batch, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{units} (layer, sequence) decode units of the {units_total} of one step, over "
-                      f"sequences {seqs} ({elapsed:.1f} s, numpy float64, BLAS threads up to {cores} cores)"}
+            "sample": f"{units} timed (layer, sequence) decode units, in passes over the "
+                      f"{len(wl.layers) * len(seqs)} of sequences {seqs} (a step has {units_total}); "
+                      f"{elapsed:.1f} s, numpy float64, BLAS threads up to {cores} cores"}
 
 
 def time_oracle_prefill(wl: synth.Workload, m: int, budget_s: float) -> dict:
