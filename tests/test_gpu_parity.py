@@ -238,6 +238,17 @@ ATTN_CASES = [
     ("split_clusters_b2", True, 0, None, [5000, 5000], 0, "bf16"),
     ("split_clusters_b4", True, 0, None, [2000] * 4, 0, "bf16"),
     ("split_clusters_f32", True, 0, None, [4000], 0, "f32"),
+    # cluster mode at every cluster size the planner picks for short histories:
+    # batch 1 takes up to 16 CTAs of ~32 rows (70 rows: 3, 150: 5, 200: 7,
+    # 300: 10, 450: 15), larger batches up to 8 of ~64 (2 x 300: 5, ragged
+    # 3 x up to 130: 3); the merge then has idle lanes in its shuffle groups
+    ("cluster_b1_r70", True, 0, None, [69], 0, "bf16"),
+    ("cluster_b1_r150", True, 0, None, [149], 0, "bf16"),
+    ("cluster_b1_r200_f32", True, 0, None, [199], 0, "f32"),
+    ("cluster_b1_r300", True, 0, None, [299], 0, "bf16"),
+    ("cluster_b1_r450", True, 0, None, [449], 0, "bf16"),
+    ("cluster_b2_r300", True, 0, None, [299, 299], 0, "bf16"),
+    ("cluster_b3_ragged", True, 0, None, [129, 100, 60], 0, "bf16"),
     # equal groups that nearly fill the GPU: one CTA per (sequence, KV head), no merge
     ("whole_groups_b64_ring", False, 512, 512, [700] * 64, 0, "bf16"),
     ("whole_groups_b30_full", True, 0, None, [299] * 30, 0, "bf16"),
