@@ -33,6 +33,7 @@
 
 #include "attn_parts.cuh"
 #include "launch.h"
+#include "partition.h"
 
 namespace spark {
 namespace {
@@ -54,19 +55,10 @@ constexpr int kMaxCluster = 8;
 // CTAs stream the rows more slowly, 2.8 TB/s, but the merge tail shrinks).
 constexpr int kLongCluster = 16;
 constexpr int kStateBytes = (8 + kGroup * kHeadDim) * 4;  // a CTA's state: m[4], l[4], o[4][256]
-// Cluster mode merges a group's state spread over the ranks: rank r owns the
-// units [merge_unit0(r), merge_unit0(r + 1)) of o (a unit: 8 floats, one
-// lane's dims of one head) and receives from every other rank q, in slot q
-// of its receive area, that rank's m[4], l[4] and its values of those units.
-constexpr int kMergeUnits = kGroup * kHeadDim / 8;
-__host__ __device__ constexpr int merge_unit0(int r, int cl) { return kMergeUnits * r / cl; }
-__host__ __device__ constexpr int merge_slot_floats(int cl) { return 8 + 8 * ((kMergeUnits + cl - 1) / cl); }
-constexpr int merge_recv_bytes_max() {
-  int most = 0;
-  for (int cl = 2; cl <= kLongCluster; ++cl)
-    if (cl * merge_slot_floats(cl) * 4 > most) most = cl * merge_slot_floats(cl) * 4;
-  return most;
-}
+// Cluster mode merges a group's state spread over the ranks (partition.h:
+// merge_unit0, merge_owner, merge_slot_floats).
+static_assert(kMergeUnits * 8 == kGroup * kHeadDim, "a merge unit is 8 floats of the group's output");
+static_assert(kMergeMaxCluster >= kLongCluster && kMergeMaxCluster >= kMaxCluster, "the receive area covers every cluster");
 template <int MINB>
 constexpr int kRecvBytes = MINB == 1 ? merge_recv_bytes_max() : 0;  // cluster mode only with one CTA per SM
 // When the next kernel may launch: 0 = right after the dependency wait, 1 =
@@ -461,9 +453,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     const int sf = merge_slot_floats(cl);
     if (tid < kMergeUnits) {  // consumer thread u sends unit u (and m, l to rank u)
       const int u = tid;
-      int q = u * cl / kMergeUnits;  // the unit's owner
-      while (q + 1 < cl && merge_unit0(q + 1, cl) <= u) ++q;
-      while (merge_unit0(q, cl) > u) --q;
+      const int q = merge_owner(u, cl);
       if (q != r) {
         const uint32_t bar = cluster_addr(merge_bar, (uint32_t)q);
         const uint32_t dst = cluster_addr(base + S::kRecv + (r * sf + 8 + 8 * (u - merge_unit0(q, cl))) * 4, (uint32_t)q);

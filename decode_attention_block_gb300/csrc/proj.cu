@@ -38,6 +38,7 @@
 #include "checks.h"
 #include "gemv_parts.cuh"
 #include "launch.h"
+#include "partition.h"
 
 namespace spark {
 namespace {
@@ -62,32 +63,13 @@ constexpr size_t kSmemBudget = SPARK_GEMV_SMEM_KB * 1024;
 constexpr int kQkvPre = 8;
 // o_proj rows per CTA whose residual is loaded with the activations
 constexpr int kOprojHRows = 64;
-// o_proj by columns (every row of the share resident, up to 2 sequences):
+// o_proj by columns (bf16 weights, every row of the share resident, up to 2 sequences):
 // each thread keeps its own weight chunks' activations in registers, so the
 // activation vector is read once instead of once per row pair
 constexpr int kOprojColRows = 32;                 // most rows of a share
 constexpr int kOprojColMaxQ = 4096;               // q_dim of the register slice
 constexpr size_t kOprojEarlyBudget = 220 * 1024;  // shared memory of a CTA shaped to the free SMs
 
-// Rows [r0, r1) of o_proj computed by CTA i of `grid`.  early > 0: the first
-// `early` CTAs (those that find a free SM at launch) take early_rows rows each
-// and the rest share the remaining rows evenly; early == 0: an even split.
-__host__ __device__ inline void oproj_share(int hidden, int grid, int early, int early_rows, int i, int& r0,
-                                            int& r1) {
-  if (early <= 0 || early >= grid) {
-    r0 = (int)((int64_t)hidden * i / grid);
-    r1 = (int)((int64_t)hidden * (i + 1) / grid);
-    return;
-  }
-  if (i < early) {
-    r0 = i * early_rows;
-    r1 = r0 + early_rows;
-    return;
-  }
-  const int base = early * early_rows, late = grid - early;
-  r0 = base + (int)((int64_t)(hidden - base) * (i - early) / late);
-  r1 = base + (int)((int64_t)(hidden - base) * (i - early + 1) / late);
-}
 
 template <int NB>
 struct QkvArgs {
