@@ -32,17 +32,19 @@ struct CacheT;
 // q.k / p.v FMA chains left the issue slots 60% idle, and a second CTA fills
 // them (measured 75% -> 90% of HBM peak at 131072 rows; one CTA with eight
 // consumer warps did not help, its single producer serialising on the ring).
-// Short histories take one CTA per SM, with an 8-stage bf16 ring: at batch 1
-// a CTA's share is 4-6 tiles (512-701 rows over 8 CTAs per KV head), so every
-// tile is requested before the dependency wait and none waits for a stage to
-// be refilled (4 stages: the two-layer batch-1 step 48.8 vs 47.2 us, the
-// 36-layer one 824.7 vs 806.5 us; large batches unchanged).
+// Short histories and batch-1 long ones take one CTA per SM, with a 12-stage
+// bf16 ring: a short history's share (2-6 tiles) is requested before the
+// dependency wait and no stage is refilled (4 stages instead of 8: the
+// two-layer batch-1 step 48.8 vs 47.2 us, the 36-layer one 824.7 vs 806.5
+// us), and a 16-CTA cluster's 32 tiles of an 8192-row layer keep more in
+// flight (8 stages instead of 12: the 36-layer step 740.3 vs 733.5 us, once
+// the cluster merge's receive area had shrunk to 5 KB).
 template <>
 struct CacheT<__nv_bfloat16> {
   static constexpr int kLineElems = 64;
   static constexpr int kDeep = 4;
   static constexpr int kDeepBlocks = 2;  // CTAs per SM
-  static constexpr int kShallow = 8;
+  static constexpr int kShallow = 12;
   static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
 template <>
