@@ -462,6 +462,14 @@ def test_decode_long_context_b8_ctx131072(B):
     run_workload_parity(B, WORKLOADS["full+sliding_bf16_b8_ctx131072"], sample=[0, 5])
 
 
+def test_decode_short_history_b1(B):
+    """One sequence at position 10 (11 rows): attention holds a handful of SMs,
+    so o_proj's grid is cut to the SMs left free (148 CTAs of 17-18 rows)."""
+    wl = synth.Workload("b1_short", "", "bf16", [10], [synth.LayerSpec(True, 0), synth.LayerSpec(False, 512)],
+                        seed=605)
+    run_workload_parity(B, wl)
+
+
 def test_decode_position_zero_and_small_batch_edges(B):
     wl = synth.Workload("edges", "", "bf16", [0, 1, 2, 513], [synth.LayerSpec(True, 0), synth.LayerSpec(False, 512)],
                         seed=600)
